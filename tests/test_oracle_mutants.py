@@ -1,0 +1,67 @@
+"""Plants plausible mistakes in copies of the oracle source and checks that the
+pins catch every one of them (no GPU needed).
+
+Each mutant is a textual edit of ``oracle/topk_oracle.cpp`` compiled into a
+temporary library; the committed oracle itself is never modified.
+"""
+
+import os
+
+import pytest
+
+import oracle
+import oracle_pins as P
+
+MUTANTS = {
+    # ranking reversed: worst scores selected
+    "ascending_order": ("if (a > b) return true;", "if (a < b) return true;"),
+    # signed zero ignored: -0 and +0 treated as equal
+    "no_signed_zero_rule": ("return !std::signbit(a) && std::signbit(b);", "return false;"),
+    # ties resolved by the highest index
+    "highest_index_ties": ("return i < j;", "return i > j;"),
+    # one selected slot too few
+    "m_off_by_one": ("const int64_t m = std::min<int64_t>(k, n);",
+                     "const int64_t m = std::min<int64_t>(k, n) - (n > 0 ? 1 : 0);"),
+    # padding written as 0 instead of -1
+    "padding_zero": ("for (int64_t j = m; j < k; ++j) out_row[j] = -1;",
+                     "for (int64_t j = m; j < k; ++j) out_row[j] = 0;"),
+    # page offset taken from the wrong operand
+    "page_offset_swapped": ("* page_size + idx % page_size;", "* page_size + idx / page_size;"),
+    # page number computed with the wrong operator
+    "page_number_modulo": ("const int64_t page = idx / page_size;",
+                           "const int64_t page = idx % page_size;"),
+    # negative lengths read as their magnitude
+    "negative_length_abs": ("if (len < 0) return 0;", "if (len < 0) return std::min<int64_t>(-static_cast<int64_t>(len), stride);"),
+    # length not clamped to the width: reads one row into the next
+    "length_clamp_off_by_one": ("return std::min<int64_t>(len, stride);",
+                                "return std::min<int64_t>(len, stride - 1);"),
+    # NaN inside the valid prefix accepted silently
+    "nan_accepted": ("if (std::isnan(row[i])) return ORACLE_ENAN;", "(void)row;"),
+}
+
+
+@pytest.fixture(scope="module")
+def source():
+    with open(oracle.source_path()) as f:
+        return f.read()
+
+
+def _build_variant(tmp_path, src_text, name):
+    src = tmp_path / f"{name}.cpp"
+    src.write_text(src_text)
+    lib = tmp_path / f"lib{name}.so"
+    oracle.build(str(src), str(lib))
+    return oracle.Oracle(str(lib))
+
+
+def test_unmutated_copy_passes(tmp_path, source):
+    P.run_all_pins(_build_variant(tmp_path, source, "clean"), quick=True)
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(tmp_path, source, name):
+    before, after = MUTANTS[name]
+    assert source.count(before) == 1, f"mutation anchor for {name} not found exactly once"
+    orc = _build_variant(tmp_path, source.replace(before, after), name)
+    with pytest.raises((AssertionError, RuntimeError)):
+        P.run_all_pins(orc, quick=True)
