@@ -1,0 +1,162 @@
+/*
+ * topk_indexer.h - C ABI of the GB300 (sm_103a) batched, ragged, exact per-row
+ * top-k over FP32 sparse-attention indexer scores.
+ *
+ * The operation (vLLM PR 56346 "sampled filtering", 执行摘要 and 实现拆解 1-3;
+ * sglang PR 39648 report, topk.py docstring of the paged top-k transform):
+ *
+ *   for every row b in [0, B):
+ *     n_b  = clamp(lengths[b], 0, stride)      negative length = no token,
+ *                                              a length past the width is clamped
+ *     m_b  = min(k, n_b)
+ *     out[b, 0 .. m_b)  = the indices (in [0, n_b)) of the m_b largest scores of
+ *                         scores[b, 0 .. n_b), as a set; the order of the slots
+ *                         is unspecified (this library writes them in ascending
+ *                         index order, the same order on every call)
+ *     out[b, m_b .. k)  = -1
+ *
+ *   Ranking is the float order with -0 below +0; -inf and +inf are ordinary
+ *   scores, so -inf outranks the -1 padding (sglang PR 39648 report,
+ *   功能与动机). The selected value multiset is exact: it equals the m_b largest
+ *   scores bit for bit (vLLM issue "persistent_topk silently drops top-k
+ *   candidates ...", 验证方法). Among scores equal to the m_b-th largest the
+ *   lowest indices are taken; any tie rule would meet the contract, this one is
+ *   fixed so that results are deterministic.
+ *
+ *   Capacity never truncates a row (the failure documented by that issue,
+ *   原因分析, and by sglang PR 37625): an internal candidate buffer that fills up
+ *   is compacted to the exact top candidates seen so far, and a sampled cutoff
+ *   that keeps fewer than m_b candidates makes the row be scanned again in full.
+ *
+ * Preconditions that are not checked (they would need a device read):
+ *   - no NaN in scores[b, 0 .. n_b); values past n_b are never read;
+ *   - paged: every mapped slot fits in int32 (see topk_paged).
+ *
+ * Memory and execution:
+ *   - every pointer is a DEVICE pointer owned by the caller; the library keeps
+ *     no reference after the call returns and allocates nothing per call;
+ *   - the call only enqueues work on `stream` (0 = legacy default stream) of
+ *     the current CUDA device and never synchronises; results are valid once
+ *     that stream reaches this point;
+ *   - `scores` needs 4-byte alignment only (rows may start at any float);
+ *     `lengths`, `out` and `page_table` need 4-byte alignment;
+ *   - `out` must not overlap any input.
+ *
+ * Errors: argument checks run before anything is enqueued; on any error other
+ * than TOPK_ECUDA nothing is written. TOPK_ECUDA reports a failed CUDA runtime
+ * call (launch, attribute query or set); the library never aborts the process.
+ * A device-side wait that exceeds its time limit (never reached by a correct
+ * launch) fills that row of `out` with TOPK_DEVICE_ERROR_INDEX instead of
+ * hanging.
+ */
+#ifndef TOPK_INDEXER_H_
+#define TOPK_INDEXER_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; declared here so the header needs no CUDA include. */
+typedef struct CUstream_st* topk_stream_t;
+
+typedef enum topk_status {
+  TOPK_OK = 0,
+  TOPK_EINVAL = 1,          /* null pointer, misalignment, negative B, bad stride/page size */
+  TOPK_EUNSUPPORTED_K = 2,  /* k outside [1, TOPK_MAX_K] */
+  TOPK_ECUDA = 3,           /* a CUDA runtime call failed */
+  TOPK_EDEVICE = 4          /* no usable sm_103 device is current */
+} topk_status;
+
+/* Largest supported k. The decode-step indexer uses k = 512, 1024 or 2048. */
+#define TOPK_MAX_K 2048
+
+/* Written into every slot of a row whose device-side wait timed out. */
+#define TOPK_DEVICE_ERROR_INDEX ((int32_t)0x80000000)
+
+/*
+ * topk_ragged - indices of the k largest scores of every row.
+ *
+ *   scores   [B, stride] float32, row-major: row b starts at scores + b * stride
+ *   stride   elements between consecutive rows, >= 1; also the row width
+ *   lengths  [B] int32 valid lengths (clamped to [0, stride])
+ *   B        number of rows, >= 0 (0 is a no-op)
+ *   k        slots per row, 1 <= k <= TOPK_MAX_K
+ *   out      [B, k] int32, contiguous; receives the indices and -1 padding
+ *   stream   CUDA stream to enqueue on
+ *
+ * Returns TOPK_OK, or an error code as described above.
+ */
+topk_status topk_ragged(const float* scores, int64_t stride, const int32_t* lengths, int32_t B,
+                        int32_t k, int32_t* out, topk_stream_t stream);
+
+/*
+ * topk_paged - as topk_ragged, with each selected index i of row b written as
+ *   page_table[b * pt_stride + i / page_size] * page_size + i % page_size
+ * (sglang PR 39648 report, topk.py docstring, and its PageTransform epilogue);
+ * the -1 slots stay -1. The product is formed in 64-bit and narrowed to int32.
+ *
+ *   page_table  [B, pt_stride] int32, row-major
+ *   pt_stride   entries per page-table row; must be >= ceil(stride / page_size)
+ *               so that every valid index has a page entry
+ *   page_size   tokens per page, >= 1 (any value; powers of two are not required)
+ */
+topk_status topk_paged(const float* scores, int64_t stride, const int32_t* lengths, int32_t B,
+                       int32_t k, const int32_t* page_table, int64_t pt_stride,
+                       int32_t page_size, int32_t* out, topk_stream_t stream);
+
+/* Static, human-readable description of a status code. */
+const char* topk_status_string(topk_status status);
+
+/* Version of this ABI (bumped on any incompatible change). */
+int32_t topk_abi_version(void);
+
+/*
+ * Test and diagnostic variant. Same operation and contract as topk_ragged /
+ * topk_paged (page_table == NULL selects the ragged output); the options only
+ * change which internal path each row takes, never the result. Zero-filled
+ * options mean "automatic", exactly like the plain calls.
+ *
+ *   sample_mode     0 automatic, 1 never use the sampled cutoff,
+ *                   2 use it on every row long enough to sample
+ *   cluster_size    0 automatic, 1 one CTA per row, or 2 / 4 / 8 CTAs of a
+ *                   thread-block cluster per row
+ *   stash_capacity  0 = default; otherwise the candidate-buffer size to use,
+ *                   in [k + 2048, default]: small values force the in-buffer
+ *                   compaction path on ordinary inputs
+ *   sample_z        0 = default margin; otherwise the number of standard
+ *                   deviations added to the sampled rank (negative values make
+ *                   the sampled cutoff too high and force the full rescan)
+ *   counters        optional DEVICE array of TOPK_NUM_COUNTERS uint32, which
+ *                   the kernel increments (see topk_counter); NULL = none
+ */
+typedef enum topk_counter {
+  TOPK_CNT_ROWS = 0,          /* rows handled */
+  TOPK_CNT_TRIVIAL = 1,       /* rows with length <= k (no selection needed) */
+  TOPK_CNT_SAMPLED = 2,       /* rows that streamed against a sampled cutoff */
+  TOPK_CNT_RESCAN = 3,        /* rows rescanned because the cutoff kept too few */
+  TOPK_CNT_COMPACTIONS = 4,   /* candidate-buffer compactions (summed over CTAs) */
+  TOPK_CNT_DEVICE_ERRORS = 5, /* CTAs whose waits timed out */
+  TOPK_CNT_CLUSTER_ROWS = 6,  /* rows split over a cluster of CTAs */
+  TOPK_NUM_COUNTERS = 8
+} topk_counter;
+
+typedef struct topk_debug_opts {
+  int32_t sample_mode;
+  int32_t cluster_size;
+  int32_t stash_capacity;
+  float sample_z;
+  uint32_t* counters;
+} topk_debug_opts;
+
+topk_status topk_select_ex(const float* scores, int64_t stride, const int32_t* lengths,
+                           int32_t B, int32_t k, const int32_t* page_table, int64_t pt_stride,
+                           int32_t page_size, int32_t* out, const topk_debug_opts* opts,
+                           topk_stream_t stream);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* TOPK_INDEXER_H_ */

@@ -1,0 +1,30 @@
+"""GB300 (sm_103a) batched, ragged, exact per-row top-k over FP32 indexer scores.
+
+Two calls, both enqueued on a CUDA stream and computed entirely by the
+library's CUDA kernels (``_build/libtopk_indexer.so``):
+
+* :func:`topk_ragged` - indices of each row's k largest scores, ``-1`` past
+  the row's length;
+* :func:`topk_paged` - the same indices mapped through a page table.
+
+PyTorch only provides device memory and streams.
+"""
+
+from ._binding import (  # noqa: F401
+    DEVICE_ERROR_INDEX,
+    LIB_PATH,
+    NUM_COUNTERS,
+    TOPK_MAX_K,
+    Counter,
+    Status,
+    TopkError,
+    load_library,
+    raw_library,
+    topk_paged,
+    topk_ragged,
+    topk_select_ex,
+)
+
+__all__ = ["topk_ragged", "topk_paged", "topk_select_ex", "TopkError", "Status", "Counter",
+           "load_library", "raw_library", "LIB_PATH", "TOPK_MAX_K", "NUM_COUNTERS",
+           "DEVICE_ERROR_INDEX"]

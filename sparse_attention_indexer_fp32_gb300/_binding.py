@@ -1,0 +1,182 @@
+"""ctypes binding of ``libtopk_indexer.so`` (argument marshalling only).
+
+Every step of the selection runs in the library's CUDA kernels; this module
+only checks tensor dtypes/devices/shapes, takes their device pointers and the
+current CUDA stream, and turns status codes into exceptions. There is no CPU
+fallback: without the built library every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import enum
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+LIB_PATH = _build.LIB
+
+TOPK_MAX_K = 2048
+DEVICE_ERROR_INDEX = -(2 ** 31)
+
+
+class Status(enum.IntEnum):
+    OK = 0
+    EINVAL = 1
+    EUNSUPPORTED_K = 2
+    ECUDA = 3
+    EDEVICE = 4
+
+
+class Counter(enum.IntEnum):
+    ROWS = 0
+    TRIVIAL = 1
+    SAMPLED = 2
+    RESCAN = 3
+    COMPACTIONS = 4
+    DEVICE_ERRORS = 5
+    CLUSTER_ROWS = 6
+
+
+NUM_COUNTERS = 8
+
+
+class TopkError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{message} (status {status})")
+        self.status = status
+
+
+class _DebugOpts(ctypes.Structure):
+    _fields_ = [("sample_mode", ctypes.c_int32), ("cluster_size", ctypes.c_int32),
+                ("stash_capacity", ctypes.c_int32), ("sample_z", ctypes.c_float),
+                ("counters", ctypes.c_void_p)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load_library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Loads the CUDA library (once). Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = path or LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"CUDA library not built: {path} is missing. Build it with "
+                "`python -m sparse_attention_indexer_fp32_gb300.build` "
+                "(nvcc, sm_103a).")
+        lib = ctypes.CDLL(path)
+        i64, i32, vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
+        lib.topk_ragged.argtypes = [vp, i64, vp, i32, i32, vp, vp]
+        lib.topk_ragged.restype = ctypes.c_int
+        lib.topk_paged.argtypes = [vp, i64, vp, i32, i32, vp, i64, i32, vp, vp]
+        lib.topk_paged.restype = ctypes.c_int
+        lib.topk_select_ex.argtypes = [vp, i64, vp, i32, i32, vp, i64, i32, vp,
+                                       ctypes.POINTER(_DebugOpts), vp]
+        lib.topk_select_ex.restype = ctypes.c_int
+        lib.topk_status_string.argtypes = [ctypes.c_int]
+        lib.topk_status_string.restype = ctypes.c_char_p
+        lib.topk_abi_version.restype = ctypes.c_int32
+        _lib = lib
+        return lib
+
+
+def _check(status: int) -> None:
+    if status != Status.OK:
+        msg = load_library().topk_status_string(status).decode()
+        raise TopkError(status, f"top-k call failed: {msg}")
+
+
+def _stream_handle(device: torch.device, stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return int(stream.cuda_stream)
+
+
+def _prepare(scores: torch.Tensor, lengths: torch.Tensor, k: int, out: Optional[torch.Tensor]):
+    if not isinstance(scores, torch.Tensor) or scores.dim() != 2:
+        raise ValueError("scores must be a 2-D tensor [B, stride]")
+    if not scores.is_cuda or scores.dtype != torch.float32 or not scores.is_contiguous():
+        raise ValueError("scores must be a contiguous float32 CUDA tensor")
+    B, stride = scores.shape
+    if lengths.dtype != torch.int32 or lengths.device != scores.device or lengths.numel() != B \
+            or not lengths.is_contiguous():
+        raise ValueError("lengths must be a contiguous int32 tensor [B] on the scores' device")
+    if out is None:
+        # an unsupported k is reported by the library itself (TOPK_EUNSUPPORTED_K)
+        out = torch.empty((B, max(int(k), 1)), dtype=torch.int32, device=scores.device)
+    elif (out.dtype != torch.int32 or out.device != scores.device
+          or tuple(out.shape) != (B, max(int(k), 1)) or not out.is_contiguous()):
+        raise ValueError("out must be a contiguous int32 tensor [B, k] on the scores' device")
+    return B, stride, out
+
+
+def topk_ragged(scores: torch.Tensor, lengths: torch.Tensor, k: int,
+                out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Indices of the ``min(k, lengths[b])`` largest scores of every row, ``-1`` after them.
+
+    ``scores`` float32 ``[B, stride]`` (CUDA, contiguous), ``lengths`` int32
+    ``[B]``. Returns ``out`` (int32 ``[B, k]``), enqueued on ``stream`` (default:
+    the current stream)."""
+    lib = load_library()
+    B, stride, out = _prepare(scores, lengths, k, out)
+    with torch.cuda.device(scores.device):
+        _check(lib.topk_ragged(scores.data_ptr(), stride, lengths.data_ptr(), B, k,
+                               out.data_ptr(), _stream_handle(scores.device, stream)))
+    return out
+
+
+def topk_paged(scores: torch.Tensor, lengths: torch.Tensor, k: int, page_table: torch.Tensor,
+               page_size: int, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """As :func:`topk_ragged`, each selected index ``i`` of row ``b`` written as
+    ``page_table[b, i // page_size] * page_size + i % page_size``."""
+    lib = load_library()
+    B, stride, out = _prepare(scores, lengths, k, out)
+    if (page_table.dtype != torch.int32 or page_table.device != scores.device
+            or page_table.dim() != 2 or page_table.shape[0] != B or not page_table.is_contiguous()):
+        raise ValueError("page_table must be a contiguous int32 tensor [B, pages] on the scores' device")
+    with torch.cuda.device(scores.device):
+        _check(lib.topk_paged(scores.data_ptr(), stride, lengths.data_ptr(), B, k,
+                              page_table.data_ptr(), page_table.shape[1], page_size,
+                              out.data_ptr(), _stream_handle(scores.device, stream)))
+    return out
+
+
+def topk_select_ex(scores: torch.Tensor, lengths: torch.Tensor, k: int,
+                   page_table: Optional[torch.Tensor] = None, page_size: int = 0,
+                   out: Optional[torch.Tensor] = None, *, sample_mode: int = 0,
+                   cluster_size: int = 0, stash_capacity: int = 0, sample_z: float = 0.0,
+                   counters: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Diagnostic variant: same result, with the internal path forced (see the
+    header's ``topk_debug_opts``). ``counters`` is an optional int32/uint32
+    CUDA tensor of ``NUM_COUNTERS`` entries that the kernel increments."""
+    lib = load_library()
+    B, stride, out = _prepare(scores, lengths, k, out)
+    pt_ptr, pt_stride = None, 0
+    if page_table is not None:
+        if page_table.dtype != torch.int32 or not page_table.is_contiguous():
+            raise ValueError("page_table must be contiguous int32")
+        pt_ptr, pt_stride = page_table.data_ptr(), page_table.shape[1]
+    opts = _DebugOpts(sample_mode, cluster_size, stash_capacity, sample_z,
+                      None if counters is None else counters.data_ptr())
+    if counters is not None and (counters.numel() < NUM_COUNTERS or not counters.is_cuda
+                                 or counters.element_size() != 4):
+        raise ValueError("counters must be a 4-byte CUDA tensor of NUM_COUNTERS entries")
+    with torch.cuda.device(scores.device):
+        _check(lib.topk_select_ex(scores.data_ptr(), stride, lengths.data_ptr(), B, k, pt_ptr,
+                                  pt_stride, page_size, out.data_ptr(), ctypes.byref(opts),
+                                  _stream_handle(scores.device, stream)))
+    return out
+
+
+def raw_library() -> ctypes.CDLL:
+    """The loaded ctypes library, for callers that pass raw pointers."""
+    return load_library()

@@ -1,0 +1,170 @@
+// C ABI of the sm_103a top-k library: argument checks, path selection and
+// kernel launches. See include/topk_indexer.h for the contract.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "topk_indexer.h"
+#include "topk_launch.cuh"
+
+namespace {
+
+using tki::Params;
+
+constexpr int kMaxDevices = 64;
+// Rows at least this long stream against a sampled cutoff by default.
+constexpr int kDefaultSampleMinN = 16384;
+// Default margin of the sampled rank, in standard deviations.
+constexpr float kDefaultSampleZ = 6.0f;
+// A cluster slice should hold at least this many scores to be worth a CTA.
+constexpr int64_t kMinClusterSlice = 16384;
+
+struct DeviceInfo {
+  std::once_flag once;
+  cudaError_t err = cudaSuccess;
+  bool supported = false;
+  int sm_count = 0;
+};
+DeviceInfo g_devices[kMaxDevices];
+
+// Device of the caller's current context, checked once per device for sm_103.
+topk_status device_info(int* dev, DeviceInfo** info) {
+  if (cudaGetDevice(dev) != cudaSuccess) return TOPK_ECUDA;
+  if (*dev < 0 || *dev >= kMaxDevices) return TOPK_EDEVICE;
+  DeviceInfo& d = g_devices[*dev];
+  std::call_once(d.once, [&]() {
+    int major = 0, minor = 0, sms = 0;
+    d.err = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, *dev);
+    if (d.err == cudaSuccess)
+      d.err = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, *dev);
+    if (d.err == cudaSuccess)
+      d.err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, *dev);
+    d.sm_count = sms;
+    d.supported = (major == 10 && minor == 3);
+  });
+  if (d.err != cudaSuccess) return TOPK_ECUDA;
+  if (!d.supported) return TOPK_EDEVICE;
+  *info = &d;
+  return TOPK_OK;
+}
+
+// CTAs per row: enough to occupy the GPU when the batch is small, as long as
+// every CTA still gets a long slice of the row.
+int auto_cluster_size(int32_t B, int64_t stride, int sm_count) {
+  const int64_t resident = 2LL * sm_count;  // two CTAs per SM
+  int G = 1;
+  while (G < 8 && static_cast<int64_t>(B) * (2 * G) <= resident &&
+         stride / (2 * G) >= kMinClusterSlice)
+    G *= 2;
+  return G;
+}
+
+bool aligned4(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 3u) == 0; }
+
+topk_status select_impl(const float* scores, int64_t stride, const int32_t* lengths, int32_t B,
+                        int32_t k, const int32_t* page_table, int64_t pt_stride, int32_t page_size,
+                        int32_t* out, const topk_debug_opts* opts, cudaStream_t stream) {
+  if (B < 0 || stride < 1 || stride > INT32_MAX) return TOPK_EINVAL;
+  if (k < 1 || k > TOPK_MAX_K) return TOPK_EUNSUPPORTED_K;
+  if (B == 0) return TOPK_OK;
+  if (scores == nullptr || lengths == nullptr || out == nullptr) return TOPK_EINVAL;
+  if (!aligned4(scores) || !aligned4(lengths) || !aligned4(out)) return TOPK_EINVAL;
+  if (page_table != nullptr) {
+    if (page_size < 1 || pt_stride < 1 || !aligned4(page_table)) return TOPK_EINVAL;
+    if (pt_stride < (stride + page_size - 1) / page_size) return TOPK_EINVAL;
+  }
+
+  const int kmax = k <= 512 ? 512 : (k <= 1024 ? 1024 : 2048);
+  const int cap_max = kmax <= 1024 ? tki::StashCap<1024>::value : tki::StashCap<2048>::value;
+
+  Params p = {};
+  p.scores = scores;
+  p.stride = stride;
+  p.lengths = lengths;
+  p.B = B;
+  p.k = k;
+  p.out = out;
+  p.page_table = page_table;
+  p.pt_stride = page_table != nullptr ? pt_stride : 0;
+  p.page_size = page_table != nullptr ? page_size : 1;
+  p.cap = cap_max;
+  p.sample_mode = 0;
+  p.sample_min_n = kDefaultSampleMinN;
+  p.sample_z = kDefaultSampleZ;
+  p.counters = nullptr;
+
+  int G = 0;
+  if (opts != nullptr) {
+    if (opts->sample_mode < 0 || opts->sample_mode > 2) return TOPK_EINVAL;
+    p.sample_mode = opts->sample_mode;
+    if (opts->stash_capacity != 0) {
+      if (opts->stash_capacity < k + tki::kStageFloats || opts->stash_capacity > cap_max)
+        return TOPK_EINVAL;
+      p.cap = opts->stash_capacity;
+    }
+    if (opts->sample_z != 0.0f) p.sample_z = opts->sample_z;
+    if (opts->cluster_size != 0) {
+      const int g = opts->cluster_size;
+      if (g != 1 && g != 2 && g != 4 && g != 8) return TOPK_EINVAL;
+      G = g;
+    }
+    if (opts->counters != nullptr && !aligned4(opts->counters)) return TOPK_EINVAL;
+    p.counters = opts->counters;
+  }
+
+  int dev = 0;
+  DeviceInfo* info = nullptr;
+  const topk_status st = device_info(&dev, &info);
+  if (st != TOPK_OK) return st;
+  if (G == 0) G = auto_cluster_size(B, stride, info->sm_count);
+  if (static_cast<int64_t>(B) * G > INT32_MAX) return TOPK_EINVAL;
+
+  switch (kmax) {
+    case 512: return tki::launch_k512(p, G, dev, stream);
+    case 1024: return tki::launch_k1024(p, G, dev, stream);
+    default: return tki::launch_k2048(p, G, dev, stream);
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+topk_status topk_ragged(const float* scores, int64_t stride, const int32_t* lengths, int32_t B,
+                        int32_t k, int32_t* out, topk_stream_t stream) {
+  return select_impl(scores, stride, lengths, B, k, nullptr, 0, 0, out, nullptr,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+topk_status topk_paged(const float* scores, int64_t stride, const int32_t* lengths, int32_t B,
+                       int32_t k, const int32_t* page_table, int64_t pt_stride, int32_t page_size,
+                       int32_t* out, topk_stream_t stream) {
+  if (page_table == nullptr && B > 0) return TOPK_EINVAL;
+  if (page_size < 1 || pt_stride < 1) return TOPK_EINVAL;
+  return select_impl(scores, stride, lengths, B, k, page_table, pt_stride, page_size, out,
+                     nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+topk_status topk_select_ex(const float* scores, int64_t stride, const int32_t* lengths, int32_t B,
+                           int32_t k, const int32_t* page_table, int64_t pt_stride,
+                           int32_t page_size, int32_t* out, const topk_debug_opts* opts,
+                           topk_stream_t stream) {
+  return select_impl(scores, stride, lengths, B, k, page_table, pt_stride, page_size, out, opts,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+const char* topk_status_string(topk_status status) {
+  switch (status) {
+    case TOPK_OK: return "success";
+    case TOPK_EINVAL: return "invalid argument (null or misaligned pointer, bad size or stride)";
+    case TOPK_EUNSUPPORTED_K: return "k outside [1, TOPK_MAX_K]";
+    case TOPK_ECUDA: return "a CUDA runtime call failed";
+    case TOPK_EDEVICE: return "current device is not an sm_103 GPU";
+    default: return "unknown status";
+  }
+}
+
+int32_t topk_abi_version(void) { return 1; }
+
+}  // extern "C"

@@ -1,0 +1,689 @@
+// Batched, ragged, exact per-row top-k over FP32 scores for sm_103a.
+//
+// One CTA (or one thread-block cluster of G CTAs) owns one row and reads it
+// from HBM once:
+//
+//  1. Order-preserving key. Each float's bit pattern becomes a uint32 whose
+//     unsigned order is the float order with -0 below +0 (the `ordered()`
+//     transform of vLLM PR 56346, 实现拆解 1).
+//  2. Sampled cutoff (DeepSelect-style filter of the same PR, 执行摘要 / 实现拆解 1).
+//     Long rows read 16 evenly spread chunks of 256 scores (4096 samples) and
+//     take, by two 11-bit radix-histogram passes in shared memory, a cutoff
+//     at rank  mu + z*sqrt(mu) + 1  of the sample, mu = k*4096/n, so that the
+//     cutoff sits below the row's k-th largest score with overwhelming
+//     probability while keeping a few thousand candidates.
+//  3. Streaming filter. The row body is brought into shared memory by a ring
+//     of 1-D bulk copies (TMA engine, cp.async.bulk + mbarrier); every score
+//     whose key clears the running threshold is appended, in index order, to
+//     a shared-memory stash of (key, index) pairs. Slots come from warp
+//     ballots and a per-stage block prefix (deterministic, no atomics).
+//  4. Compaction instead of truncation. When the stash would overflow, the
+//     exact top-k of the stash is found (below) and kept in place, and the
+//     threshold rises to just above the new cutoff. Nothing a later step
+//     could need is ever dropped, so overflow never loses candidates
+//     (the failure of vLLM issue "persistent_topk silently drops ...", 原因分析,
+//     and sglang PR 37625) and never costs another HBM pass.
+//  5. Underflow rescan. If the sampled cutoff was above the k-th largest
+//     score (fewer than k candidates survived), the row is streamed again with
+//     no cutoff (the full-row fallback of vLLM PR 56346, 执行摘要 "双回退兜底").
+//  6. Exact cutoff. Radix refinement of the stash keys: an 11-bit coarse
+//     histogram pass, then 11 and 10 bits under the found prefix (sglang PR
+//     37625's exact-key refinement, and `threshold()` of vLLM PR 56346), with
+//     early exit as soon as the remaining rank fills a whole bin.
+//  7. Emission. Keys strictly above the cutoff and the first r tied keys are
+//     written in stash (= index) order; the paged variant maps each index
+//     through the page table (sglang PR 39648's PageTransform epilogue).
+//
+// Cluster split (sglang PR 39648 report, 实现拆解 4): for batches too small to
+// fill the GPU, G CTAs of a cluster each stream a contiguous slice of the row
+// with their own stash; histograms are merged over distributed shared memory
+// so every CTA derives the same cutoffs, and per-CTA counts give each CTA its
+// output offsets.
+#pragma once
+
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace tki {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kStageFloats = 2048;                   // one ring stage: 8 KiB of scores
+constexpr int kVec = kStageFloats / (4 * kThreads);  // float4 per thread per stage
+constexpr int kStages = 6;                           // ring depth: 48 KiB
+constexpr int kSampleVec4 = 1024;                    // 4096 sampled scores ...
+constexpr int kSampleChunkVec4 = 64;                 // ... in 16 chunks of 256
+constexpr int kSampleChunks = kSampleVec4 / kSampleChunkVec4;
+constexpr int kBins = 2048;
+constexpr int kRoundEntries = 4 * kThreads;          // stash entries per emission round
+constexpr uint64_t kWaitLimitNs = 2000000000ull;     // 2 s: far beyond any stage latency
+
+static_assert(kVec == 2, "stage layout assumes two float4 per thread");
+
+// Counter slots of the optional diagnostics array (mirrors topk_counter).
+enum : int {
+  kCntRows = 0,
+  kCntTrivial = 1,
+  kCntSampled = 2,
+  kCntRescan = 3,
+  kCntCompactions = 4,
+  kCntDeviceErrors = 5,
+  kCntClusterRows = 6,
+};
+
+template <int KMAX>
+struct StashCap {
+  // Room for k kept candidates plus one full stage of new ones.
+  static constexpr int value = KMAX <= 1024 ? 4096 : 6144;
+};
+
+template <int C>
+struct __align__(128) Smem {
+  float ring[kStages][kStageFloats];
+  uint32_t skey[C];
+  uint32_t sidx[C];
+  uint32_t hist[kBins];
+  uint64_t full[kStages];
+  uint32_t stab[2][kVec * kWarps];  // per-stage per-warp hit counts; bit 31 = a wait timed out
+  uint32_t rtab[2][kWarps];         // per-round per-warp (above << 16 | tied) counts
+  uint32_t scan[kWarps];
+  uint32_t res[4];
+  uint32_t pub[4];                  // values the other CTAs of the cluster read
+};
+
+struct Params {
+  const float* scores;
+  int64_t stride;
+  const int32_t* lengths;
+  int32_t B;
+  int32_t k;
+  int32_t* out;
+  const int32_t* page_table;
+  int64_t pt_stride;
+  int32_t page_size;
+  int32_t cap;           // stash capacity in use, in [k + kStageFloats, C]
+  int32_t sample_mode;   // 0 automatic, 1 never, 2 whenever the row is long enough
+  int32_t sample_min_n;  // automatic sampling gate on the row length
+  float sample_z;        // standard deviations of margin on the sampled rank
+  uint32_t* counters;    // optional diagnostics
+};
+
+// Cutoff description: an entry is selected if (key >> shift) > P, or if
+// (key >> shift) == P and fewer than r such entries precede it.
+struct Cut {
+  uint32_t shift;
+  uint32_t P;
+  uint32_t r;
+};
+
+__device__ __forceinline__ uint32_t order_key(float x) {
+  const uint32_t u = __float_as_uint(x);
+  return u ^ (static_cast<uint32_t>(static_cast<int32_t>(u) >> 31) | 0x80000000u);
+}
+
+__device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, v, d);
+    if (lane >= d) v += y;
+  }
+  return v;
+}
+
+template <int C>
+__device__ __forceinline__ uint32_t block_incl_scan(uint32_t v, Smem<C>& S) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  v = warp_incl_scan(v);
+  if (lane == 31) S.scan[w] = v;
+  __syncthreads();
+  uint32_t add = 0;
+#pragma unroll
+  for (int i = 0; i < kWarps; ++i) add += (i < w) ? S.scan[i] : 0u;
+  return v + add;
+}
+
+// Warp-aggregated shared-memory histogram increment: lanes holding the same
+// bin combine into one atomic. `bin` = 0xffffffff means "no increment".
+// Every lane of the warp must call it.
+__device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t bin) {
+  const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+  const int lane = threadIdx.x & 31;
+  if (bin != 0xffffffffu && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+}
+
+// Locates the bin holding the target-th largest element (1 <= target <= total).
+// Thread t owns BPT consecutive bins, given in DESCENDING bin order in c[].
+// Returns the bin; *above = elements in higher bins; *inbin = elements in it.
+template <int BPT, int C>
+__device__ uint32_t find_bin(const uint32_t (&c)[BPT], uint32_t target, Smem<C>& S,
+                             uint32_t* above, uint32_t* inbin) {
+  constexpr int nbins = BPT * kThreads;
+  uint32_t s = 0;
+#pragma unroll
+  for (int i = 0; i < BPT; ++i) s += c[i];
+  const uint32_t incl = block_incl_scan(s, S);
+  uint32_t acc = incl - s;
+  if (acc < target && target <= incl) {
+#pragma unroll
+    for (int i = 0; i < BPT; ++i) {
+      if (acc < target && acc + c[i] >= target) {
+        S.res[0] = nbins - 1 - (BPT * threadIdx.x + i);
+        S.res[1] = acc;
+        S.res[2] = c[i];
+      }
+      acc += c[i];
+    }
+  }
+  __syncthreads();
+  *above = S.res[1];
+  *inbin = S.res[2];
+  return S.res[0];
+}
+
+// Reads this thread's BPT bins (descending), merged over the cluster when
+// G > 1, zeroes them, and finds the bin of the target-th largest element.
+// Must be called by every thread (of every CTA of the cluster) after the
+// histogram increments.
+template <int G, int BPT, int C>
+__device__ uint32_t merged_find(Smem<C>& S, uint32_t target, uint32_t* above, uint32_t* inbin) {
+  const int lo = (BPT * kThreads) - BPT * (threadIdx.x + 1);  // lowest owned bin
+  uint32_t c[BPT];
+  if constexpr (G == 1) {
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < BPT; ++i) {
+      c[i] = S.hist[lo + BPT - 1 - i];
+      S.hist[lo + BPT - 1 - i] = 0;  // only this thread reads or writes its bins here
+    }
+    return find_bin<BPT>(c, target, S, above, inbin);
+  } else {
+    cluster_sync();  // every CTA's histogram is complete
+#pragma unroll
+    for (int i = 0; i < BPT; ++i) c[i] = 0;
+    const uint32_t local = smem_addr(&S.hist[lo]);
+#pragma unroll 1
+    for (int r = 0; r < G; ++r) {
+      const uint32_t a = map_rank(local, r);
+#pragma unroll
+      for (int q = 0; q < BPT; q += 4) {
+        const uint4 v = ld_dsmem_v4(a + 4 * q);
+        c[BPT - 1 - q] += v.x;
+        c[BPT - 2 - q] += v.y;
+        c[BPT - 3 - q] += v.z;
+        c[BPT - 4 - q] += v.w;
+      }
+    }
+    const uint32_t bin = find_bin<BPT>(c, target, S, above, inbin);
+    cluster_sync();  // every CTA has read every histogram
+#pragma unroll
+    for (int i = 0; i < BPT; ++i) S.hist[lo + i] = 0;
+    __syncthreads();
+    return bin;
+  }
+}
+
+// Histogram of stash keys: entries e < n with (key >> fshift) == fval (all
+// entries when !filter) add one to bin (key >> dshift) & dmask.
+template <int C>
+__device__ void stash_hist(Smem<C>& S, int n, bool filter, uint32_t fshift, uint32_t fval,
+                           uint32_t dshift, uint32_t dmask) {
+  for (int base0 = 0; base0 < n; base0 += kRoundEntries) {
+    const int base = base0 + 4 * threadIdx.x;
+    uint4 k4 = make_uint4(0, 0, 0, 0);
+    if (base < n) k4 = *reinterpret_cast<const uint4*>(&S.skey[base]);
+    const uint32_t kv[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint32_t key = kv[c];
+      const bool ok = (base + c < n) && (!filter || (key >> fshift) == fval);
+      hist_add(S.hist, ok ? ((key >> dshift) & dmask) : 0xffffffffu);
+    }
+  }
+}
+
+// Exact cutoff of the target-th largest key over the stash (merged over the
+// cluster when G > 1). 1 <= target <= total entries.
+template <int G, int C>
+__device__ Cut select_stash(Smem<C>& S, int n, uint32_t target) {
+  uint32_t above, inbin;
+  stash_hist(S, n, false, 0, 0, 21, 0x7ff);
+  const uint32_t b1 = merged_find<G, 8>(S, target, &above, &inbin);
+  uint32_t rem = target - above;
+  if (rem == inbin) return Cut{21, b1, rem};
+  stash_hist(S, n, true, 21, b1, 10, 0x7ff);
+  const uint32_t b2 = merged_find<G, 8>(S, rem, &above, &inbin);
+  const uint32_t p2 = (b1 << 11) | b2;
+  rem -= above;
+  if (rem == inbin) return Cut{10, p2, rem};
+  stash_hist(S, n, true, 10, p2, 0, 0x3ff);
+  const uint32_t b3 = merged_find<G, 4>(S, rem, &above, &inbin);
+  rem -= above;
+  return Cut{0, (p2 << 10) | b3, rem};
+}
+
+// Walks stash entries [0, n) in order and calls sink(pos, key, idx) for each
+// selected one, pos = (#above-cut before it) + min(#tied before it, r), with
+// the counts starting at gt0 / eq0 (entries of lower-ranked cluster CTAs).
+// Safe for in-place compaction: pos never exceeds the entry's own position
+// and a round's entries are all read before any of them is written.
+template <int C, class Sink>
+__device__ void emit_rounds(Smem<C>& S, int n, Cut cut, uint32_t gt0, uint32_t eq0, Sink sink) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  uint32_t run_gt = gt0, run_eq = eq0;
+  int par = 0;
+  for (int base0 = 0; base0 < n; base0 += kRoundEntries, par ^= 1) {
+    const int base = base0 + 4 * threadIdx.x;
+    uint4 k4 = make_uint4(0, 0, 0, 0), i4 = make_uint4(0, 0, 0, 0);
+    if (base < n) {
+      k4 = *reinterpret_cast<const uint4*>(&S.skey[base]);
+      i4 = *reinterpret_cast<const uint4*>(&S.sidx[base]);
+    }
+    const uint32_t kv[4] = {k4.x, k4.y, k4.z, k4.w};
+    const uint32_t iv[4] = {i4.x, i4.y, i4.z, i4.w};
+    uint32_t gtm = 0, eqm = 0, pgt = 0, peq = 0, wgt = 0, weq = 0;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const bool valid = base + c < n;
+      const uint32_t hi = kv[c] >> cut.shift;
+      const bool gt = valid && hi > cut.P;
+      const bool eq = valid && hi == cut.P;
+      gtm |= static_cast<uint32_t>(gt) << c;
+      eqm |= static_cast<uint32_t>(eq) << c;
+      const uint32_t mg = __ballot_sync(0xffffffffu, gt);
+      const uint32_t me = __ballot_sync(0xffffffffu, eq);
+      pgt += __popc(mg & lt_mask);
+      peq += __popc(me & lt_mask);
+      wgt += __popc(mg);
+      weq += __popc(me);
+    }
+    if (lane == 0) S.rtab[par][w] = (wgt << 16) | weq;
+    __syncthreads();
+    const uint32_t e = lane < kWarps ? S.rtab[par][lane] : 0u;
+    const uint32_t incl = warp_incl_scan(e);
+    const uint32_t before = __shfl_sync(0xffffffffu, incl - e, w);
+    const uint32_t total = __shfl_sync(0xffffffffu, incl, kWarps - 1);
+    uint32_t gb = run_gt + (before >> 16) + pgt;
+    uint32_t eb = run_eq + (before & 0xffffu) + peq;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const bool gt = (gtm >> c) & 1u, eq = (eqm >> c) & 1u;
+      if (gt || (eq && eb < cut.r)) sink(gb + min(eb, cut.r), kv[c], iv[c]);
+      gb += gt;
+      eb += eq;
+    }
+    run_gt += total >> 16;
+    run_eq += total & 0xffffu;
+  }
+}
+
+template <int KMAX, int G>
+__global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) {
+  constexpr int C = StashCap<KMAX>::value;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  Smem<C>& S = *reinterpret_cast<Smem<C>*>(smem_raw);
+
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  const int row = static_cast<int>(blockIdx.x) / G;
+  const int rank = (G > 1) ? static_cast<int>(cluster_ctarank()) : 0;
+
+  const int64_t len_raw = p.lengths[row];
+  const int n = static_cast<int>(len_raw < 0 ? 0 : (len_raw > p.stride ? p.stride : len_raw));
+  int32_t* out_row = p.out + static_cast<int64_t>(row) * p.k;
+  const int32_t* pt_row =
+      p.page_table == nullptr ? nullptr : p.page_table + static_cast<int64_t>(row) * p.pt_stride;
+  const bool leader = (t == 0 && rank == 0);
+
+  auto map_index = [&](uint32_t i) -> int32_t {
+    if (pt_row == nullptr) return static_cast<int32_t>(i);
+    const uint32_t ps = static_cast<uint32_t>(p.page_size);
+    const uint32_t page = i / ps;
+    return static_cast<int32_t>(static_cast<int64_t>(pt_row[page]) * ps + (i - page * ps));
+  };
+
+  if (p.counters != nullptr && leader) {
+    atomicAdd(&p.counters[kCntRows], 1u);
+    if (G > 1) atomicAdd(&p.counters[kCntClusterRows], 1u);
+  }
+
+  // ---- rows with no more than k scores: every index is selected -----------
+  if (n <= p.k) {
+    for (int j = rank * kThreads + t; j < p.k; j += kThreads * G)
+      out_row[j] = (j < n) ? map_index(static_cast<uint32_t>(j)) : -1;
+    if (p.counters != nullptr && leader) atomicAdd(&p.counters[kCntTrivial], 1u);
+    return;  // uniform over the cluster: no cluster barrier has been used yet
+  }
+  const uint32_t kk = static_cast<uint32_t>(p.k);  // n > k: exactly k slots are filled
+  const uint32_t cap = static_cast<uint32_t>(p.cap);
+
+  // ---- row geometry: scalar head up to 16-byte alignment, bulk body, tail --
+  const float* rp = p.scores + static_cast<int64_t>(row) * p.stride;
+  const int mis = static_cast<int>((reinterpret_cast<uintptr_t>(rp) >> 2) & 3);
+  const int h = min((4 - mis) & 3, n);
+  const int nb = ((n - h) >> 2) << 2;
+  const int tail = n - h - nb;
+  const float* body = rp + h;
+  const int nstages = (nb + kStageFloats - 1) / kStageFloats;
+  const int s0 = static_cast<int>(static_cast<int64_t>(nstages) * rank / G);
+  const int s1 = static_cast<int>(static_cast<int64_t>(nstages) * (rank + 1) / G);
+
+  if (t == 0) {
+#pragma unroll
+    for (int s = 0; s < kStages; ++s) mbar_init(&S.full[s], 1);
+    fence_mbar_init();
+  }
+  for (int i = t; i < kBins; i += kThreads) S.hist[i] = 0;
+  __syncthreads();
+
+  // Ring bookkeeping. `issued` / `next_stage` live in thread 0; `consumed`
+  // is uniform over the CTA.
+  uint32_t issued = 0, consumed = 0, t0_seen = 0;
+  int next_stage = s0;
+  bool abort = false;
+
+  auto issue_one = [&]() {  // thread 0 only
+    const int j = next_stage++;
+    const int cnt = min(kStageFloats, nb - j * kStageFloats);
+    const uint32_t slot = issued++ % kStages;
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(&S.full[slot], static_cast<uint32_t>(cnt) * 4u);
+    bulk_load(&S.ring[slot][0], body + static_cast<int64_t>(j) * kStageFloats,
+              static_cast<uint32_t>(cnt) * 4u, &S.full[slot]);
+  };
+  auto prime = [&]() {
+    if (t == 0 && !abort) {
+      next_stage = s0;
+      while (next_stage < s1 && next_stage < s0 + kStages) issue_one();
+    }
+  };
+  prime();  // the first stages are in flight while the sample is examined
+
+  // ---- sampled cutoff -------------------------------------------------------
+  uint32_t thr = 0;
+  bool sampled = false;
+  {
+    const bool long_enough = nb >= 2 * 4 * kSampleVec4;
+    const bool want = long_enough && (p.sample_mode == 2 || (p.sample_mode == 0 && n >= p.sample_min_n));
+    uint32_t target = 0;
+    if (want) {
+      const float mu = static_cast<float>(kk) * (4.0f * kSampleVec4) / static_cast<float>(n);
+      float rf = ceilf(mu + p.sample_z * sqrtf(mu)) + 1.0f;
+      rf = fmaxf(rf, 1.0f);
+      if (rf < 4.0f * kSampleVec4) {
+        sampled = true;
+        target = static_cast<uint32_t>(rf);
+      }
+    }
+    if (sampled) {
+      const int nb4 = nb >> 2;
+      constexpr int per_rank = kSampleVec4 / G;
+      uint32_t sk[16];
+      uint32_t smask = 0;
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const int f = t + v * kThreads;
+        if (f < per_rank) {
+          const int gf = rank * per_rank + f;
+          const int chunk = gf / kSampleChunkVec4, within = gf % kSampleChunkVec4;
+          const int64_t off4 =
+              static_cast<int64_t>(chunk) * (nb4 - kSampleChunkVec4) / (kSampleChunks - 1) + within;
+          const float4 x = __ldg(reinterpret_cast<const float4*>(body) + off4);
+          sk[4 * v + 0] = order_key(x.x);
+          sk[4 * v + 1] = order_key(x.y);
+          sk[4 * v + 2] = order_key(x.z);
+          sk[4 * v + 3] = order_key(x.w);
+          smask |= 0xfu << (4 * v);
+        } else {
+          sk[4 * v + 0] = sk[4 * v + 1] = sk[4 * v + 2] = sk[4 * v + 3] = 0;
+        }
+      }
+      uint32_t above, inbin;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) hist_add(S.hist, ((smask >> i) & 1u) ? (sk[i] >> 21) : 0xffffffffu);
+      const uint32_t b1 = merged_find<G, 8>(S, target, &above, &inbin);
+      const uint32_t rem = target - above;
+      if (rem == inbin) {
+        thr = b1 << 21;
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const bool ok = ((smask >> i) & 1u) && (sk[i] >> 21) == b1;
+          hist_add(S.hist, ok ? ((sk[i] >> 10) & 0x7ffu) : 0xffffffffu);
+        }
+        const uint32_t b2 = merged_find<G, 8>(S, rem, &above, &inbin);
+        thr = (b1 << 21) | (b2 << 10);
+      }
+    }
+  }
+
+  // ---- streaming filter into the stash --------------------------------------
+  uint32_t n_st = 0;        // stash entries (uniform)
+  uint32_t grp = 0;         // groups processed (uniform), selects the count table half
+  uint32_t compactions = 0;
+
+  auto compact = [&]() {
+    const Cut cut = select_stash<1>(S, static_cast<int>(n_st), kk);
+    emit_rounds(S, static_cast<int>(n_st), cut, 0u, 0u, [&](uint32_t pos, uint32_t key, uint32_t idx) {
+      if (pos < kk) {  // exactly kk entries are selected; the guard only bounds a corrupted cut
+        S.skey[pos] = key;
+        S.sidx[pos] = idx;
+      }
+    });
+    __syncthreads();
+    n_st = kk;
+    thr = max(thr, (cut.P << cut.shift) + 1u);
+    ++compactions;
+  };
+
+  // Per-warp ballot counts of this thread's hits in each float4 group.
+  auto count_hits = [&](uint32_t pm, uint32_t (&below)[kVec], uint32_t (&wcnt)[kVec]) {
+#pragma unroll
+    for (int v = 0; v < kVec; ++v) {
+      const uint32_t nib = (pm >> (4 * v)) & 0xfu;
+      below[v] = 0;
+      wcnt[v] = 0;
+      if (__any_sync(0xffffffffu, nib != 0)) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t m = __ballot_sync(0xffffffffu, (nib >> c) & 1u);
+          below[v] += __popc(m & lt_mask);
+          wcnt[v] += __popc(m);
+        }
+      }
+    }
+  };
+  auto read_table = [&](int par, uint32_t (&base)[kVec], uint32_t& total, bool& any_err) {
+    uint32_t e = lane < kVec * kWarps ? S.stab[par][lane] : 0u;
+    any_err = __any_sync(0xffffffffu, e >> 31);
+    e &= 0x7fffffffu;
+    const uint32_t incl = warp_incl_scan(e);
+    total = __shfl_sync(0xffffffffu, incl, kVec * kWarps - 1);
+#pragma unroll
+    for (int v = 0; v < kVec; ++v) base[v] = __shfl_sync(0xffffffffu, incl - e, v * kWarps + w);
+  };
+
+  // Processes one group of up to 8 scores per thread: element (v, c) has key
+  // key[v][c], index idx[v] + c, and takes part if bit 4v+c of `valid` is set.
+  // Every thread of the CTA calls it; it contains block barriers.
+  auto process_group = [&](const uint32_t (&key)[kVec][4], uint32_t valid, const uint32_t (&idx)[kVec],
+                           bool err, bool refill) {
+    uint32_t pm = 0;
+#pragma unroll
+    for (int v = 0; v < kVec; ++v)
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        if (((valid >> (4 * v + c)) & 1u) && key[v][c] >= thr) pm |= 1u << (4 * v + c);
+    uint32_t below[kVec], wcnt[kVec];
+    count_hits(pm, below, wcnt);
+    const bool werr = __any_sync(0xffffffffu, err);
+    const int par = static_cast<int>(grp & 1u);
+    if (lane == 0) {
+#pragma unroll
+      for (int v = 0; v < kVec; ++v) S.stab[par][v * kWarps + w] = wcnt[v] | (werr ? 0x80000000u : 0u);
+    }
+    __syncthreads();  // this group's ring slot has been read by every thread
+    if (refill && t == 0 && next_stage < s1 && !abort) issue_one();
+    uint32_t base[kVec], total;
+    bool any_err;
+    read_table(par, base, total, any_err);
+    if (any_err) abort = true;
+    if (abort) {
+      ++grp;
+      return;
+    }
+    if (n_st + total > cap) {
+      compact();
+      pm = 0;
+#pragma unroll
+      for (int v = 0; v < kVec; ++v)
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          if (((valid >> (4 * v + c)) & 1u) && key[v][c] >= thr) pm |= 1u << (4 * v + c);
+      count_hits(pm, below, wcnt);
+      if (lane == 0) {
+#pragma unroll
+        for (int v = 0; v < kVec; ++v) S.stab[par][v * kWarps + w] = wcnt[v];
+      }
+      __syncthreads();
+      read_table(par, base, total, any_err);
+    }
+#pragma unroll
+    for (int v = 0; v < kVec; ++v) {
+      uint32_t pos = n_st + base[v] + below[v];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        if ((pm >> (4 * v + c)) & 1u) {
+          S.skey[pos] = key[v][c];
+          S.sidx[pos] = idx[v] + c;
+          ++pos;
+        }
+      }
+    }
+    n_st += total;
+    ++grp;
+  };
+
+  // Scalar group: thread t < cnt holds score at index first + t.
+  auto scalar_group = [&](int first, int cnt) {
+    uint32_t key[kVec][4] = {};
+    uint32_t idx[kVec] = {static_cast<uint32_t>(first + t), 0u};
+    uint32_t valid = 0;
+    if (t < cnt) {
+      key[0][0] = order_key(rp[first + t]);
+      valid = 1u;
+    }
+    process_group(key, valid, idx, false, false);
+  };
+
+  auto stream_pass = [&]() {
+    if (rank == 0 && h > 0) scalar_group(0, h);
+    for (int j = s0; j < s1; ++j) {
+      const uint32_t slot = consumed % kStages;
+      const uint32_t parity = (consumed / kStages) & 1u;
+      bool err = false;
+      if (!abort) {
+        err = !mbar_wait_bounded(&S.full[slot], parity, kWaitLimitNs);
+        if (!err) ++t0_seen;  // in order: stages [t0_seen, issued) are unobserved
+      }
+      const int cnt = min(kStageFloats, nb - j * kStageFloats);
+      uint32_t key[kVec][4];
+      uint32_t idx[kVec];
+      uint32_t valid = 0;
+#pragma unroll
+      for (int v = 0; v < kVec; ++v) {
+        const int f = v * kThreads + t;
+        idx[v] = static_cast<uint32_t>(h + j * kStageFloats + 4 * f);
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (4 * f < cnt) {
+          x = *reinterpret_cast<const float4*>(&S.ring[slot][4 * f]);
+          valid |= 0xfu << (4 * v);
+        }
+        key[v][0] = order_key(x.x);
+        key[v][1] = order_key(x.y);
+        key[v][2] = order_key(x.z);
+        key[v][3] = order_key(x.w);
+      }
+      ++consumed;
+      process_group(key, valid, idx, err, true);
+    }
+    if (rank == G - 1 && tail > 0) scalar_group(h + nb, tail);
+  };
+
+  stream_pass();
+
+  // ---- underflow: the sampled cutoff kept fewer than k candidates -----------
+  if (sampled) {
+    uint32_t total = n_st;
+    if constexpr (G > 1) {
+      if (t == 0) S.pub[0] = n_st;
+      cluster_sync();
+      total = 0;
+      for (int r = 0; r < G; ++r) total += ld_dsmem_u32(map_rank(smem_addr(&S.pub[0]), r));
+      cluster_sync();
+    }
+    if (total < kk) {  // uniform over the cluster
+      if (p.counters != nullptr && leader) atomicAdd(&p.counters[kCntRescan], 1u);
+      thr = 0;
+      n_st = 0;
+      prime();
+      stream_pass();
+    }
+  }
+
+  // ---- exact cutoff over the stash(es) and emission --------------------------
+  const Cut cut = select_stash<G>(S, static_cast<int>(n_st), kk);
+  uint32_t gt0 = 0, eq0 = 0;
+  if constexpr (G > 1) {
+    // Entries above / at the cutoff in this CTA's stash; lower ranks come first.
+    if (t == 0) {
+      S.pub[1] = 0;
+      S.pub[2] = 0;
+    }
+    __syncthreads();
+    uint32_t lg = 0, le = 0;
+    for (int e = t; e < static_cast<int>(n_st); e += kThreads) {
+      const uint32_t hi = S.skey[e] >> cut.shift;
+      lg += hi > cut.P;
+      le += hi == cut.P;
+    }
+    for (int d = 16; d > 0; d >>= 1) {
+      lg += __shfl_xor_sync(0xffffffffu, lg, d);
+      le += __shfl_xor_sync(0xffffffffu, le, d);
+    }
+    if (lane == 0) {
+      atomicAdd(&S.pub[1], lg);
+      atomicAdd(&S.pub[2], le);
+    }
+    cluster_sync();
+    for (int r = 0; r < rank; ++r) {
+      gt0 += ld_dsmem_u32(map_rank(smem_addr(&S.pub[1]), r));
+      eq0 += ld_dsmem_u32(map_rank(smem_addr(&S.pub[2]), r));
+    }
+  }
+  emit_rounds(S, static_cast<int>(n_st), cut, gt0, eq0,
+              [&](uint32_t pos, uint32_t, uint32_t idx) {
+                if (pos < kk) out_row[pos] = map_index(idx);
+              });
+
+  if constexpr (G > 1) cluster_sync();  // no CTA leaves while others may read its shared memory
+
+  if (p.counters != nullptr && t == 0) {
+    if (compactions) atomicAdd(&p.counters[kCntCompactions], compactions);
+    if (rank == 0 && sampled) atomicAdd(&p.counters[kCntSampled], 1u);
+  }
+  if (abort) {
+    // A wait timed out: let copies still in flight land (bounded), then mark
+    // the whole row as failed so the caller cannot mistake it for a result.
+    if (t == 0) {
+      for (uint32_t u = t0_seen; u < issued; ++u)
+        (void)mbar_wait_bounded(&S.full[u % kStages], (u / kStages) & 1u, kWaitLimitNs);
+      if (p.counters != nullptr) atomicAdd(&p.counters[kCntDeviceErrors], 1u);
+    }
+    for (int j = t; j < p.k; j += kThreads) out_row[j] = static_cast<int32_t>(0x80000000u);
+  }
+}
+
+}  // namespace tki

@@ -1,0 +1,68 @@
+// Launch of one kernel variant (k bucket x cluster size). Each k bucket is
+// instantiated in its own translation unit so the variants compile in parallel.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+
+#include "topk_indexer.h"
+#include "topk_kernel.cuh"
+
+namespace tki {
+
+// Per variant, bit d set once the kernel's shared-memory attribute is set on device d.
+template <int KMAX, int G>
+std::atomic<uint64_t>& attr_flags() {
+  static std::atomic<uint64_t> flags{0};
+  return flags;
+}
+
+template <int KMAX, int G>
+topk_status launch_variant(const Params& p, int dev, cudaStream_t stream) {
+  constexpr int C = StashCap<KMAX>::value;
+  auto kernel = topk_rows_kernel<KMAX, G>;
+  const size_t smem = sizeof(Smem<C>);
+  const uint64_t bit = 1ull << dev;
+  std::atomic<uint64_t>& flags = attr_flags<KMAX, G>();
+  if ((flags.load(std::memory_order_acquire) & bit) == 0) {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return TOPK_ECUDA;
+    flags.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.B) * G, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if (G > 1) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = G;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, kernel, p) == cudaSuccess ? TOPK_OK : TOPK_ECUDA;
+}
+
+template <int KMAX>
+topk_status launch_bucket(const Params& p, int G, int dev, cudaStream_t stream) {
+  switch (G) {
+    case 1: return launch_variant<KMAX, 1>(p, dev, stream);
+    case 2: return launch_variant<KMAX, 2>(p, dev, stream);
+    case 4: return launch_variant<KMAX, 4>(p, dev, stream);
+    case 8: return launch_variant<KMAX, 8>(p, dev, stream);
+    default: return TOPK_EINVAL;
+  }
+}
+
+// Defined in topk_k512.cu, topk_k1024.cu and topk_k2048.cu.
+topk_status launch_k512(const Params& p, int G, int dev, cudaStream_t stream);
+topk_status launch_k1024(const Params& p, int G, int dev, cudaStream_t stream);
+topk_status launch_k2048(const Params& p, int G, int dev, cudaStream_t stream);
+
+}  // namespace tki

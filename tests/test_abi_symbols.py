@@ -1,0 +1,68 @@
+"""The C-ABI library builds, loads and exports every function the header
+declares; host-side argument checks return their codes without a GPU."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import sparse_attention_indexer_fp32_gb300 as tk
+from sparse_attention_indexer_fp32_gb300 import build as cuda_build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "topk_indexer.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if cuda_build.is_stale():
+        cuda_build.build()
+    return tk.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(topk_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_two_calls():
+    names = declared_functions()
+    assert "topk_ragged" in names and "topk_paged" in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} missing from {cuda_build.LIB}"
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.topk_abi_version() == 1
+    for code in range(5):
+        assert lib.topk_status_string(code)
+    assert b"unknown" in lib.topk_status_string(99)
+
+
+def test_argument_checks_need_no_gpu(lib):
+    # All of these fail (or succeed, for B = 0) before any CUDA call.
+    P = ctypes.c_void_p
+    some = ctypes.c_void_p(0x1000)
+    assert lib.topk_ragged(some, 64, some, 0, 512, some, None) == tk.Status.OK
+    assert lib.topk_ragged(some, 64, some, 2, 0, some, None) == tk.Status.EUNSUPPORTED_K
+    assert lib.topk_ragged(some, 64, some, 2, 2049, some, None) == tk.Status.EUNSUPPORTED_K
+    assert lib.topk_ragged(some, 64, some, -1, 512, some, None) == tk.Status.EINVAL
+    assert lib.topk_ragged(some, 0, some, 2, 512, some, None) == tk.Status.EINVAL
+    assert lib.topk_ragged(P(None), 64, some, 2, 512, some, None) == tk.Status.EINVAL
+    assert lib.topk_ragged(ctypes.c_void_p(0x1002), 64, some, 2, 512, some, None) == tk.Status.EINVAL
+    assert lib.topk_paged(some, 64, some, 2, 512, P(None), 4, 16, some, None) == tk.Status.EINVAL
+    assert lib.topk_paged(some, 64, some, 2, 512, some, 4, 0, some, None) == tk.Status.EINVAL
+    assert lib.topk_paged(some, 64, some, 2, 512, some, 3, 16, some, None) == tk.Status.EINVAL
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    from sparse_attention_indexer_fp32_gb300 import _binding
+
+    monkeypatch.setattr(_binding, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        _binding.load_library(str(tmp_path / "missing.so"))

@@ -1,0 +1,246 @@
+"""Parity of the CUDA path with the CPU oracle (needs an sm_103 GPU).
+
+Every case runs the C ABI through the Python binding and compares with the
+oracle on the same seeded inputs: identical -1 pattern, identical index set
+(both take the lowest indices among ties at the cutoff, so the sets match even
+with ties), identical selected value multiset.
+"""
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from gpu_helpers import (assert_parity, check_against_oracle, counters_tensor, run_gpu,  # noqa: E402
+                         run_oracle, to_dev)
+from synth import make_rows, make_workload  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - CPU-only machines
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import sparse_attention_indexer_fp32_gb300 as tk  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    tk.load_library()
+
+
+# ---------------------------------------------------------------- workloads
+
+
+@pytest.mark.parametrize("config", [1, 2, 5])
+def test_workload_full(config):
+    w = make_workload(config)
+    check_against_oracle(w.scores, w.lengths, w.k)
+
+
+@pytest.mark.parametrize("config", [3, 4])
+def test_workload_leading_rows(config):
+    w = make_workload(config, B=48)
+    if w.paged:
+        check_against_oracle(w.scores, w.lengths, w.k, w.page_table, w.page_size)
+    check_against_oracle(w.scores, w.lengths, w.k)
+
+
+# ------------------------------------------------------------ forced paths
+
+
+def _mixed_rows():
+    """Rows of every workload kind at moderate width, with lengths that hit
+    the head/tail and stage boundaries."""
+    w2 = make_rows(2, [0, 1, 33, 40, 63])
+    w5 = make_rows(5, list(range(90, 108)))
+    stride = 70001
+    scores = np.full((w2.B + w5.B, stride), np.nan, dtype=np.float32)
+    lengths = np.zeros(w2.B + w5.B, dtype=np.int32)
+    for i in range(w2.B):
+        n = min(int(w2.lengths[i]), stride)
+        scores[i, :n] = w2.scores[i, :n]
+        lengths[i] = n
+    for i in range(w5.B):
+        n = min(max(int(w5.lengths[i]), 0), stride)
+        scores[w2.B + i, :n] = w5.scores[i, :n]
+        lengths[w2.B + i] = w5.lengths[i] if w5.lengths[i] < stride else stride + 17
+    return scores, lengths
+
+
+@pytest.mark.parametrize("k", [512, 1024, 2048])
+@pytest.mark.parametrize("sample_mode", [1, 2])
+@pytest.mark.parametrize("cluster", [1, 2, 4, 8])
+def test_forced_paths(k, sample_mode, cluster):
+    scores, lengths = _mixed_rows()
+    check_against_oracle(scores, lengths, k, sample_mode=sample_mode, cluster_size=cluster)
+
+
+@pytest.mark.parametrize("k", [512, 2048])
+@pytest.mark.parametrize("cluster", [1, 4])
+def test_compaction_path(k, cluster):
+    """Smallest candidate buffer: the in-buffer compaction runs many times."""
+    scores, lengths = _mixed_rows()
+    cnt = counters_tensor()
+    check_against_oracle(scores, lengths, k, sample_mode=1, cluster_size=cluster,
+                         stash_capacity=k + 2048, counters=cnt)
+    assert int(cnt[tk.Counter.COMPACTIONS]) > 0
+
+
+@pytest.mark.parametrize("cluster", [1, 2, 8])
+def test_underflow_rescan_path(cluster):
+    """A sampled cutoff set far too high keeps fewer than k candidates: every
+    sampled row must be rescanned and still come out exact."""
+    w = make_workload(3, B=8)
+    cnt = counters_tensor()
+    check_against_oracle(w.scores, w.lengths, w.k, sample_mode=2, sample_z=-1e4,
+                         cluster_size=cluster, counters=cnt)
+    assert int(cnt[tk.Counter.SAMPLED]) == 8
+    assert int(cnt[tk.Counter.RESCAN]) == 8
+
+
+def test_sampled_rows_are_counted():
+    w = make_workload(4, B=16)
+    cnt = counters_tensor()
+    check_against_oracle(w.scores, w.lengths, w.k, w.page_table, w.page_size, counters=cnt)
+    assert int(cnt[tk.Counter.ROWS]) == 16
+    assert int(cnt[tk.Counter.SAMPLED]) == 16
+    assert int(cnt[tk.Counter.DEVICE_ERRORS]) == 0
+
+
+# ------------------------------------------------------------ edge cases
+
+
+def test_capacity_boundaries_without_sampling():
+    """Row lengths around the candidate-buffer capacity: the buffer fills
+    exactly, one short of, and one past its end."""
+    rng = np.random.default_rng(11)
+    for k, cap in ((512, 4096), (1024, 4096), (2048, 6144)):
+        ns = [cap - 1, cap, cap + 1, cap + 2047, cap + 2048, cap + 2049, 2 * cap + 5]
+        stride = max(ns) + 3
+        scores = rng.standard_normal((len(ns), stride)).astype(np.float32)
+        lengths = np.array(ns, dtype=np.int32)
+        check_against_oracle(scores, lengths, k, sample_mode=1, cluster_size=1)
+
+
+def test_pages_capacity_boundaries():
+    """One narrow band holding the top scores with the populations the pages
+    report failures at (4096, 16384, 16385) and around them."""
+    rng = np.random.default_rng(3)
+    pops = [4095, 4096, 4097, 16384, 16385]
+    stride = 16385 + 7000
+    scores = np.full((len(pops), stride), np.nan, dtype=np.float32)
+    lengths = np.zeros(len(pops), dtype=np.int32)
+    for i, pop in enumerate(pops):
+        n = pop + 5000
+        x = rng.standard_normal(n).astype(np.float32) - 10.0
+        band = (np.uint32(0x3F800000) + rng.integers(0, 8193, pop).astype(np.uint32)).view(np.float32)
+        x[rng.permutation(n)[:pop]] = band
+        scores[i, :n] = x
+        lengths[i] = n
+    for k in (512, 2048):
+        check_against_oracle(scores, lengths, k)
+        check_against_oracle(scores, lengths, k, sample_mode=1)
+
+
+@pytest.mark.parametrize("offset", [0, 1, 2, 3])
+def test_unaligned_rows(offset):
+    """Row starts at every 4-byte offset from a 16-byte boundary; odd stride."""
+    rng = np.random.default_rng(offset)
+    B, stride = 6, 20011
+    flat = rng.standard_normal(B * stride + 4).astype(np.float32)
+    lengths = np.array([stride, 20000, 9999, 2049, 2050, 3], dtype=np.int32)
+    buf = to_dev(flat)
+    s = buf[offset: offset + B * stride].view(B, stride)
+    l = to_dev(lengths)
+    host = flat[offset: offset + B * stride].reshape(B, stride)
+    for k in (1, 17, 512, 2048):
+        out = tk.topk_ragged(s, l, k)
+        torch.cuda.synchronize()
+        assert_parity(host, lengths, k, out.cpu().numpy(), run_oracle(host, lengths, k))
+
+
+@pytest.mark.parametrize("k", [1, 2, 3, 100, 511, 513, 2047])
+def test_other_k_values(k):
+    w = make_rows(5, list(range(0, 128, 5)))
+    check_against_oracle(w.scores, w.lengths, k)
+
+
+def test_special_values():
+    rng = np.random.default_rng(8)
+    stride = 40000
+    rows = []
+    rows.append(np.full(stride, -np.inf))                      # all -inf
+    rows.append(np.full(stride, np.inf))                       # all +inf
+    x = np.zeros(stride); x[::2] = -0.0; rows.append(x)        # signed zeros
+    x = np.where(rng.random(stride) < 0.5, -0.0, 0.0); rows.append(x)
+    rows.append(np.full(stride, 7.25))                         # constant
+    x = np.arange(stride, dtype=np.float64)[::-1].copy(); rows.append(x)  # descending
+    x = rng.standard_normal(stride); x[12345] = np.inf; rows.append(x)
+    x = rng.uniform(65504, 1e6, stride); rows.append(x)        # above the fp16 range
+    x = np.full(stride, np.float32(3.4028235e38)); x[::3] = -np.float32(3.4028235e38); rows.append(x)
+    x = (np.float32(1.4e-45) * rng.integers(-3, 4, stride)); rows.append(x)  # subnormals
+    scores = np.stack([np.asarray(r, dtype=np.float32) for r in rows])
+    lengths = np.array([stride, 300, stride, 30000, stride, stride, stride, 31111, stride, stride],
+                       dtype=np.int32)
+    for k in (512, 1024, 2048):
+        for mode in (0, 1, 2):
+            check_against_oracle(scores, lengths, k, sample_mode=mode)
+
+
+def test_lengths_convention():
+    rng = np.random.default_rng(1)
+    stride = 5000
+    scores = rng.standard_normal((8, stride)).astype(np.float32)
+    lengths = np.array([-5, -1, 0, 1, 511, 512, 513, stride + 17], dtype=np.int32)
+    check_against_oracle(scores, lengths, 512)
+
+
+def test_empty_batch_is_a_noop():
+    s = torch.zeros((0, 128), dtype=torch.float32, device="cuda:0")
+    l = torch.zeros((0,), dtype=torch.int32, device="cuda:0")
+    out = tk.topk_ragged(s, l, 512)
+    assert out.shape == (0, 512)
+
+
+def test_paged_full_mapping():
+    w = make_workload(4, B=24)
+    got = run_gpu(w.scores, w.lengths, w.k, w.page_table, w.page_size)
+    want = run_oracle(w.scores, w.lengths, w.k, w.page_table, w.page_size)
+    assert_parity(w.scores, w.lengths, w.k, got, want, page_table=w.page_table)
+    # odd page size and short rows
+    rng = np.random.default_rng(2)
+    B, stride, ps = 5, 9000, 7
+    scores = rng.standard_normal((B, stride)).astype(np.float32)
+    lengths = np.array([9000, 700, 513, 512, 0], dtype=np.int32)
+    pt = rng.permutation(B * 1300).astype(np.int32).reshape(B, 1300)
+    check_against_oracle(scores, lengths, 512, pt, ps)
+
+
+def test_status_codes():
+    s = torch.zeros((2, 64), dtype=torch.float32, device="cuda:0")
+    l = torch.full((2,), 64, dtype=torch.int32, device="cuda:0")
+    for bad_k in (0, -1, 2049):
+        with pytest.raises(tk.TopkError) as e:
+            tk.topk_ragged(s, l, bad_k)
+        assert e.value.status == tk.Status.EUNSUPPORTED_K
+    pt = torch.zeros((2, 1), dtype=torch.int32, device="cuda:0")
+    with pytest.raises(tk.TopkError) as e:  # page table too narrow for the width
+        tk.topk_paged(s, l, 8, pt, 16)
+    assert e.value.status == tk.Status.EINVAL
+    with pytest.raises(tk.TopkError) as e:
+        tk.topk_select_ex(s, l, 8, stash_capacity=100)
+    assert e.value.status == tk.Status.EINVAL
+
+
+# ------------------------------------------------------------ determinism
+
+
+@pytest.mark.parametrize("config", [2, 5])
+def test_deterministic_over_100_calls(config):
+    w = make_workload(config)
+    s, l = to_dev(w.scores), to_dev(w.lengths)
+    first = tk.topk_ragged(s, l, w.k).clone()
+    for _ in range(99):
+        again = tk.topk_ragged(s, l, w.k)
+        assert torch.equal(first, again)
+    torch.cuda.synchronize()
