@@ -1,0 +1,437 @@
+"""Benchmark of the batched ragged exact top-k on GB300.
+
+One step = one call of the library on one batch of seeded synthetic scores
+already resident in HBM (all rows, the whole hot path: sampling, streaming
+filter, exact cutoff, emission). Default workload: B=1024 rows of width
+262144, lengths uniform in [0.8w, w], k=512, paged output (page_size 64); the
+B=1024 x 131072, k=2048 ragged workload is measured too and reported under
+"also". Prints ONE JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+``--impl reference`` times the CPU oracle (the reference arm of this build) on
+a bounded sample of the same workload instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "µs/call and scores-read GB/s (% of HBM peak) at B=1024, 80–100% ragged, k=512/2048"
+UNIT = "µs/call"
+FALLBACK_HBM_GBS = 6800.0
+# The pages' own B300 (GB300 GPU) warm latencies for the same B=1024 ragged
+# workloads (vLLM PR 56346, 执行摘要), context only.
+PAGE_LATENCY_US = {3: 207.06, 4: 301.72}
+WORKLOADS = {"w262144_k512_paged": 4, "w131072_k2048_ragged": 3}
+
+
+def kernel_source_hash() -> str:
+    csrc = os.path.join(ROOT, "sparse_attention_indexer_fp32_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            doc = json.load(f)
+    except (OSError, ValueError):
+        return None
+    entry = doc.get("workloads", {}).get(workload)
+    if not entry or doc.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+def algorithmic_bytes(lengths: np.ndarray, stride: int, B: int, k: int) -> int:
+    n = np.clip(lengths.astype(np.int64), 0, stride)
+    return int(n.sum() * 4 + B * k * 4)
+
+
+# ----------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.path is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+# ------------------------------------------------------------ distributed
+
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, local, world
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Largest value over all ranks (every rank gets it)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64,
+                     device=device if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------- GPU arm
+
+
+def time_device(fn, steps: int, warmup: int, world: int):
+    import torch
+
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(steps):
+        fn()
+    end.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    return start.elapsed_time(end)  # ms for all steps
+
+
+def bench_workload(config: int, steps: int, warmup: int, world: int, local: int, with_e2e: bool,
+                   e2e_steps: int, clocks: bool, rows=None):
+    import torch
+
+    import sparse_attention_indexer_fp32_gb300 as tk
+    from synth import make_workload
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = make_workload(config, B=rows)
+    s = torch.from_numpy(w.scores).to(dev)
+    l = torch.from_numpy(w.lengths).to(dev)
+    pt = None if w.page_table is None else torch.from_numpy(w.page_table).to(dev)
+    out = torch.empty((w.B, w.k), dtype=torch.int32, device=dev)
+    if pt is None:
+        fn = lambda: tk.topk_ragged(s, l, w.k, out=out)  # noqa: E731
+    else:
+        fn = lambda: tk.topk_paged(s, l, w.k, pt, w.page_size, out=out)  # noqa: E731
+
+    sampler = ClockSampler(torch.cuda.current_device()) if clocks else None
+    if sampler:
+        sampler.__enter__()
+    ms_total = time_device(fn, steps, warmup, world)
+    if sampler:
+        sampler.__exit__()
+    ms_total = max_over_ranks(ms_total, world, dev)
+    us_per_call = 1000.0 * ms_total / steps
+
+    algo = algorithmic_bytes(w.lengths, w.stride, w.B, w.k)
+    peak, peak_kind = measured_peak()
+    achieved = algo / (us_per_call * 1e-6) / 1e9
+    res = {
+        "workload": w.name,
+        "us_per_call": us_per_call,
+        "rows_per_s": w.B / (us_per_call * 1e-6),
+        "scores_read_gbs": (algo - w.B * w.k * 4) / (us_per_call * 1e-6) / 1e9,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": f"{peak_kind} hbm_gbs (burst copy)",
+                     "traffic": profiled_traffic(w.name),
+                     "algorithmic_bytes_per_launch": algo},
+        "config": {"workload": w.name, "B": w.B, "stride": w.stride, "k": w.k,
+                   "lengths": "uniform integer in [ceil(0.8*stride), stride]",
+                   "paged": pt is not None, "page_size": w.page_size or None,
+                   "scores_bytes": int(w.scores.nbytes),
+                   "l2": "inputs larger than L2 (no flush needed)"},
+        "gpu_launches": steps,
+        "sampler": sampler.summary() if sampler else None,
+    }
+    if with_e2e:
+        res["e2e"] = bench_e2e(w, dev, e2e_steps, world)
+    del s, l, pt, out
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_e2e(w, dev, steps: int, world: int):
+    """Same call through the public API with host buffers: every step copies the
+    inputs from pinned host memory to the device and reads the result back."""
+    import torch
+
+    import sparse_attention_indexer_fp32_gb300 as tk
+
+    hs = torch.from_numpy(w.scores).pin_memory()
+    hl = torch.from_numpy(w.lengths).pin_memory()
+    hpt = None if w.page_table is None else torch.from_numpy(w.page_table).pin_memory()
+    hout = torch.empty((w.B, w.k), dtype=torch.int32).pin_memory()
+    ds = torch.empty_like(hs, device=dev)
+    dl = torch.empty_like(hl, device=dev)
+    dpt = None if hpt is None else torch.empty_like(hpt, device=dev)
+    dout = torch.empty((w.B, w.k), dtype=torch.int32, device=dev)
+
+    def step():
+        ds.copy_(hs, non_blocking=True)
+        dl.copy_(hl, non_blocking=True)
+        if dpt is None:
+            tk.topk_ragged(ds, dl, w.k, out=dout)
+        else:
+            dpt.copy_(hpt, non_blocking=True)
+            tk.topk_paged(ds, dl, w.k, dpt, w.page_size, out=dout)
+        hout.copy_(dout, non_blocking=True)
+
+    ms = max_over_ranks(time_device(step, steps, 3, world), world, dev)
+    h2d = hs.nbytes + hl.nbytes + (0 if hpt is None else hpt.nbytes)
+    return {"value": 1000.0 * ms / steps, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(hout.nbytes), "steps": steps}
+
+
+def cpu_baseline(config: int, budget_s: float = 12.0, min_rows: int = 8):
+    """The CPU oracle as it stands (single thread) on a bounded sample of rows
+    of the same workload, scaled to the whole batch."""
+    import oracle
+    from synth import CONFIGS, make_rows
+
+    spec = CONFIGS[config]
+    orc = oracle.load()
+    rng = np.random.default_rng(0)
+    order = rng.permutation(spec.B)
+    done, elapsed = 0, 0.0
+    while done < spec.B and (elapsed < budget_s or done < min_rows):
+        rows = order[done: done + 8]
+        wk = make_rows(config, rows)
+        t0 = time.perf_counter()
+        if wk.page_table is None:
+            orc.topk_ragged(wk.scores, wk.lengths, wk.k)
+        else:
+            orc.topk_paged(wk.scores, wk.lengths, wk.k, wk.page_table, wk.page_size)
+        elapsed += time.perf_counter() - t0
+        done += len(rows)
+    us = 1e6 * elapsed / done * spec.B
+    return {"value": us, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{done} random rows of {spec.B} (single-threaded full sort per row), "
+                      f"{elapsed:.1f} s, scaled to the whole batch"}
+
+
+def run_gpu_arm(args):
+    rank, local, world = dist_setup(args.gpus)
+    primary = WORKLOADS[args.workload]
+    secondary = 3 if primary == 4 else 4
+    res = bench_workload(primary, args.steps, args.warmup, world, local, with_e2e=not args.quick,
+                         e2e_steps=args.e2e_steps, clocks=not args.quick, rows=args.rows)
+    also = None
+    if not args.quick:
+        also = bench_workload(secondary, max(args.steps // 2, 1), args.warmup, world, local,
+                              with_e2e=False, e2e_steps=0, clocks=False, rows=args.rows)
+    if rank != 0:
+        return
+    if args.quick:  # profiling runs: timing of the primary workload only
+        print(json.dumps({"quick": True, "workload": res["workload"], "B": res["config"]["B"],
+                          "us_per_call": res["us_per_call"], "roofline": res["roofline"]}),
+              flush=True)
+        return
+    clocks = res.pop("sampler")
+    also.pop("sampler")
+    line = {
+        "metric": METRIC,
+        "value": res["us_per_call"],
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": res["us_per_call"] / 1000.0,
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "u32",
+        "data": "synthetic (seeded Philox rows shaped like the decode-step indexer workload)",
+        "config": dict(res["config"], parallelism=f"replicas x{world}"),
+        "rows_per_s": res["rows_per_s"] * world,
+        "scores_read_gbs": res["scores_read_gbs"],
+        "roofline": res["roofline"],
+        "clocks": clocks,
+        "e2e": res["e2e"],
+        "gpu_launches": res["gpu_launches"],
+        "also": [{"workload": also["workload"], "us_per_call": also["us_per_call"],
+                  "rows_per_s": also["rows_per_s"], "scores_read_gbs": also["scores_read_gbs"],
+                  "roofline": also["roofline"], "config": also["config"],
+                  "steps": max(args.steps // 2, 1),
+                  "page_b300_us": PAGE_LATENCY_US.get(secondary)}],
+        "page_b300_us": PAGE_LATENCY_US.get(primary),
+        "kernel_source_hash": kernel_source_hash(),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(primary)
+    print(json.dumps(line), flush=True)
+
+
+def run_reference_arm(args):
+    """The oracle, as it stands, on the host cores: each step is a bounded
+    sample of rows of the same workload; the value is scaled to the batch."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    from synth import CONFIGS, make_rows
+
+    config = WORKLOADS[args.workload]
+    spec = CONFIGS[config]
+    orc = oracle.load()
+    rows_per_step = 1
+    rng = np.random.default_rng(1)
+    order = rng.permutation(spec.B)
+    # steps cycle through pre-drawn rows so that drawing is not timed
+    pool = make_rows(config, order[: min(spec.B, 16)])
+
+    def step(i):
+        j = i % pool.B
+        sl = slice(j, j + rows_per_step)
+        if pool.page_table is None:
+            orc.topk_ragged(pool.scores[sl], pool.lengths[sl], pool.k)
+        else:
+            orc.topk_paged(pool.scores[sl], pool.lengths[sl], pool.k, pool.page_table[sl],
+                           pool.page_size)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    elapsed = time.perf_counter() - t0
+    us = 1e6 * elapsed / (args.steps * rows_per_step) * spec.B
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1000.0 * elapsed / args.steps,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "u32",
+        "data": "synthetic (seeded Philox rows shaped like the decode-step indexer workload)",
+        "config": {"workload": spec.name, "B": spec.B, "stride": spec.stride, "k": spec.k,
+                   "paged": bool(spec.page_size), "page_size": spec.page_size or None,
+                   "parallelism": "none (host oracle)"},
+        "cpu_baseline": {"value": us, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{args.steps} steps of {rows_per_step} row each, cycling over "
+                                   f"{pool.B} random rows; scaled to the {spec.B}-row batch"},
+        "e2e": {"value": us, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="w262144_k512_paged")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rows", type=int, default=None,
+                    help="use only the first ROWS rows of the workload (profiling runs)")
+    ap.add_argument("--quick", action="store_true",
+                    help="primary workload only, no e2e / clocks / CPU baseline (profiling runs)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference_arm(args)
+    else:
+        run_gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -64,6 +64,18 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return true;
 }
 
+// Shared-memory fetch-and-add with acquire-release semantics at CTA scope:
+// accesses before it (by this thread, or ordered before it by __syncwarp)
+// happen-before accesses after the matching add in another thread.
+__device__ __forceinline__ uint32_t atom_add_acq_rel_cta(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;"
+               : "=r"(old)
+               : "r"(smem_addr(p)), "r"(v)
+               : "memory");
+  return old;
+}
+
 // ---- bulk copy (TMA, non-tensor) ------------------------------------------
 
 // Copies `bytes` (multiple of 16) from 16-byte aligned global memory into this

@@ -76,7 +76,7 @@ topk_status select_impl(const float* scores, int64_t stride, const int32_t* leng
   }
 
   const int kmax = k <= 512 ? 512 : (k <= 1024 ? 1024 : 2048);
-  const int cap_max = kmax <= 1024 ? tki::StashCap<1024>::value : tki::StashCap<2048>::value;
+  const int cap_max = kmax + tki::kStageFloats;  // tki::StashCap<kmax>::value
 
   Params p = {};
   p.scores = scores;

@@ -49,9 +49,9 @@ namespace tki {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kStageFloats = 2048;                   // one ring stage: 8 KiB of scores
-constexpr int kVec = kStageFloats / (4 * kThreads);  // float4 per thread per stage
-constexpr int kStages = 6;                           // ring depth: 48 KiB
+constexpr int kStageFloats = 4096;                     // one ring stage: 16 KiB of scores
+constexpr int kPerThread = kStageFloats / kThreads;    // 16 consecutive scores per thread
+constexpr int kStages = 3;                             // ring depth: 48 KiB
 constexpr int kSampleVec4 = 1024;                    // 4096 sampled scores ...
 constexpr int kSampleChunkVec4 = 64;                 // ... in 16 chunks of 256
 constexpr int kSampleChunks = kSampleVec4 / kSampleChunkVec4;
@@ -59,7 +59,7 @@ constexpr int kBins = 2048;
 constexpr int kRoundEntries = 4 * kThreads;          // stash entries per emission round
 constexpr uint64_t kWaitLimitNs = 2000000000ull;     // 2 s: far beyond any stage latency
 
-static_assert(kVec == 2, "stage layout assumes two float4 per thread");
+static_assert(kPerThread == 16, "stage layout assumes four float4 per thread");
 
 // Counter slots of the optional diagnostics array (mirrors topk_counter).
 enum : int {
@@ -75,7 +75,7 @@ enum : int {
 template <int KMAX>
 struct StashCap {
   // Room for k kept candidates plus one full stage of new ones.
-  static constexpr int value = KMAX <= 1024 ? 4096 : 6144;
+  static constexpr int value = KMAX + kStageFloats;
 };
 
 template <int C>
@@ -85,7 +85,9 @@ struct __align__(128) Smem {
   uint32_t sidx[C];
   uint32_t hist[kBins];
   uint64_t full[kStages];
-  uint32_t stab[2][kVec * kWarps];  // per-stage per-warp hit counts; bit 31 = a wait timed out
+  uint32_t rel[kStages];            // warps done with each ring slot (the last one refills it)
+  uint32_t issued;                  // stages issued into the ring (for the error drain)
+  alignas(16) uint32_t tab[2][kWarps];  // per-group per-warp hit counts; bit 31 = a wait timed out
   uint32_t rtab[2][kWarps];         // per-round per-warp (above << 16 | tied) counts
   uint32_t scan[kWarps];
   uint32_t res[4];
@@ -122,10 +124,26 @@ __device__ __forceinline__ uint32_t order_key(float x) {
   return u ^ (static_cast<uint32_t>(static_cast<int32_t>(u) >> 31) | 0x80000000u);
 }
 
+// Largest float b with  order_key(x) >= thr  =>  x >= b  (float compare).
+// Float comparison equates -0 and +0, so `x >= b` is a superset test that
+// lets the exact key comparison run only on the few scores that pass it.
+__device__ __forceinline__ float prefilter_bound(uint32_t thr) {
+  if (thr <= 0x007fffffu) return -__int_as_float(0x7f800000);  // every score passes: -inf
+  const uint32_t u = (thr & 0x80000000u) ? (thr ^ 0x80000000u) : ~thr;
+  return __uint_as_float(u);
+}
+
+__device__ __forceinline__ float4 pick4(const float4 (&v)[4], int j) {
+  return j == 0 ? v[0] : (j == 1 ? v[1] : (j == 2 ? v[2] : v[3]));
+}
+
+// Inclusive prefix sum over lanes [0, LANES) of the warp (lanes past LANES
+// receive partial sums).
+template <int LANES = 32>
 __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
+  for (int d = 1; d < LANES; d <<= 1) {
     const uint32_t y = __shfl_up_sync(0xffffffffu, v, d);
     if (lane >= d) v += y;
   }
@@ -144,13 +162,9 @@ __device__ __forceinline__ uint32_t block_incl_scan(uint32_t v, Smem<C>& S) {
   return v + add;
 }
 
-// Warp-aggregated shared-memory histogram increment: lanes holding the same
-// bin combine into one atomic. `bin` = 0xffffffff means "no increment".
-// Every lane of the warp must call it.
+// Shared-memory histogram increment; `bin` = 0xffffffff means "no increment".
 __device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t bin) {
-  const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-  const int lane = threadIdx.x & 31;
-  if (bin != 0xffffffffu && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+  if (bin != 0xffffffffu) atomicAdd(&hist[bin], 1u);
 }
 
 // Locates the bin holding the target-th largest element (1 <= target <= total).
@@ -192,10 +206,16 @@ __device__ uint32_t merged_find(Smem<C>& S, uint32_t target, uint32_t* above, ui
   uint32_t c[BPT];
   if constexpr (G == 1) {
     __syncthreads();
+    // Only this thread reads or writes its bins here.
+    uint4* h4 = reinterpret_cast<uint4*>(&S.hist[lo]);
 #pragma unroll
-    for (int i = 0; i < BPT; ++i) {
-      c[i] = S.hist[lo + BPT - 1 - i];
-      S.hist[lo + BPT - 1 - i] = 0;  // only this thread reads or writes its bins here
+    for (int q = 0; q < BPT; q += 4) {
+      const uint4 v = h4[q / 4];
+      h4[q / 4] = make_uint4(0, 0, 0, 0);
+      c[BPT - 1 - q] = v.x;
+      c[BPT - 2 - q] = v.y;
+      c[BPT - 3 - q] = v.z;
+      c[BPT - 4 - q] = v.w;
     }
     return find_bin<BPT>(c, target, S, above, inbin);
   } else {
@@ -244,11 +264,13 @@ __device__ void stash_hist(Smem<C>& S, int n, bool filter, uint32_t fshift, uint
 }
 
 // Exact cutoff of the target-th largest key over the stash (merged over the
-// cluster when G > 1). 1 <= target <= total entries.
+// cluster when G > 1). 1 <= target <= total entries. The coarse (key >> 21)
+// histogram of the stash is kept up to date by the inserts, so the first
+// pass only reads it. The histogram is all zero on return.
 template <int G, int C>
 __device__ Cut select_stash(Smem<C>& S, int n, uint32_t target) {
   uint32_t above, inbin;
-  stash_hist(S, n, false, 0, 0, 21, 0x7ff);
+  __syncthreads();  // the last stash writes of every thread are visible
   const uint32_t b1 = merged_find<G, 8>(S, target, &above, &inbin);
   uint32_t rem = target - above;
   if (rem == inbin) return Cut{21, b1, rem};
@@ -326,7 +348,6 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
   Smem<C>& S = *reinterpret_cast<Smem<C>*>(smem_raw);
 
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
-  const uint32_t lt_mask = (1u << lane) - 1u;
   const int row = static_cast<int>(blockIdx.x) / G;
   const int rank = (G > 1) ? static_cast<int>(cluster_ctarank()) : 0;
 
@@ -372,22 +393,25 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
 
   if (t == 0) {
 #pragma unroll
-    for (int s = 0; s < kStages; ++s) mbar_init(&S.full[s], 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&S.full[s], 1);
+      S.rel[s] = 0;
+    }
+    S.issued = 0;
     fence_mbar_init();
   }
   for (int i = t; i < kBins; i += kThreads) S.hist[i] = 0;
   __syncthreads();
 
-  // Ring bookkeeping. `issued` / `next_stage` live in thread 0; `consumed`
-  // is uniform over the CTA.
-  uint32_t issued = 0, consumed = 0, t0_seen = 0;
-  int next_stage = s0;
+  // Ring bookkeeping. Stage j of a pass goes to slot (pass start + j - s0) %
+  // kStages; `consumed` (stages taken from the ring so far) is uniform.
+  // Thread 0 fills the ring at the start of a pass; afterwards the last warp
+  // to finish with a slot refills it with the stage kStages further on.
+  uint32_t consumed = 0, t0_seen = 0;
   bool abort = false;
 
-  auto issue_one = [&]() {  // thread 0 only
-    const int j = next_stage++;
+  auto issue_stage = [&](int j, uint32_t slot) {  // one thread
     const int cnt = min(kStageFloats, nb - j * kStageFloats);
-    const uint32_t slot = issued++ % kStages;
     fence_proxy_async_smem();
     mbar_arrive_expect_tx(&S.full[slot], static_cast<uint32_t>(cnt) * 4u);
     bulk_load(&S.ring[slot][0], body + static_cast<int64_t>(j) * kStageFloats,
@@ -395,8 +419,20 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
   };
   auto prime = [&]() {
     if (t == 0 && !abort) {
-      next_stage = s0;
-      while (next_stage < s1 && next_stage < s0 + kStages) issue_one();
+      const int m = min(s1 - s0, kStages);
+      for (int u = 0; u < m; ++u) issue_stage(s0 + u, (consumed + u) % kStages);
+      S.issued += m;
+    }
+  };
+  // Called by every thread once it no longer reads ring slot `slot` (stage j).
+  auto release_slot = [&](int j, uint32_t slot) {
+    __syncwarp();
+    if (lane == 0 && atom_add_acq_rel_cta(&S.rel[slot], 1u) == kWarps - 1) {
+      S.rel[slot] = 0;
+      if (!abort && j + kStages < s1) {
+        issue_stage(j + kStages, slot);
+        atomicAdd(&S.issued, 1u);
+      }
     }
   };
   prime();  // the first stages are in flight while the sample is examined
@@ -463,6 +499,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
   uint32_t n_st = 0;        // stash entries (uniform)
   uint32_t grp = 0;         // groups processed (uniform), selects the count table half
   uint32_t compactions = 0;
+  float bound = prefilter_bound(thr);
 
   auto compact = [&]() {
     const Cut cut = select_stash<1>(S, static_cast<int>(n_st), kk);
@@ -470,115 +507,131 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
       if (pos < kk) {  // exactly kk entries are selected; the guard only bounds a corrupted cut
         S.skey[pos] = key;
         S.sidx[pos] = idx;
+        atomicAdd(&S.hist[key >> 21], 1u);  // coarse histogram of the kept entries
       }
     });
     __syncthreads();
     n_st = kk;
     thr = max(thr, (cut.P << cut.shift) + 1u);
+    bound = prefilter_bound(thr);
     ++compactions;
   };
 
-  // Per-warp ballot counts of this thread's hits in each float4 group.
-  auto count_hits = [&](uint32_t pm, uint32_t (&below)[kVec], uint32_t (&wcnt)[kVec]) {
+  // Exact hit mask: bit e set when score e of this thread's group (index
+  // order) has a key >= thr. `bound` is the float whose key is thr, so a float
+  // comparison is exact unless bound is a zero, where -0 < +0 must come from
+  // the keys.
+  auto hit_mask = [&](const float4 (&v)[4], int rot, uint32_t valid) -> uint32_t {
+    uint32_t pm = 0;
+    if (bound != 0.0f) {
 #pragma unroll
-    for (int v = 0; v < kVec; ++v) {
-      const uint32_t nib = (pm >> (4 * v)) & 0xfu;
-      below[v] = 0;
-      wcnt[v] = 0;
-      if (__any_sync(0xffffffffu, nib != 0)) {
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t b = static_cast<uint32_t>(v[j].x >= bound) |
+                           (static_cast<uint32_t>(v[j].y >= bound) << 1) |
+                           (static_cast<uint32_t>(v[j].z >= bound) << 2) |
+                           (static_cast<uint32_t>(v[j].w >= bound) << 3);
+        pm |= b << (4 * ((j + rot) & 3));
+      }
+    } else {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint32_t m = __ballot_sync(0xffffffffu, (nib >> c) & 1u);
-          below[v] += __popc(m & lt_mask);
-          wcnt[v] += __popc(m);
-        }
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t b = static_cast<uint32_t>(order_key(v[j].x) >= thr) |
+                           (static_cast<uint32_t>(order_key(v[j].y) >= thr) << 1) |
+                           (static_cast<uint32_t>(order_key(v[j].z) >= thr) << 2) |
+                           (static_cast<uint32_t>(order_key(v[j].w) >= thr) << 3);
+        pm |= b << (4 * ((j + rot) & 3));
       }
     }
-  };
-  auto read_table = [&](int par, uint32_t (&base)[kVec], uint32_t& total, bool& any_err) {
-    uint32_t e = lane < kVec * kWarps ? S.stab[par][lane] : 0u;
-    any_err = __any_sync(0xffffffffu, e >> 31);
-    e &= 0x7fffffffu;
-    const uint32_t incl = warp_incl_scan(e);
-    total = __shfl_sync(0xffffffffu, incl, kVec * kWarps - 1);
-#pragma unroll
-    for (int v = 0; v < kVec; ++v) base[v] = __shfl_sync(0xffffffffu, incl - e, v * kWarps + w);
+    return pm & valid;
   };
 
-  // Processes one group of up to 8 scores per thread: element (v, c) has key
-  // key[v][c], index idx[v] + c, and takes part if bit 4v+c of `valid` is set.
-  // Every thread of the CTA calls it; it contains block barriers.
-  auto process_group = [&](const uint32_t (&key)[kVec][4], uint32_t valid, const uint32_t (&idx)[kVec],
-                           bool err, bool refill) {
-    uint32_t pm = 0;
+  auto read_table = [&](int par, uint32_t& base, uint32_t& total, bool& any_err) {
+    const uint4 a = *reinterpret_cast<const uint4*>(&S.tab[par][0]);
+    const uint4 b = *reinterpret_cast<const uint4*>(&S.tab[par][4]);
+    const uint32_t e[kWarps] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t orv = 0;
+    base = 0;
+    total = 0;
 #pragma unroll
-    for (int v = 0; v < kVec; ++v)
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        if (((valid >> (4 * v + c)) & 1u) && key[v][c] >= thr) pm |= 1u << (4 * v + c);
-    uint32_t below[kVec], wcnt[kVec];
-    count_hits(pm, below, wcnt);
+    for (int i = 0; i < kWarps; ++i) {
+      orv |= e[i];
+      const uint32_t c = e[i] & 0x7fffffffu;
+      base += (i < w) ? c : 0u;
+      total += c;
+    }
+    any_err = (orv >> 31) != 0u;
+  };
+
+  // One group of scores: thread t holds up to 16 consecutive scores with
+  // indices idx0 + e (e in [0, 16), present where bit e of `valid` is set);
+  // v[j] holds scores e = 4*((j + rot) & 3) .. +3, absent ones as -inf. The
+  // same scores are readable at vals[e] (a ring slot) or, for a scalar group
+  // (vals == nullptr), score 0 is v[0].x. Every thread of the CTA calls it;
+  // it contains block barriers.
+  auto process_group = [&](const float4 (&v)[4], int rot, uint32_t valid, uint32_t idx0, bool err,
+                           const float* vals) {
+    float mx = fmaxf(fmaxf(fmaxf(v[0].x, v[0].y), fmaxf(v[0].z, v[0].w)),
+                     fmaxf(fmaxf(v[1].x, v[1].y), fmaxf(v[1].z, v[1].w)));
+    mx = fmaxf(mx, fmaxf(fmaxf(fmaxf(v[2].x, v[2].y), fmaxf(v[2].z, v[2].w)),
+                         fmaxf(fmaxf(v[3].x, v[3].y), fmaxf(v[3].z, v[3].w))));
+    uint32_t pm = (mx >= bound) ? hit_mask(v, rot, valid) : 0u;
+    uint32_t cnt = __popc(pm);
+    uint32_t incl = warp_incl_scan(cnt);  // this warp's slots, before the barrier
+    uint32_t wtot = __shfl_sync(0xffffffffu, incl, 31);
     const bool werr = __any_sync(0xffffffffu, err);
     const int par = static_cast<int>(grp & 1u);
-    if (lane == 0) {
-#pragma unroll
-      for (int v = 0; v < kVec; ++v) S.stab[par][v * kWarps + w] = wcnt[v] | (werr ? 0x80000000u : 0u);
-    }
-    __syncthreads();  // this group's ring slot has been read by every thread
-    if (refill && t == 0 && next_stage < s1 && !abort) issue_one();
-    uint32_t base[kVec], total;
+    ++grp;
+    if (lane == 0) S.tab[par][w] = wtot | (werr ? 0x80000000u : 0u);
+    __syncthreads();
+    uint32_t base, total;
     bool any_err;
     read_table(par, base, total, any_err);
     if (any_err) abort = true;
-    if (abort) {
-      ++grp;
-      return;
-    }
+    if (abort || total == 0) return;  // uniform
     if (n_st + total > cap) {
       compact();
-      pm = 0;
-#pragma unroll
-      for (int v = 0; v < kVec; ++v)
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          if (((valid >> (4 * v + c)) & 1u) && key[v][c] >= thr) pm |= 1u << (4 * v + c);
-      count_hits(pm, below, wcnt);
-      if (lane == 0) {
-#pragma unroll
-        for (int v = 0; v < kVec; ++v) S.stab[par][v * kWarps + w] = wcnt[v];
-      }
+      pm = (mx >= bound) ? hit_mask(v, rot, valid) : 0u;
+      cnt = __popc(pm);
+      incl = warp_incl_scan(cnt);
+      wtot = __shfl_sync(0xffffffffu, incl, 31);
+      if (lane == 0) S.tab[par][w] = wtot;
       __syncthreads();
       read_table(par, base, total, any_err);
     }
-#pragma unroll
-    for (int v = 0; v < kVec; ++v) {
-      uint32_t pos = n_st + base[v] + below[v];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        if ((pm >> (4 * v + c)) & 1u) {
-          S.skey[pos] = key[v][c];
-          S.sidx[pos] = idx[v] + c;
-          ++pos;
-        }
+    if (wtot != 0) {  // warp-uniform
+      uint32_t pos = n_st + base + incl - cnt;
+      uint32_t m = pm;
+      while (m != 0u) {  // this lane's hits, in index order
+        const int e = __ffs(m) - 1;
+        m &= m - 1u;
+        const float x = vals != nullptr ? vals[e] : v[0].x;
+        const uint32_t key = order_key(x);
+        S.skey[pos] = key;
+        S.sidx[pos] = idx0 + e;
+        atomicAdd(&S.hist[key >> 21], 1u);  // coarse histogram of the stash, kept current
+        ++pos;
       }
     }
     n_st += total;
-    ++grp;
   };
 
-  // Scalar group: thread t < cnt holds score at index first + t.
+  // Scalar group: thread t < cnt holds the score at index first + t.
   auto scalar_group = [&](int first, int cnt) {
-    uint32_t key[kVec][4] = {};
-    uint32_t idx[kVec] = {static_cast<uint32_t>(first + t), 0u};
+    const float ninf = -__int_as_float(0x7f800000);
+    float4 v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = make_float4(ninf, ninf, ninf, ninf);
     uint32_t valid = 0;
     if (t < cnt) {
-      key[0][0] = order_key(rp[first + t]);
+      v[0].x = rp[first + t];
       valid = 1u;
     }
-    process_group(key, valid, idx, false, false);
+    process_group(v, 0, valid, static_cast<uint32_t>(first + t), false, nullptr);
   };
 
   auto stream_pass = [&]() {
+    const float ninf = -__int_as_float(0x7f800000);
+    const int rot = (t >> 1) & 3;  // rotates the float4 order: conflict-free shared loads
     if (rank == 0 && h > 0) scalar_group(0, h);
     for (int j = s0; j < s1; ++j) {
       const uint32_t slot = consumed % kStages;
@@ -589,25 +642,23 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
         if (!err) ++t0_seen;  // in order: stages [t0_seen, issued) are unobserved
       }
       const int cnt = min(kStageFloats, nb - j * kStageFloats);
-      uint32_t key[kVec][4];
-      uint32_t idx[kVec];
+      float4 v[4];
       uint32_t valid = 0;
 #pragma unroll
-      for (int v = 0; v < kVec; ++v) {
-        const int f = v * kThreads + t;
-        idx[v] = static_cast<uint32_t>(h + j * kStageFloats + 4 * f);
-        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (4 * f < cnt) {
-          x = *reinterpret_cast<const float4*>(&S.ring[slot][4 * f]);
-          valid |= 0xfu << (4 * v);
+      for (int jj = 0; jj < 4; ++jj) {
+        const int q = (jj + rot) & 3;
+        const int e0 = kPerThread * t + 4 * q;
+        if (e0 < cnt) {
+          v[jj] = *reinterpret_cast<const float4*>(&S.ring[slot][e0]);
+          valid |= 0xfu << (4 * q);
+        } else {
+          v[jj] = make_float4(ninf, ninf, ninf, ninf);
         }
-        key[v][0] = order_key(x.x);
-        key[v][1] = order_key(x.y);
-        key[v][2] = order_key(x.z);
-        key[v][3] = order_key(x.w);
       }
       ++consumed;
-      process_group(key, valid, idx, err, true);
+      process_group(v, rot, valid, static_cast<uint32_t>(h + j * kStageFloats + kPerThread * t), err,
+                    &S.ring[slot][kPerThread * t]);
+      release_slot(j, slot);
     }
     if (rank == G - 1 && tail > 0) scalar_group(h + nb, tail);
   };
@@ -627,7 +678,10 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
     if (total < kk) {  // uniform over the cluster
       if (p.counters != nullptr && leader) atomicAdd(&p.counters[kCntRescan], 1u);
       thr = 0;
+      bound = prefilter_bound(thr);
       n_st = 0;
+      for (int i = t; i < kBins; i += kThreads) S.hist[i] = 0;  // forget the first pass
+      __syncthreads();
       prime();
       stream_pass();
     }
@@ -678,7 +732,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
     // A wait timed out: let copies still in flight land (bounded), then mark
     // the whole row as failed so the caller cannot mistake it for a result.
     if (t == 0) {
-      for (uint32_t u = t0_seen; u < issued; ++u)
+      for (uint32_t u = t0_seen; u < S.issued; ++u)
         (void)mbar_wait_bounded(&S.full[u % kStages], (u / kStages) & 1u, kWaitLimitNs);
       if (p.counters != nullptr) atomicAdd(&p.counters[kCntDeviceErrors], 1u);
     }

@@ -1,0 +1,62 @@
+"""Full-size workloads (B=1024 x 131072 / 262144), in the launch configuration
+the benchmark times: every row is checked by properties that hold at any size,
+and a sample of rows is compared element by element with the CPU oracle."""
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle_pins as P  # noqa: E402
+from gpu_helpers import assert_parity, run_oracle, to_dev  # noqa: E402
+from synth import make_workload  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import sparse_attention_indexer_fp32_gb300 as tk  # noqa: E402
+
+SAMPLED_ROWS = 24
+
+
+def _properties_all_rows(scores, lengths, k, out):
+    """Exactly min(k, n) unique indices in [0, n), -1 after them, and no
+    unselected score outranking a selected one - for every row."""
+    B, stride = scores.shape
+    for b in range(B):
+        n = P.valid_len(lengths[b], stride)
+        m = min(k, n)
+        sel = out[b, :m]
+        assert np.all(out[b, m:] == -1), b
+        assert np.all((sel >= 0) & (sel < n)), b
+        assert np.unique(sel).size == m, b
+        if m < n:
+            tov = P.total_order(scores[b, :n])
+            chosen = np.zeros(n, dtype=bool)
+            chosen[sel] = True
+            assert tov[chosen].min() >= tov[~chosen].max(), b
+
+
+@pytest.mark.parametrize("config", [3, 4])
+def test_full_size_workload(config):
+    w = make_workload(config)
+    s, l = to_dev(w.scores), to_dev(w.lengths)
+    ragged = tk.topk_ragged(s, l, w.k).cpu().numpy()
+    _properties_all_rows(w.scores, w.lengths, w.k, ragged)
+
+    rows = np.random.default_rng(config).choice(w.B, SAMPLED_ROWS, replace=False)
+    want = run_oracle(w.scores[rows], w.lengths[rows], w.k)
+    assert_parity(w.scores[rows], w.lengths[rows], w.k, ragged[rows], want, rows=rows)
+
+    if w.paged:
+        pt = to_dev(w.page_table)
+        paged = tk.topk_paged(s, l, w.k, pt, w.page_size).cpu().numpy()
+        assert np.array_equal(paged, P.page_map_reference(ragged, w.page_table, w.page_size))
+        want_p = run_oracle(w.scores[rows], w.lengths[rows], w.k, w.page_table[rows], w.page_size)
+        assert_parity(w.scores[rows], w.lengths[rows], w.k, paged[rows], want_p, rows=rows,
+                      page_table=w.page_table)
+    # the same answer on a second call
+    again = tk.topk_ragged(s, l, w.k).cpu().numpy()
+    assert np.array_equal(again, ragged)

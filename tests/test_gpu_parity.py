@@ -82,7 +82,7 @@ def test_compaction_path(k, cluster):
     scores, lengths = _mixed_rows()
     cnt = counters_tensor()
     check_against_oracle(scores, lengths, k, sample_mode=1, cluster_size=cluster,
-                         stash_capacity=k + 2048, counters=cnt)
+                         stash_capacity=k + 4096, counters=cnt)
     assert int(cnt[tk.Counter.COMPACTIONS]) > 0
 
 
@@ -114,7 +114,7 @@ def test_capacity_boundaries_without_sampling():
     """Row lengths around the candidate-buffer capacity: the buffer fills
     exactly, one short of, and one past its end."""
     rng = np.random.default_rng(11)
-    for k, cap in ((512, 4096), (1024, 4096), (2048, 6144)):
+    for k, cap in ((512, 4608), (1024, 5120), (2048, 6144)):
         ns = [cap - 1, cap, cap + 1, cap + 2047, cap + 2048, cap + 2049, 2 * cap + 5]
         stride = max(ns) + 3
         scores = rng.standard_normal((len(ns), stride)).astype(np.float32)
