@@ -133,8 +133,21 @@ __device__ __forceinline__ float prefilter_bound(uint32_t thr) {
   return __uint_as_float(u);
 }
 
-__device__ __forceinline__ float4 pick4(const float4 (&v)[4], int j) {
-  return j == 0 ? v[0] : (j == 1 ? v[1] : (j == 2 ? v[2] : v[3]));
+// Three-input maximum (one instruction on sm_100 and later).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Maximum of the 16 scores held in v.
+__device__ __forceinline__ float max16(const float4 (&v)[4]) {
+  const float a = max3f(v[0].x, v[0].y, v[0].z);
+  const float b = max3f(v[0].w, v[1].x, v[1].y);
+  const float c = max3f(v[1].z, v[1].w, v[2].x);
+  const float d = max3f(v[2].y, v[2].z, v[2].w);
+  const float e = max3f(v[3].x, v[3].y, v[3].z);
+  return max3f(max3f(a, b, c), max3f(d, e, v[3].w), -__int_as_float(0x7f800000));
 }
 
 // Inclusive prefix sum over lanes [0, LANES) of the warp (lanes past LANES
@@ -570,10 +583,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
   // it contains block barriers.
   auto process_group = [&](const float4 (&v)[4], int rot, uint32_t valid, uint32_t idx0, bool err,
                            const float* vals) {
-    float mx = fmaxf(fmaxf(fmaxf(v[0].x, v[0].y), fmaxf(v[0].z, v[0].w)),
-                     fmaxf(fmaxf(v[1].x, v[1].y), fmaxf(v[1].z, v[1].w)));
-    mx = fmaxf(mx, fmaxf(fmaxf(fmaxf(v[2].x, v[2].y), fmaxf(v[2].z, v[2].w)),
-                         fmaxf(fmaxf(v[3].x, v[3].y), fmaxf(v[3].z, v[3].w))));
+    const float mx = max16(v);
     uint32_t pm = (mx >= bound) ? hit_mask(v, rot, valid) : 0u;
     uint32_t cnt = __popc(pm);
     uint32_t incl = warp_incl_scan(cnt);  // this warp's slots, before the barrier
@@ -642,22 +652,29 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
         if (!err) ++t0_seen;  // in order: stages [t0_seen, issued) are unobserved
       }
       const int cnt = min(kStageFloats, nb - j * kStageFloats);
+      const float* ts = &S.ring[slot][kPerThread * t];
       float4 v[4];
-      uint32_t valid = 0;
+      uint32_t valid = 0xffffu;
+      if (cnt == kStageFloats) {
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        const int q = (jj + rot) & 3;
-        const int e0 = kPerThread * t + 4 * q;
-        if (e0 < cnt) {
-          v[jj] = *reinterpret_cast<const float4*>(&S.ring[slot][e0]);
-          valid |= 0xfu << (4 * q);
-        } else {
-          v[jj] = make_float4(ninf, ninf, ninf, ninf);
+        for (int jj = 0; jj < 4; ++jj)
+          v[jj] = *reinterpret_cast<const float4*>(ts + 4 * ((jj + rot) & 3));
+      } else {
+        valid = 0;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const int q = (jj + rot) & 3;
+          if (kPerThread * t + 4 * q < cnt) {
+            v[jj] = *reinterpret_cast<const float4*>(ts + 4 * q);
+            valid |= 0xfu << (4 * q);
+          } else {
+            v[jj] = make_float4(ninf, ninf, ninf, ninf);
+          }
         }
       }
       ++consumed;
       process_group(v, rot, valid, static_cast<uint32_t>(h + j * kStageFloats + kPerThread * t), err,
-                    &S.ring[slot][kPerThread * t]);
+                    ts);
       release_slot(j, slot);
     }
     if (rank == G - 1 && tail > 0) scalar_group(h + nb, tail);
