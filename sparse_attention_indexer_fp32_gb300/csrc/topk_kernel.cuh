@@ -404,6 +404,49 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
   const int s0 = static_cast<int>(static_cast<int64_t>(nstages) * rank / G);
   const int s1 = static_cast<int>(static_cast<int64_t>(nstages) * (rank + 1) / G);
 
+  // ---- sampled cutoff: decision and sample loads (issued before the ring
+  // setup so their latency overlaps it) ---------------------------------------
+  uint32_t thr = 0;
+  bool sampled = false;
+  uint32_t target = 0;
+  uint32_t sk[16];
+  uint32_t smask = 0;
+  {
+    const bool long_enough = nb >= 2 * 4 * kSampleVec4;
+    const bool want = long_enough && (p.sample_mode == 2 || (p.sample_mode == 0 && n >= p.sample_min_n));
+    if (want) {
+      const float mu = static_cast<float>(kk) * (4.0f * kSampleVec4) / static_cast<float>(n);
+      float rf = ceilf(mu + p.sample_z * sqrtf(mu)) + 1.0f;
+      rf = fmaxf(rf, 1.0f);
+      if (rf < 4.0f * kSampleVec4) {
+        sampled = true;
+        target = static_cast<uint32_t>(rf);
+      }
+    }
+#pragma unroll
+    for (int v = 0; v < 4; ++v) sk[4 * v + 0] = sk[4 * v + 1] = sk[4 * v + 2] = sk[4 * v + 3] = 0;
+    if (sampled) {
+      const int nb4 = nb >> 2;
+      constexpr int per_rank = kSampleVec4 / G;
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const int f = t + v * kThreads;
+        if (f < per_rank) {
+          const int gf = rank * per_rank + f;
+          const int chunk = gf / kSampleChunkVec4, within = gf % kSampleChunkVec4;
+          const int64_t off4 =
+              static_cast<int64_t>(chunk) * (nb4 - kSampleChunkVec4) / (kSampleChunks - 1) + within;
+          const float4 x = __ldg(reinterpret_cast<const float4*>(body) + off4);
+          sk[4 * v + 0] = order_key(x.x);
+          sk[4 * v + 1] = order_key(x.y);
+          sk[4 * v + 2] = order_key(x.z);
+          sk[4 * v + 3] = order_key(x.w);
+          smask |= 0xfu << (4 * v);
+        }
+      }
+    }
+  }
+
   if (t == 0) {
 #pragma unroll
     for (int s = 0; s < kStages; ++s) {
@@ -450,61 +493,23 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
   };
   prime();  // the first stages are in flight while the sample is examined
 
-  // ---- sampled cutoff -------------------------------------------------------
-  uint32_t thr = 0;
-  bool sampled = false;
-  {
-    const bool long_enough = nb >= 2 * 4 * kSampleVec4;
-    const bool want = long_enough && (p.sample_mode == 2 || (p.sample_mode == 0 && n >= p.sample_min_n));
-    uint32_t target = 0;
-    if (want) {
-      const float mu = static_cast<float>(kk) * (4.0f * kSampleVec4) / static_cast<float>(n);
-      float rf = ceilf(mu + p.sample_z * sqrtf(mu)) + 1.0f;
-      rf = fmaxf(rf, 1.0f);
-      if (rf < 4.0f * kSampleVec4) {
-        sampled = true;
-        target = static_cast<uint32_t>(rf);
-      }
-    }
-    if (sampled) {
-      const int nb4 = nb >> 2;
-      constexpr int per_rank = kSampleVec4 / G;
-      uint32_t sk[16];
-      uint32_t smask = 0;
+  // ---- sampled cutoff: two 11-bit radix passes over the sample ---------------
+  if (sampled) {
+    uint32_t above, inbin;
 #pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        const int f = t + v * kThreads;
-        if (f < per_rank) {
-          const int gf = rank * per_rank + f;
-          const int chunk = gf / kSampleChunkVec4, within = gf % kSampleChunkVec4;
-          const int64_t off4 =
-              static_cast<int64_t>(chunk) * (nb4 - kSampleChunkVec4) / (kSampleChunks - 1) + within;
-          const float4 x = __ldg(reinterpret_cast<const float4*>(body) + off4);
-          sk[4 * v + 0] = order_key(x.x);
-          sk[4 * v + 1] = order_key(x.y);
-          sk[4 * v + 2] = order_key(x.z);
-          sk[4 * v + 3] = order_key(x.w);
-          smask |= 0xfu << (4 * v);
-        } else {
-          sk[4 * v + 0] = sk[4 * v + 1] = sk[4 * v + 2] = sk[4 * v + 3] = 0;
-        }
-      }
-      uint32_t above, inbin;
+    for (int i = 0; i < 16; ++i) hist_add(S.hist, ((smask >> i) & 1u) ? (sk[i] >> 21) : 0xffffffffu);
+    const uint32_t b1 = merged_find<G, 8>(S, target, &above, &inbin);
+    const uint32_t rem = target - above;
+    if (rem == inbin) {
+      thr = b1 << 21;
+    } else {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) hist_add(S.hist, ((smask >> i) & 1u) ? (sk[i] >> 21) : 0xffffffffu);
-      const uint32_t b1 = merged_find<G, 8>(S, target, &above, &inbin);
-      const uint32_t rem = target - above;
-      if (rem == inbin) {
-        thr = b1 << 21;
-      } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const bool ok = ((smask >> i) & 1u) && (sk[i] >> 21) == b1;
-          hist_add(S.hist, ok ? ((sk[i] >> 10) & 0x7ffu) : 0xffffffffu);
-        }
-        const uint32_t b2 = merged_find<G, 8>(S, rem, &above, &inbin);
-        thr = (b1 << 21) | (b2 << 10);
+      for (int i = 0; i < 16; ++i) {
+        const bool ok = ((smask >> i) & 1u) && (sk[i] >> 21) == b1;
+        hist_add(S.hist, ok ? ((sk[i] >> 10) & 0x7ffu) : 0xffffffffu);
       }
+      const uint32_t b2 = merged_find<G, 8>(S, rem, &above, &inbin);
+      thr = (b1 << 21) | (b2 << 10);
     }
   }
 
@@ -611,15 +616,25 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
     if (wtot != 0) {  // warp-uniform
       uint32_t pos = n_st + base + incl - cnt;
       uint32_t m = pm;
-      while (m != 0u) {  // this lane's hits, in index order
-        const int e = __ffs(m) - 1;
+      while (m != 0u) {  // this lane's hits, in index order, two at a time
+        const int e0 = __ffs(m) - 1;
         m &= m - 1u;
-        const float x = vals != nullptr ? vals[e] : v[0].x;
-        const uint32_t key = order_key(x);
-        S.skey[pos] = key;
-        S.sidx[pos] = idx0 + e;
-        atomicAdd(&S.hist[key >> 21], 1u);  // coarse histogram of the stash, kept current
+        const bool two = m != 0u;
+        const int e1 = two ? __ffs(m) - 1 : e0;
+        if (two) m &= m - 1u;
+        const float x0 = vals != nullptr ? vals[e0] : v[0].x;
+        const float x1 = vals != nullptr ? vals[e1] : v[0].x;
+        const uint32_t k0 = order_key(x0), k1 = order_key(x1);
+        S.skey[pos] = k0;
+        S.sidx[pos] = idx0 + e0;
+        atomicAdd(&S.hist[k0 >> 21], 1u);  // coarse histogram of the stash, kept current
         ++pos;
+        if (two) {
+          S.skey[pos] = k1;
+          S.sidx[pos] = idx0 + e1;
+          atomicAdd(&S.hist[k1 >> 21], 1u);
+          ++pos;
+        }
       }
     }
     n_st += total;
