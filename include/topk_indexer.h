@@ -132,6 +132,13 @@ int32_t topk_abi_version(void);
  *                   the sampled cutoff too high and force the full rescan)
  *   counters        optional DEVICE array of TOPK_NUM_COUNTERS uint32, which
  *                   the kernel increments (see topk_counter); NULL = none
+ *   probe_stage     0 = off; s >= 1 makes the wait for streamed stage s-1 of
+ *                   every row wait instead on a barrier that nothing completes,
+ *                   so it runs out after probe_wait_us microseconds (1 ..
+ *                   5,000,000): the row then takes the device-error path
+ *                   (TOPK_DEVICE_ERROR_INDEX in every slot, counted). This
+ *                   tests the bounded waits without a real fault; results of
+ *                   such a call are not a selection.
  */
 typedef enum topk_counter {
   TOPK_CNT_ROWS = 0,          /* rows handled */
@@ -150,6 +157,8 @@ typedef struct topk_debug_opts {
   int32_t stash_capacity;
   float sample_z;
   uint32_t* counters;
+  int32_t probe_stage;
+  uint32_t probe_wait_us;
 } topk_debug_opts;
 
 topk_status topk_select_ex(const float* scores, int64_t stride, const int32_t* lengths,

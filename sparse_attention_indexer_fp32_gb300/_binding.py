@@ -54,7 +54,8 @@ class TopkError(RuntimeError):
 class _DebugOpts(ctypes.Structure):
     _fields_ = [("sample_mode", ctypes.c_int32), ("cluster_size", ctypes.c_int32),
                 ("stash_capacity", ctypes.c_int32), ("sample_z", ctypes.c_float),
-                ("counters", ctypes.c_void_p)]
+                ("counters", ctypes.c_void_p), ("probe_stage", ctypes.c_int32),
+                ("probe_wait_us", ctypes.c_uint32)]
 
 
 _lib = None
@@ -154,7 +155,8 @@ def topk_select_ex(scores: torch.Tensor, lengths: torch.Tensor, k: int,
                    page_table: Optional[torch.Tensor] = None, page_size: int = 0,
                    out: Optional[torch.Tensor] = None, *, sample_mode: int = 0,
                    cluster_size: int = 0, stash_capacity: int = 0, sample_z: float = 0.0,
-                   counters: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                   counters: Optional[torch.Tensor] = None, probe_stage: int = 0,
+                   probe_wait_us: int = 0, stream=None) -> torch.Tensor:
     """Diagnostic variant: same result, with the internal path forced (see the
     header's ``topk_debug_opts``). ``counters`` is an optional int32/uint32
     CUDA tensor of ``NUM_COUNTERS`` entries that the kernel increments."""
@@ -166,7 +168,7 @@ def topk_select_ex(scores: torch.Tensor, lengths: torch.Tensor, k: int,
             raise ValueError("page_table must be contiguous int32")
         pt_ptr, pt_stride = page_table.data_ptr(), page_table.shape[1]
     opts = _DebugOpts(sample_mode, cluster_size, stash_capacity, sample_z,
-                      None if counters is None else counters.data_ptr())
+                      None if counters is None else counters.data_ptr(), probe_stage, probe_wait_us)
     if counters is not None and (counters.numel() < NUM_COUNTERS or not counters.is_cuda
                                  or counters.element_size() != 4):
         raise ValueError("counters must be a 4-byte CUDA tensor of NUM_COUNTERS entries")

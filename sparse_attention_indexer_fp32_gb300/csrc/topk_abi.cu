@@ -93,6 +93,8 @@ topk_status select_impl(const float* scores, int64_t stride, const int32_t* leng
   p.sample_min_n = kDefaultSampleMinN;
   p.sample_z = kDefaultSampleZ;
   p.counters = nullptr;
+  p.probe_stage = -1;
+  p.probe_wait_us = 0;
 
   int G = 0;
   if (opts != nullptr) {
@@ -111,6 +113,10 @@ topk_status select_impl(const float* scores, int64_t stride, const int32_t* leng
     }
     if (opts->counters != nullptr && !aligned4(opts->counters)) return TOPK_EINVAL;
     p.counters = opts->counters;
+    if (opts->probe_stage < 0 || (opts->probe_stage > 0 && opts->probe_wait_us == 0)) return TOPK_EINVAL;
+    if (opts->probe_wait_us > 5000000u) return TOPK_EINVAL;  // the probe wait stays short
+    p.probe_stage = opts->probe_stage - 1;
+    p.probe_wait_us = opts->probe_wait_us;
   }
 
   int dev = 0;

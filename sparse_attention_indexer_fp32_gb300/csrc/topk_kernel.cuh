@@ -85,6 +85,7 @@ struct __align__(128) Smem {
   uint32_t sidx[C];
   uint32_t hist[kBins];
   uint64_t full[kStages];
+  uint64_t never;                   // an mbarrier nothing arrives on (the wait-limit test)
   uint32_t rel[kStages];            // warps done with each ring slot (the last one refills it)
   uint32_t issued;                  // stages issued into the ring (for the error drain)
   alignas(16) uint32_t tab[2][kWarps];  // per-group per-warp hit counts; bit 31 = a wait timed out
@@ -109,6 +110,8 @@ struct Params {
   int32_t sample_min_n;  // automatic sampling gate on the row length
   float sample_z;        // standard deviations of margin on the sampled rank
   uint32_t* counters;    // optional diagnostics
+  int32_t probe_stage;   // test only: >= 0 makes that stage's wait run out on a barrier
+  uint32_t probe_wait_us;  // that nothing completes, after this many microseconds
 };
 
 // Cutoff description: an entry is selected if (key >> shift) > P, or if
@@ -453,6 +456,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
       mbar_init(&S.full[s], 1);
       S.rel[s] = 0;
     }
+    mbar_init(&S.never, 1);
     S.issued = 0;
     fence_mbar_init();
   }
@@ -663,8 +667,12 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
       const uint32_t parity = (consumed / kStages) & 1u;
       bool err = false;
       if (!abort) {
-        err = !mbar_wait_bounded(&S.full[slot], parity, kWaitLimitNs);
-        if (!err) ++t0_seen;  // in order: stages [t0_seen, issued) are unobserved
+        if (j - s0 == p.probe_stage) {
+          err = !mbar_wait_bounded(&S.never, 0u, 1000ull * p.probe_wait_us);  // runs out
+        } else {
+          err = !mbar_wait_bounded(&S.full[slot], parity, kWaitLimitNs);
+          if (!err) ++t0_seen;  // in order: stages [t0_seen, issued) are unobserved
+        }
       }
       const int cnt = min(kStageFloats, nb - j * kStageFloats);
       const float* ts = &S.ring[slot][kPerThread * t];

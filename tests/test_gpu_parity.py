@@ -244,3 +244,17 @@ def test_deterministic_over_100_calls(config):
         again = tk.topk_ragged(s, l, w.k)
         assert torch.equal(first, again)
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("cluster", [1, 2])
+def test_wait_limit_reports_device_error(cluster):
+    """A wait that runs out (on a barrier nothing completes) is reported: the
+    rows carry TOPK_DEVICE_ERROR_INDEX, the error is counted, the call
+    returns, and the context keeps working."""
+    w = make_workload(3, B=4)
+    cnt = counters_tensor()
+    out = run_gpu(w.scores, w.lengths, w.k, cluster_size=cluster, counters=cnt,
+                  probe_stage=2, probe_wait_us=2000)
+    assert np.all(out == tk.DEVICE_ERROR_INDEX)
+    assert int(cnt[tk.Counter.DEVICE_ERRORS]) == 4 * cluster
+    check_against_oracle(w.scores, w.lengths, w.k, cluster_size=cluster)
