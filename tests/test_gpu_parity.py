@@ -258,3 +258,39 @@ def test_wait_limit_reports_device_error(cluster):
     assert np.all(out == tk.DEVICE_ERROR_INDEX)
     assert int(cnt[tk.Counter.DEVICE_ERRORS]) == 4 * cluster
     check_against_oracle(w.scores, w.lengths, w.k, cluster_size=cluster)
+
+
+@pytest.mark.parametrize("paged", [False, True])
+def test_cuda_graph_replay_with_mutated_lengths(paged):
+    """One captured call replayed with the row lengths (and once the scores)
+    rewritten in place between replays, as a decode step would: every replay
+    matches the oracle on the inputs current at that replay."""
+    rng = np.random.default_rng(21)
+    B, stride, k, ps = 6, 98307 + 3, 1024, 64
+    scores = rng.standard_normal((B, stride)).astype(np.float32)
+    pt = rng.permutation(B * 1600).astype(np.int32).reshape(B, 1600) if paged else None
+    s, l = to_dev(scores), to_dev(np.full(B, stride, np.int32))
+    dpt = to_dev(pt) if paged else None
+    out = torch.empty((B, k), dtype=torch.int32, device="cuda:0")
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):  # warm the library (attributes, device query) first
+        tk.topk_ragged(s, l, k, out=out) if not paged else tk.topk_paged(s, l, k, dpt, ps, out=out)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        if paged:
+            tk.topk_paged(s, l, k, dpt, ps, out=out)
+        else:
+            tk.topk_ragged(s, l, k, out=out)
+    boundary = [-1, 0, 1, k - 1, k, 32769, 65535, 98307, stride, stride + 17]
+    for rep in range(4):
+        lengths = np.array([boundary[(rep * B + i) % len(boundary)] for i in range(B)], np.int32)
+        if rep == 2:
+            scores = -scores  # flip the scores once
+            s.copy_(to_dev(scores))
+        l.copy_(to_dev(lengths))
+        graph.replay()
+        torch.cuda.synchronize()
+        want = run_oracle(scores, lengths, k, pt, ps if paged else 0)
+        assert_parity(scores, lengths, k, out.cpu().numpy(), want, page_table=pt)
+
