@@ -123,10 +123,10 @@ int32_t topk_abi_version(void);
  *   cluster_size    0 automatic, 1 one CTA per row, or 2 / 4 / 8 CTAs of a
  *                   thread-block cluster per row
  *   stash_capacity  0 = default; otherwise the candidate-buffer size to use,
- *                   in [k + 4096, default]: small values force the in-buffer
+ *                   in [k + 2048, default]: small values force the in-buffer
  *                   compaction path on ordinary inputs. The default is
- *                   b + 4096 entries, b = 512, 1024 or 2048 the smallest of
- *                   these not below k
+ *                   min(b + 4096, 5120) entries, b = 512, 1024 or 2048 the
+ *                   smallest of these not below k
  *   sample_z        0 = default margin; otherwise the number of standard
  *                   deviations added to the sampled rank (negative values make
  *                   the sampled cutoff too high and force the full rescan)

@@ -76,7 +76,9 @@ topk_status select_impl(const float* scores, int64_t stride, const int32_t* leng
   }
 
   const int kmax = k <= 512 ? 512 : (k <= 1024 ? 1024 : 2048);
-  const int cap_max = kmax + tki::kStageFloats;  // tki::StashCap<kmax>::value
+  const int cap_max = kmax == 512    ? tki::StashCap<512>::value
+                      : kmax == 1024 ? tki::StashCap<1024>::value
+                                     : tki::StashCap<2048>::value;
 
   Params p = {};
   p.scores = scores;
@@ -101,7 +103,7 @@ topk_status select_impl(const float* scores, int64_t stride, const int32_t* leng
     if (opts->sample_mode < 0 || opts->sample_mode > 2) return TOPK_EINVAL;
     p.sample_mode = opts->sample_mode;
     if (opts->stash_capacity != 0) {
-      if (opts->stash_capacity < k + tki::kStageFloats || opts->stash_capacity > cap_max)
+      if (opts->stash_capacity < k + tki::kMinStashRoom || opts->stash_capacity > cap_max)
         return TOPK_EINVAL;
       p.cap = opts->stash_capacity;
     }

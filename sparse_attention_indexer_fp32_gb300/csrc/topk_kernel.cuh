@@ -51,13 +51,20 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kStageFloats = 4096;                     // one ring stage: 16 KiB of scores
 constexpr int kPerThread = kStageFloats / kThreads;    // 16 consecutive scores per thread
-constexpr int kStages = 3;                             // ring depth: 48 KiB
+constexpr int kStages = 4;                             // ring depth: 64 KiB
 constexpr int kSampleVec4 = 1024;                    // 4096 sampled scores ...
 constexpr int kSampleChunkVec4 = 64;                 // ... in 16 chunks of 256
 constexpr int kSampleChunks = kSampleVec4 / kSampleChunkVec4;
 constexpr int kBins = 2048;
 constexpr int kRoundEntries = 4 * kThreads;          // stash entries per emission round
 constexpr uint64_t kWaitLimitNs = 2000000000ull;     // 2 s: far beyond any stage latency
+// Packed per-warp hit counts of a pair of stages: stage A in bits [0, 13),
+// stage B in bits [17, 30) (each at most one stage, 4096 < 2^13), and the
+// warps' wait-error flags summed in bits [13, 17) (at most 8 < 2^4).
+constexpr uint32_t kFieldB = 17;
+constexpr uint32_t kFieldMask = 0x1fffu;
+constexpr uint32_t kErrUnit = 1u << 13;
+constexpr uint32_t kErrMask = 0xfu << 13;
 
 static_assert(kPerThread == 16, "stage layout assumes four float4 per thread");
 
@@ -74,9 +81,12 @@ enum : int {
 
 template <int KMAX>
 struct StashCap {
-  // Room for k kept candidates plus one full stage of new ones.
-  static constexpr int value = KMAX + kStageFloats;
+  // Room for k kept candidates plus the new ones of one stage, at most 5120
+  // entries so that two CTAs with a four-stage ring fit on an SM.
+  static constexpr int value = KMAX + kStageFloats < 5120 ? KMAX + kStageFloats : 5120;
 };
+// Smallest stash capacity beyond k: the hits of half a CTA on one stage.
+constexpr int kMinStashRoom = kStageFloats / 2;
 
 template <int C>
 struct __align__(128) Smem {
@@ -484,14 +494,24 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
       S.issued += m;
     }
   };
-  // Called by every thread once it no longer reads ring slot `slot` (stage j).
-  auto release_slot = [&](int j, uint32_t slot) {
+  // Called by every thread once it no longer reads ring slot `slot` (stage
+  // j) nor, when `two`, the next slot (stage j + 1). The last warp refills
+  // both with the stages kStages further on.
+  auto release_slots = [&](int j, uint32_t slot, bool two) {
     __syncwarp();
     if (lane == 0 && atom_add_acq_rel_cta(&S.rel[slot], 1u) == kWarps - 1) {
       S.rel[slot] = 0;
-      if (!abort && j + kStages < s1) {
-        issue_stage(j + kStages, slot);
-        atomicAdd(&S.issued, 1u);
+      if (!abort) {
+        uint32_t m = 0;
+        if (j + kStages < s1) {
+          issue_stage(j + kStages, slot);
+          ++m;
+        }
+        if (two && j + 1 + kStages < s1) {
+          issue_stage(j + 1 + kStages, (slot + 1) % kStages);
+          ++m;
+        }
+        if (m != 0) atomicAdd(&S.issued, m);
       }
     }
   };
@@ -567,138 +587,178 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
     return pm & valid;
   };
 
-  auto read_table = [&](int par, uint32_t& base, uint32_t& total, bool& any_err) {
+  // Hit mask of this thread's 16 scores of a ring stage (ts points at them;
+  // scores past the stage's end are stale and masked off by `valid`). The
+  // float4 reads are rotated by `rot` so that they are bank-conflict free.
+  // A scalar group (ts == nullptr) has one score, sx, present when bit 0 of
+  // `valid` is set.
+  auto group_mask = [&](const float* ts, float sx, int rot, uint32_t valid) -> uint32_t {
+    if (ts == nullptr) return ((valid & 1u) != 0u && order_key(sx) >= thr) ? 1u : 0u;
+    float4 v[4];
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) v[jj] = *reinterpret_cast<const float4*>(ts + 4 * ((jj + rot) & 3));
+    return (max16(v) >= bound) ? hit_mask(v, rot, valid) : 0u;
+  };
+
+  // Base (lower warps) and total of the packed per-warp counts in table half `par`.
+  auto read_table = [&](int par, uint32_t& base, uint32_t& total) {
     const uint4 a = *reinterpret_cast<const uint4*>(&S.tab[par][0]);
     const uint4 b = *reinterpret_cast<const uint4*>(&S.tab[par][4]);
     const uint32_t e[kWarps] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-    uint32_t orv = 0;
     base = 0;
     total = 0;
 #pragma unroll
     for (int i = 0; i < kWarps; ++i) {
-      orv |= e[i];
-      const uint32_t c = e[i] & 0x7fffffffu;
-      base += (i < w) ? c : 0u;
-      total += c;
+      base += (i < w) ? e[i] : 0u;
+      total += e[i];
     }
-    any_err = (orv >> 31) != 0u;
   };
 
-  // One group of scores: thread t holds up to 16 consecutive scores with
-  // indices idx0 + e (e in [0, 16), present where bit e of `valid` is set);
-  // v[j] holds scores e = 4*((j + rot) & 3) .. +3, absent ones as -inf. The
-  // same scores are readable at vals[e] (a ring slot) or, for a scalar group
-  // (vals == nullptr), score 0 is v[0].x. Every thread of the CTA calls it;
-  // it contains block barriers.
-  auto process_group = [&](const float4 (&v)[4], int rot, uint32_t valid, uint32_t idx0, bool err,
-                           const float* vals) {
-    const float mx = max16(v);
-    uint32_t pm = (mx >= bound) ? hit_mask(v, rot, valid) : 0u;
-    uint32_t cnt = __popc(pm);
-    uint32_t incl = warp_incl_scan(cnt);  // this warp's slots, before the barrier
-    uint32_t wtot = __shfl_sync(0xffffffffu, incl, 31);
+  // Publishes this warp's packed count and error flag and synchronises the
+  // CTA. Returns this lane's inclusive packed count in the warp, and the
+  // packed counts of the lower warps (base) and of all warps (total).
+  auto publish = [&](uint32_t cnt, bool err, uint32_t& incl, uint32_t& base, uint32_t& total) {
+    incl = warp_incl_scan(cnt);
+    const uint32_t wtot = __shfl_sync(0xffffffffu, incl, 31);
     const bool werr = __any_sync(0xffffffffu, err);
     const int par = static_cast<int>(grp & 1u);
     ++grp;
-    if (lane == 0) S.tab[par][w] = wtot | (werr ? 0x80000000u : 0u);
+    if (lane == 0) S.tab[par][w] = wtot + (werr ? kErrUnit : 0u);
     __syncthreads();
-    uint32_t base, total;
-    bool any_err;
-    read_table(par, base, total, any_err);
-    if (any_err) abort = true;
-    if (abort || total == 0) return;  // uniform
-    if (n_st + total > cap) {
-      compact();
-      pm = (mx >= bound) ? hit_mask(v, rot, valid) : 0u;
-      cnt = __popc(pm);
-      incl = warp_incl_scan(cnt);
-      wtot = __shfl_sync(0xffffffffu, incl, 31);
-      if (lane == 0) S.tab[par][w] = wtot;
-      __syncthreads();
-      read_table(par, base, total, any_err);
-    }
-    if (wtot != 0) {  // warp-uniform
-      uint32_t pos = n_st + base + incl - cnt;
-      uint32_t m = pm;
-      while (m != 0u) {  // this lane's hits, in index order, two at a time
-        const int e0 = __ffs(m) - 1;
-        m &= m - 1u;
-        const bool two = m != 0u;
-        const int e1 = two ? __ffs(m) - 1 : e0;
-        if (two) m &= m - 1u;
-        const float x0 = vals != nullptr ? vals[e0] : v[0].x;
-        const float x1 = vals != nullptr ? vals[e1] : v[0].x;
-        const uint32_t k0 = order_key(x0), k1 = order_key(x1);
-        S.skey[pos] = k0;
-        S.sidx[pos] = idx0 + e0;
-        atomicAdd(&S.hist[k0 >> 21], 1u);  // coarse histogram of the stash, kept current
+    read_table(par, base, total);
+  };
+
+  // Appends this lane's hits (bits of m, in index order) from stash position
+  // pos on; score e is ts[e] (or sx for a scalar group), its index idx0 + e.
+  auto write_hits = [&](uint32_t m, uint32_t pos, const float* ts, float sx, uint32_t idx0) {
+    while (m != 0u) {  // two at a time
+      const int e0 = __ffs(m) - 1;
+      m &= m - 1u;
+      const bool two = m != 0u;
+      const int e1 = two ? __ffs(m) - 1 : e0;
+      if (two) m &= m - 1u;
+      const float x0 = ts != nullptr ? ts[e0] : sx;
+      const float x1 = ts != nullptr ? ts[e1] : sx;
+      const uint32_t k0 = order_key(x0), k1 = order_key(x1);
+      S.skey[pos] = k0;
+      S.sidx[pos] = idx0 + e0;
+      atomicAdd(&S.hist[k0 >> 21], 1u);  // coarse histogram of the stash, kept current
+      ++pos;
+      if (two) {
+        S.skey[pos] = k1;
+        S.sidx[pos] = idx0 + e1;
+        atomicAdd(&S.hist[k1 >> 21], 1u);
         ++pos;
-        if (two) {
-          S.skey[pos] = k1;
-          S.sidx[pos] = idx0 + e1;
-          atomicAdd(&S.hist[k1 >> 21], 1u);
-          ++pos;
-        }
       }
     }
-    n_st += total;
+  };
+
+  // One group: two consecutive ring stages A and B (B absent when tsB is
+  // null), or one scalar group as A. Thread t's 16 scores of stage A start at
+  // tsA and have indices idxA + e (present where bit e of validA is set);
+  // likewise for B. Hits of A precede those of B in the stash, each in index
+  // order, so the stash stays in index order. One block barrier per group
+  // (more only when the stash must be compacted). Every thread of the CTA
+  // calls it.
+  auto process_group = [&](const float* tsA, const float* tsB, float sx, int rot, uint32_t validA,
+                           uint32_t validB, uint32_t idxA, uint32_t idxB, bool err) {
+    uint32_t pmA = group_mask(tsA, sx, rot, validA);
+    uint32_t pmB = tsB != nullptr ? group_mask(tsB, sx, rot, validB) : 0u;
+    uint32_t cnt = __popc(pmA) + (static_cast<uint32_t>(__popc(pmB)) << kFieldB);
+    uint32_t incl, base, total;
+    publish(cnt, err, incl, base, total);
+    if ((total & kErrMask) != 0u) abort = true;
+    if (abort) return;  // uniform
+    uint32_t tA = total & kFieldMask, tB = (total >> kFieldB) & kFieldMask;
+    if (tA + tB == 0u) return;  // uniform
+    if (n_st + tA + tB > cap) {
+      if (n_st > kk) {  // keep the exact top-k so far and raise the cutoff
+        compact();
+        pmA = group_mask(tsA, sx, rot, validA);
+        pmB = tsB != nullptr ? group_mask(tsB, sx, rot, validB) : 0u;
+        cnt = __popc(pmA) + (static_cast<uint32_t>(__popc(pmB)) << kFieldB);
+        publish(cnt, false, incl, base, total);
+        tA = total & kFieldMask;
+        tB = (total >> kFieldB) & kFieldMask;
+      }
+      if (n_st + tA + tB > cap) {
+        // More hits than the stash has room for, even above a raised cutoff.
+        // Quarters of the group (half the CTA on one stage, at most
+        // kMinStashRoom hits each) append in index order, compacting in
+        // between (a quarter overflows only when the stash holds more than
+        // k entries).
+        for (int part = 0; part < 4; ++part) {
+          const bool second = part >= 2;
+          if (second && tsB == nullptr) break;  // uniform
+          const bool mine = (w >> 2) == (part & 1);
+          const float* ts = second ? tsB : tsA;
+          const uint32_t valid = second ? validB : validA;
+          uint32_t pm = mine ? group_mask(ts, sx, rot, valid) : 0u;
+          uint32_t c = __popc(pm);
+          publish(c, false, incl, base, total);
+          if (n_st + (total & kFieldMask) > cap) {
+            compact();
+            pm = mine ? group_mask(ts, sx, rot, valid) : 0u;
+            c = __popc(pm);
+            publish(c, false, incl, base, total);
+          }
+          write_hits(pm, n_st + (base & kFieldMask) + incl - c, ts, sx, second ? idxB : idxA);
+          n_st += total & kFieldMask;
+        }
+        return;
+      }
+    }
+    const uint32_t before = incl - cnt;  // packed hits of the lower lanes of this warp
+    write_hits(pmA, n_st + (base & kFieldMask) + (before & kFieldMask), tsA, sx, idxA);
+    write_hits(pmB, n_st + tA + ((base >> kFieldB) & kFieldMask) + ((before >> kFieldB) & kFieldMask),
+               tsB, sx, idxB);
+    n_st += tA + tB;
   };
 
   // Scalar group: thread t < cnt holds the score at index first + t.
   auto scalar_group = [&](int first, int cnt) {
-    const float ninf = -__int_as_float(0x7f800000);
-    float4 v[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) v[j] = make_float4(ninf, ninf, ninf, ninf);
+    float sx = 0.0f;
     uint32_t valid = 0;
     if (t < cnt) {
-      v[0].x = rp[first + t];
+      sx = rp[first + t];
       valid = 1u;
     }
-    process_group(v, 0, valid, static_cast<uint32_t>(first + t), false, nullptr);
+    process_group(nullptr, nullptr, sx, 0, valid, 0u, static_cast<uint32_t>(first + t), 0u, false);
+  };
+
+  // Takes stage j from the ring: waits for it (bounded) and returns this
+  // thread's 16 scores in it, with the mask of those present.
+  auto take_stage = [&](int j, bool& err, uint32_t& valid, uint32_t& slot) -> const float* {
+    slot = consumed % kStages;
+    const uint32_t parity = (consumed / kStages) & 1u;
+    ++consumed;
+    if (!abort) {
+      if (j - s0 == p.probe_stage) {
+        err |= !mbar_wait_bounded(&S.never, 0u, 1000ull * p.probe_wait_us);  // runs out
+      } else if (mbar_wait_bounded(&S.full[slot], parity, kWaitLimitNs)) {
+        ++t0_seen;  // in order: stages [t0_seen, issued) are unobserved
+      } else {
+        err = true;
+      }
+    }
+    const int cnt = min(kStageFloats, nb - j * kStageFloats);
+    const int have = cnt - kPerThread * t;
+    valid = have >= kPerThread ? 0xffffu : (have <= 0 ? 0u : (1u << have) - 1u);
+    return &S.ring[slot][kPerThread * t];
   };
 
   auto stream_pass = [&]() {
-    const float ninf = -__int_as_float(0x7f800000);
     const int rot = (t >> 1) & 3;  // rotates the float4 order: conflict-free shared loads
     if (rank == 0 && h > 0) scalar_group(0, h);
-    for (int j = s0; j < s1; ++j) {
-      const uint32_t slot = consumed % kStages;
-      const uint32_t parity = (consumed / kStages) & 1u;
+    for (int j = s0; j < s1; j += 2) {
+      const bool two = j + 1 < s1;
       bool err = false;
-      if (!abort) {
-        if (j - s0 == p.probe_stage) {
-          err = !mbar_wait_bounded(&S.never, 0u, 1000ull * p.probe_wait_us);  // runs out
-        } else {
-          err = !mbar_wait_bounded(&S.full[slot], parity, kWaitLimitNs);
-          if (!err) ++t0_seen;  // in order: stages [t0_seen, issued) are unobserved
-        }
-      }
-      const int cnt = min(kStageFloats, nb - j * kStageFloats);
-      const float* ts = &S.ring[slot][kPerThread * t];
-      float4 v[4];
-      uint32_t valid = 0xffffu;
-      if (cnt == kStageFloats) {
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj)
-          v[jj] = *reinterpret_cast<const float4*>(ts + 4 * ((jj + rot) & 3));
-      } else {
-        valid = 0;
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const int q = (jj + rot) & 3;
-          if (kPerThread * t + 4 * q < cnt) {
-            v[jj] = *reinterpret_cast<const float4*>(ts + 4 * q);
-            valid |= 0xfu << (4 * q);
-          } else {
-            v[jj] = make_float4(ninf, ninf, ninf, ninf);
-          }
-        }
-      }
-      ++consumed;
-      process_group(v, rot, valid, static_cast<uint32_t>(h + j * kStageFloats + kPerThread * t), err,
-                    ts);
-      release_slot(j, slot);
+      uint32_t validA, validB = 0, slotA, slotB;
+      const float* tsA = take_stage(j, err, validA, slotA);
+      const float* tsB = two ? take_stage(j + 1, err, validB, slotB) : nullptr;
+      const uint32_t idxA = static_cast<uint32_t>(h + j * kStageFloats + kPerThread * t);
+      process_group(tsA, tsB, 0.0f, rot, validA, validB, idxA, idxA + kStageFloats, err);
+      release_slots(j, slotA, two);
     }
     if (rank == G - 1 && tail > 0) scalar_group(h + nb, tail);
   };

@@ -75,14 +75,17 @@ def test_forced_paths(k, sample_mode, cluster):
     check_against_oracle(scores, lengths, k, sample_mode=sample_mode, cluster_size=cluster)
 
 
-@pytest.mark.parametrize("k", [512, 2048])
+@pytest.mark.parametrize("k", [512, 1024, 2048])
 @pytest.mark.parametrize("cluster", [1, 4])
 def test_compaction_path(k, cluster):
-    """Smallest candidate buffer: the in-buffer compaction runs many times."""
+    """Smallest candidate buffer (k + 2048 entries): the in-buffer compaction
+    runs many times, and on the ascending rows the hits of one group exceed
+    the room left even after compaction, so quarters of the group append in
+    turn."""
     scores, lengths = _mixed_rows()
     cnt = counters_tensor()
     check_against_oracle(scores, lengths, k, sample_mode=1, cluster_size=cluster,
-                         stash_capacity=k + 4096, counters=cnt)
+                         stash_capacity=k + 2048, counters=cnt)
     assert int(cnt[tk.Counter.COMPACTIONS]) > 0
 
 
@@ -114,7 +117,7 @@ def test_capacity_boundaries_without_sampling():
     """Row lengths around the candidate-buffer capacity: the buffer fills
     exactly, one short of, and one past its end."""
     rng = np.random.default_rng(11)
-    for k, cap in ((512, 4608), (1024, 5120), (2048, 6144)):
+    for k, cap in ((512, 4608), (1024, 5120), (2048, 5120)):
         ns = [cap - 1, cap, cap + 1, cap + 2047, cap + 2048, cap + 2049, 2 * cap + 5]
         stride = max(ns) + 3
         scores = rng.standard_normal((len(ns), stride)).astype(np.float32)
