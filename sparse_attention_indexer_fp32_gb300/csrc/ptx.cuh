@@ -107,6 +107,11 @@ __device__ __forceinline__ void bulk_load(void* dst_smem, const void* src_gmem, 
 
 // ---- thread-block clusters --------------------------------------------------
 
+// Hint to bring the 128-byte line holding *p into L2 (no data returned).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));

@@ -128,10 +128,14 @@ topk_status select_impl(const float* scores, int64_t stride, const int32_t* leng
   if (G == 0) G = auto_cluster_size(B, stride, info->sm_count);
   if (static_cast<int64_t>(B) * G > INT32_MAX) return TOPK_EINVAL;
 
+  const bool paged = page_table != nullptr;
   switch (kmax) {
-    case 512: return tki::launch_k512(p, G, dev, stream);
-    case 1024: return tki::launch_k1024(p, G, dev, stream);
-    default: return tki::launch_k2048(p, G, dev, stream);
+    case 512: return paged ? tki::launch_k512_paged(p, G, dev, stream)
+                           : tki::launch_k512_ragged(p, G, dev, stream);
+    case 1024: return paged ? tki::launch_k1024_paged(p, G, dev, stream)
+                            : tki::launch_k1024_ragged(p, G, dev, stream);
+    default: return paged ? tki::launch_k2048_paged(p, G, dev, stream)
+                          : tki::launch_k2048_ragged(p, G, dev, stream);
   }
 }
 

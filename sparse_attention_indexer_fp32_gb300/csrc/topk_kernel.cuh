@@ -367,7 +367,9 @@ __device__ void emit_rounds(Smem<C>& S, int n, Cut cut, uint32_t gt0, uint32_t e
   }
 }
 
-template <int KMAX, int G>
+// PAGED: the output indices go through the page table (p.page_table is
+// not null); the ragged kernel carries no page-table code at all.
+template <int KMAX, int G, bool PAGED>
 __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) {
   constexpr int C = StashCap<KMAX>::value;
   extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -380,12 +382,11 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
   const int64_t len_raw = p.lengths[row];
   const int n = static_cast<int>(len_raw < 0 ? 0 : (len_raw > p.stride ? p.stride : len_raw));
   int32_t* out_row = p.out + static_cast<int64_t>(row) * p.k;
-  const int32_t* pt_row =
-      p.page_table == nullptr ? nullptr : p.page_table + static_cast<int64_t>(row) * p.pt_stride;
+  const int32_t* pt_row = PAGED ? p.page_table + static_cast<int64_t>(row) * p.pt_stride : nullptr;
   const bool leader = (t == 0 && rank == 0);
 
   auto map_index = [&](uint32_t i) -> int32_t {
-    if (pt_row == nullptr) return static_cast<int32_t>(i);
+    if constexpr (!PAGED) return static_cast<int32_t>(i);
     const uint32_t ps = static_cast<uint32_t>(p.page_size);
     const uint32_t page = i / ps;
     return static_cast<int32_t>(static_cast<int64_t>(pt_row[page]) * ps + (i - page * ps));
@@ -788,6 +789,16 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
   }
 
   // ---- exact cutoff over the stash(es) and emission --------------------------
+  if (PAGED && !abort) {
+    // The emission maps every selected index through the page table: start
+    // bringing this CTA's part of the table row into L2 while the cutoff is
+    // found (one line per 32 entries).
+    const int first = rank == 0 ? 0 : h + s0 * kStageFloats;
+    const int last = rank == G - 1 ? n : h + s1 * kStageFloats;
+    const int p0 = first / p.page_size, p1 = (last + p.page_size - 1) / p.page_size;
+    for (int q = p0 + 32 * t; q < p1; q += 32 * kThreads) prefetch_l2(pt_row + q);
+    if (t == 0 && p1 > p0) prefetch_l2(pt_row + p1 - 1);  // the last line, if no start fell in it
+  }
   const Cut cut = select_stash<G>(S, static_cast<int>(n_st), kk);
   uint32_t gt0 = 0, eq0 = 0;
   if constexpr (G > 1) {

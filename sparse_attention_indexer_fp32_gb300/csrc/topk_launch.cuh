@@ -13,19 +13,19 @@
 namespace tki {
 
 // Per variant, bit d set once the kernel's shared-memory attribute is set on device d.
-template <int KMAX, int G>
+template <int KMAX, int G, bool PAGED>
 std::atomic<uint64_t>& attr_flags() {
   static std::atomic<uint64_t> flags{0};
   return flags;
 }
 
-template <int KMAX, int G>
+template <int KMAX, int G, bool PAGED>
 topk_status launch_variant(const Params& p, int dev, cudaStream_t stream) {
   constexpr int C = StashCap<KMAX>::value;
-  auto kernel = topk_rows_kernel<KMAX, G>;
+  auto kernel = topk_rows_kernel<KMAX, G, PAGED>;
   const size_t smem = sizeof(Smem<C>);
   const uint64_t bit = 1ull << dev;
-  std::atomic<uint64_t>& flags = attr_flags<KMAX, G>();
+  std::atomic<uint64_t>& flags = attr_flags<KMAX, G, PAGED>();
   if ((flags.load(std::memory_order_acquire) & bit) == 0) {
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
@@ -49,20 +49,25 @@ topk_status launch_variant(const Params& p, int dev, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, kernel, p) == cudaSuccess ? TOPK_OK : TOPK_ECUDA;
 }
 
-template <int KMAX>
-topk_status launch_bucket(const Params& p, int G, int dev, cudaStream_t stream) {
+template <int KMAX, bool PAGED>
+topk_status launch_cluster(const Params& p, int G, int dev, cudaStream_t stream) {
   switch (G) {
-    case 1: return launch_variant<KMAX, 1>(p, dev, stream);
-    case 2: return launch_variant<KMAX, 2>(p, dev, stream);
-    case 4: return launch_variant<KMAX, 4>(p, dev, stream);
-    case 8: return launch_variant<KMAX, 8>(p, dev, stream);
+    case 1: return launch_variant<KMAX, 1, PAGED>(p, dev, stream);
+    case 2: return launch_variant<KMAX, 2, PAGED>(p, dev, stream);
+    case 4: return launch_variant<KMAX, 4, PAGED>(p, dev, stream);
+    case 8: return launch_variant<KMAX, 8, PAGED>(p, dev, stream);
     default: return TOPK_EINVAL;
   }
 }
 
-// Defined in topk_k512.cu, topk_k1024.cu and topk_k2048.cu.
-topk_status launch_k512(const Params& p, int G, int dev, cudaStream_t stream);
-topk_status launch_k1024(const Params& p, int G, int dev, cudaStream_t stream);
-topk_status launch_k2048(const Params& p, int G, int dev, cudaStream_t stream);
+
+// Defined in topk_k{512,1024,2048}_{ragged,paged}.cu, one translation unit
+// each so that they compile in parallel.
+topk_status launch_k512_ragged(const Params& p, int G, int dev, cudaStream_t stream);
+topk_status launch_k512_paged(const Params& p, int G, int dev, cudaStream_t stream);
+topk_status launch_k1024_ragged(const Params& p, int G, int dev, cudaStream_t stream);
+topk_status launch_k1024_paged(const Params& p, int G, int dev, cudaStream_t stream);
+topk_status launch_k2048_ragged(const Params& p, int G, int dev, cudaStream_t stream);
+topk_status launch_k2048_paged(const Params& p, int G, int dev, cudaStream_t stream);
 
 }  // namespace tki
