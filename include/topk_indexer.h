@@ -52,6 +52,7 @@
 #ifndef TOPK_INDEXER_H_
 #define TOPK_INDEXER_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -106,6 +107,50 @@ topk_status topk_paged(const float* scores, int64_t stride, const int32_t* lengt
                        int32_t k, const int32_t* page_table, int64_t pt_stride,
                        int32_t page_size, int32_t* out, topk_stream_t stream);
 
+/*
+ * Workspace variants. In a large batch the rows that start last run while
+ * most of the GPU has nothing left to do. topk_ragged_ws / topk_paged_ws
+ * stream some of those rows with two CTAs each: every CTA finds the exact
+ * top-k of its half of the row (same order, same lowest-index tie rule) and
+ * leaves it in the workspace; the half that finishes second merges the two
+ * and writes the row. No CTA waits for another. Results are identical to
+ * topk_ragged / topk_paged, bit for bit and slot for slot. This split of a
+ * row over independent CTAs is this library's own scheduling device; the
+ * pages' cluster split (sglang PR 39648 report, 实现拆解 4) needs the CTAs of a
+ * row to run together.
+ *
+ * The library chooses how many rows to split from B and the SM count (none
+ * when the batch leaves no idle slot, or when rows are short), at most as
+ * many as the workspace holds.
+ *
+ *   workspace        DEVICE memory owned by the caller, 16-byte aligned, at
+ *                    least 12 KiB. Its first 4 KiB must be zero before its
+ *                    first use, and every call that completes leaves them zero
+ *                    again; the rest is scratch. NULL: no row is split (the
+ *                    call is then topk_ragged / topk_paged).
+ *   workspace_bytes  its size; topk_workspace_bytes tells how much lets every
+ *                    row the library would split be split
+ *
+ * Calls that may run at the same time on the GPU (other streams, concurrent
+ * graph launches) need different workspaces: they would race on it.
+ */
+topk_status topk_ragged_ws(const float* scores, int64_t stride, const int32_t* lengths,
+                           int32_t B, int32_t k, int32_t* out, void* workspace,
+                           size_t workspace_bytes, topk_stream_t stream);
+topk_status topk_paged_ws(const float* scores, int64_t stride, const int32_t* lengths,
+                          int32_t B, int32_t k, const int32_t* page_table, int64_t pt_stride,
+                          int32_t page_size, int32_t* out, void* workspace,
+                          size_t workspace_bytes, topk_stream_t stream);
+
+/*
+ * topk_workspace_bytes - writes to *bytes the workspace size that lets a call
+ * with this k split up to max_split_rows rows (0 = the most the library ever
+ * splits on the current device: its SM count; at most 1024). Errors:
+ * TOPK_EUNSUPPORTED_K, TOPK_EINVAL (bytes NULL, max_split_rows out of range),
+ * TOPK_ECUDA / TOPK_EDEVICE (device query).
+ */
+topk_status topk_workspace_bytes(int32_t k, int32_t max_split_rows, size_t* bytes);
+
 /* Static, human-readable description of a status code. */
 const char* topk_status_string(topk_status status);
 
@@ -139,15 +184,21 @@ int32_t topk_abi_version(void);
  *                   (TOPK_DEVICE_ERROR_INDEX in every slot, counted). This
  *                   tests the bounded waits without a real fault; results of
  *                   such a call are not a selection.
+ *   split_rows      0 automatic; -1 split no row; m > 0 split exactly the last
+ *                   m rows (m <= B, the workspace must hold them; forces one
+ *                   CTA per row, so cluster_size must be 0 or 1)
+ *   workspace,      as for topk_ragged_ws; NULL = none (no row is split, and
+ *   workspace_bytes split_rows must be 0 or -1)
  */
 typedef enum topk_counter {
   TOPK_CNT_ROWS = 0,          /* rows handled */
   TOPK_CNT_TRIVIAL = 1,       /* rows with length <= k (no selection needed) */
   TOPK_CNT_SAMPLED = 2,       /* rows that streamed against a sampled cutoff */
-  TOPK_CNT_RESCAN = 3,        /* rows rescanned because the cutoff kept too few */
+  TOPK_CNT_RESCAN = 3,        /* rows (halves of split rows) rescanned because the cutoff kept too few */
   TOPK_CNT_COMPACTIONS = 4,   /* candidate-buffer compactions (summed over CTAs) */
   TOPK_CNT_DEVICE_ERRORS = 5, /* CTAs whose waits timed out */
   TOPK_CNT_CLUSTER_ROWS = 6,  /* rows split over a cluster of CTAs */
+  TOPK_CNT_SPLIT_ROWS = 7,    /* rows streamed by two independent CTAs and merged */
   TOPK_NUM_COUNTERS = 8
 } topk_counter;
 
@@ -159,6 +210,9 @@ typedef struct topk_debug_opts {
   uint32_t* counters;
   int32_t probe_stage;
   uint32_t probe_wait_us;
+  int32_t split_rows;
+  void* workspace;
+  size_t workspace_bytes;
 } topk_debug_opts;
 
 topk_status topk_select_ex(const float* scores, int64_t stride, const int32_t* lengths,

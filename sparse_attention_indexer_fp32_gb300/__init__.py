@@ -23,8 +23,10 @@ from ._binding import (  # noqa: F401
     topk_paged,
     topk_ragged,
     topk_select_ex,
+    workspace_bytes,
 )
 
-__all__ = ["topk_ragged", "topk_paged", "topk_select_ex", "TopkError", "Status", "Counter",
+__all__ = ["topk_ragged", "topk_paged", "topk_select_ex", "workspace_bytes", "TopkError",
+           "Status", "Counter",
            "load_library", "raw_library", "LIB_PATH", "TOPK_MAX_K", "NUM_COUNTERS",
            "DEVICE_ERROR_INDEX"]

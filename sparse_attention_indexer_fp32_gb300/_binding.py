@@ -40,6 +40,7 @@ class Counter(enum.IntEnum):
     COMPACTIONS = 4
     DEVICE_ERRORS = 5
     CLUSTER_ROWS = 6
+    SPLIT_ROWS = 7
 
 
 NUM_COUNTERS = 8
@@ -55,7 +56,8 @@ class _DebugOpts(ctypes.Structure):
     _fields_ = [("sample_mode", ctypes.c_int32), ("cluster_size", ctypes.c_int32),
                 ("stash_capacity", ctypes.c_int32), ("sample_z", ctypes.c_float),
                 ("counters", ctypes.c_void_p), ("probe_stage", ctypes.c_int32),
-                ("probe_wait_us", ctypes.c_uint32)]
+                ("probe_wait_us", ctypes.c_uint32), ("split_rows", ctypes.c_int32),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
 
 
 _lib = None
@@ -83,6 +85,13 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.topk_select_ex.argtypes = [vp, i64, vp, i32, i32, vp, i64, i32, vp,
                                        ctypes.POINTER(_DebugOpts), vp]
         lib.topk_select_ex.restype = ctypes.c_int
+        sz = ctypes.c_size_t
+        lib.topk_ragged_ws.argtypes = [vp, i64, vp, i32, i32, vp, vp, sz, vp]
+        lib.topk_ragged_ws.restype = ctypes.c_int
+        lib.topk_paged_ws.argtypes = [vp, i64, vp, i32, i32, vp, i64, i32, vp, vp, sz, vp]
+        lib.topk_paged_ws.restype = ctypes.c_int
+        lib.topk_workspace_bytes.argtypes = [i32, i32, ctypes.POINTER(sz)]
+        lib.topk_workspace_bytes.restype = ctypes.c_int
         lib.topk_status_string.argtypes = [ctypes.c_int]
         lib.topk_status_string.restype = ctypes.c_char_p
         lib.topk_abi_version.restype = ctypes.c_int32
@@ -100,6 +109,30 @@ def _stream_handle(device: torch.device, stream) -> int:
     if stream is None:
         stream = torch.cuda.current_stream(device)
     return int(stream.cuda_stream)
+
+
+def workspace_bytes(k: int = TOPK_MAX_K, max_split_rows: int = 0) -> int:
+    """Workspace size for calls with this k that split up to
+    ``max_split_rows`` rows (0: the most the library splits on the current
+    device)."""
+    out = ctypes.c_size_t(0)
+    _check(load_library().topk_workspace_bytes(int(k), int(max_split_rows), ctypes.byref(out)))
+    return int(out.value)
+
+
+# One zero-initialised workspace per (device, stream): calls on one stream run
+# one after another, so they can share it; the library leaves its counters
+# zero after every call.
+_workspaces = {}
+
+
+def _workspace(device: torch.device, stream_handle: int) -> torch.Tensor:
+    key = (device.index, stream_handle)
+    ws = _workspaces.get(key)
+    if ws is None:
+        ws = torch.zeros(workspace_bytes(TOPK_MAX_K), dtype=torch.uint8, device=device)
+        _workspaces[key] = ws
+    return ws
 
 
 def _prepare(scores: torch.Tensor, lengths: torch.Tensor, k: int, out: Optional[torch.Tensor]):
@@ -121,22 +154,33 @@ def _prepare(scores: torch.Tensor, lengths: torch.Tensor, k: int, out: Optional[
 
 
 def topk_ragged(scores: torch.Tensor, lengths: torch.Tensor, k: int,
-                out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                out: Optional[torch.Tensor] = None, stream=None,
+                split: bool = True) -> torch.Tensor:
     """Indices of the ``min(k, lengths[b])`` largest scores of every row, ``-1`` after them.
 
     ``scores`` float32 ``[B, stride]`` (CUDA, contiguous), ``lengths`` int32
     ``[B]``. Returns ``out`` (int32 ``[B, k]``), enqueued on ``stream`` (default:
-    the current stream)."""
+    the current stream). With ``split`` (the default) the call goes through
+    ``topk_ragged_ws`` with a workspace cached per device and stream, so that
+    the last rows of a large batch may be split over two CTAs; the result is
+    the same either way."""
     lib = load_library()
     B, stride, out = _prepare(scores, lengths, k, out)
     with torch.cuda.device(scores.device):
-        _check(lib.topk_ragged(scores.data_ptr(), stride, lengths.data_ptr(), B, k,
-                               out.data_ptr(), _stream_handle(scores.device, stream)))
+        sh = _stream_handle(scores.device, stream)
+        if split:
+            ws = _workspace(scores.device, sh)
+            _check(lib.topk_ragged_ws(scores.data_ptr(), stride, lengths.data_ptr(), B, k,
+                                      out.data_ptr(), ws.data_ptr(), ws.numel(), sh))
+        else:
+            _check(lib.topk_ragged(scores.data_ptr(), stride, lengths.data_ptr(), B, k,
+                                   out.data_ptr(), sh))
     return out
 
 
 def topk_paged(scores: torch.Tensor, lengths: torch.Tensor, k: int, page_table: torch.Tensor,
-               page_size: int, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+               page_size: int, out: Optional[torch.Tensor] = None, stream=None,
+               split: bool = True) -> torch.Tensor:
     """As :func:`topk_ragged`, each selected index ``i`` of row ``b`` written as
     ``page_table[b, i // page_size] * page_size + i % page_size``."""
     lib = load_library()
@@ -145,9 +189,16 @@ def topk_paged(scores: torch.Tensor, lengths: torch.Tensor, k: int, page_table: 
             or page_table.dim() != 2 or page_table.shape[0] != B or not page_table.is_contiguous()):
         raise ValueError("page_table must be a contiguous int32 tensor [B, pages] on the scores' device")
     with torch.cuda.device(scores.device):
-        _check(lib.topk_paged(scores.data_ptr(), stride, lengths.data_ptr(), B, k,
-                              page_table.data_ptr(), page_table.shape[1], page_size,
-                              out.data_ptr(), _stream_handle(scores.device, stream)))
+        sh = _stream_handle(scores.device, stream)
+        if split:
+            ws = _workspace(scores.device, sh)
+            _check(lib.topk_paged_ws(scores.data_ptr(), stride, lengths.data_ptr(), B, k,
+                                     page_table.data_ptr(), page_table.shape[1], page_size,
+                                     out.data_ptr(), ws.data_ptr(), ws.numel(), sh))
+        else:
+            _check(lib.topk_paged(scores.data_ptr(), stride, lengths.data_ptr(), B, k,
+                                  page_table.data_ptr(), page_table.shape[1], page_size,
+                                  out.data_ptr(), sh))
     return out
 
 
@@ -156,10 +207,13 @@ def topk_select_ex(scores: torch.Tensor, lengths: torch.Tensor, k: int,
                    out: Optional[torch.Tensor] = None, *, sample_mode: int = 0,
                    cluster_size: int = 0, stash_capacity: int = 0, sample_z: float = 0.0,
                    counters: Optional[torch.Tensor] = None, probe_stage: int = 0,
-                   probe_wait_us: int = 0, stream=None) -> torch.Tensor:
+                   probe_wait_us: int = 0, split_rows: int = 0,
+                   workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """Diagnostic variant: same result, with the internal path forced (see the
     header's ``topk_debug_opts``). ``counters`` is an optional int32/uint32
-    CUDA tensor of ``NUM_COUNTERS`` entries that the kernel increments."""
+    CUDA tensor of ``NUM_COUNTERS`` entries that the kernel increments;
+    ``workspace`` an optional uint8 CUDA tensor (first 4 KiB zero) that lets
+    rows be split (``split_rows``)."""
     lib = load_library()
     B, stride, out = _prepare(scores, lengths, k, out)
     pt_ptr, pt_stride = None, 0
@@ -167,8 +221,13 @@ def topk_select_ex(scores: torch.Tensor, lengths: torch.Tensor, k: int,
         if page_table.dtype != torch.int32 or not page_table.is_contiguous():
             raise ValueError("page_table must be contiguous int32")
         pt_ptr, pt_stride = page_table.data_ptr(), page_table.shape[1]
+    if workspace is not None and (not workspace.is_cuda or workspace.dtype != torch.uint8
+                                  or not workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous uint8 CUDA tensor")
     opts = _DebugOpts(sample_mode, cluster_size, stash_capacity, sample_z,
-                      None if counters is None else counters.data_ptr(), probe_stage, probe_wait_us)
+                      None if counters is None else counters.data_ptr(), probe_stage, probe_wait_us,
+                      split_rows, None if workspace is None else workspace.data_ptr(),
+                      0 if workspace is None else workspace.numel())
     if counters is not None and (counters.numel() < NUM_COUNTERS or not counters.is_cuda
                                  or counters.element_size() != 4):
         raise ValueError("counters must be a 4-byte CUDA tensor of NUM_COUNTERS entries")

@@ -19,6 +19,34 @@ constexpr int kDefaultSampleMinN = 16384;
 constexpr float kDefaultSampleZ = 6.0f;
 // A cluster slice should hold at least this many scores to be worth a CTA.
 constexpr int64_t kMinClusterSlice = 16384;
+// Workspace layout: per split row one arrival counter (the first 4 KiB,
+// which persist between calls and are zero outside a call), two hand-over
+// counts (the next 8 KiB), then per split row and half k keys and k indices.
+constexpr int kMaxSplitRows = 1024;
+constexpr size_t kWsCounterBytes = 4 * kMaxSplitRows;
+constexpr size_t kWsHeaderBytes = kWsCounterBytes + 8 * kMaxSplitRows;
+// Resident CTAs per SM (shared memory and the launch bounds fix two).
+constexpr int kCtasPerSm = 2;
+
+size_t ws_bytes_for(int32_t k, int64_t split_rows) {
+  return kWsHeaderBytes + static_cast<size_t>(split_rows) * 2 * static_cast<size_t>(k) * 8;
+}
+
+// Rows narrower than this are not split: each half pays the fixed costs of
+// a row (sampling, hand-over, and for one of them the merge), which on GB300
+// outweighs the shorter tail unless a half still streams ~80K scores or more
+// (measured: a gain at width 262144, a loss at 131072).
+constexpr int64_t kMinSplitWidth = 196608;
+
+// Rows to split: enough of the last ones to fill the slots that the final
+// partial wave of one-CTA rows leaves idle, and no more (each split row takes
+// two slots).
+int auto_split_rows(int32_t B, int64_t stride, int sm_count) {
+  const int64_t slots = static_cast<int64_t>(kCtasPerSm) * sm_count;
+  if (stride < kMinSplitWidth || slots <= 0) return 0;
+  const int64_t r = B >= slots ? B % slots : B;
+  return static_cast<int>(r < slots - r ? r : slots - r);
+}
 
 struct DeviceInfo {
   std::once_flag once;
@@ -64,7 +92,8 @@ bool aligned4(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 3u) 
 
 topk_status select_impl(const float* scores, int64_t stride, const int32_t* lengths, int32_t B,
                         int32_t k, const int32_t* page_table, int64_t pt_stride, int32_t page_size,
-                        int32_t* out, const topk_debug_opts* opts, cudaStream_t stream) {
+                        int32_t* out, void* workspace, size_t workspace_bytes,
+                        const topk_debug_opts* opts, cudaStream_t stream) {
   if (B < 0 || stride < 1 || stride > INT32_MAX) return TOPK_EINVAL;
   if (k < 1 || k > TOPK_MAX_K) return TOPK_EUNSUPPORTED_K;
   if (B == 0) return TOPK_OK;
@@ -97,8 +126,10 @@ topk_status select_impl(const float* scores, int64_t stride, const int32_t* leng
   p.counters = nullptr;
   p.probe_stage = -1;
   p.probe_wait_us = 0;
+  p.split_first = B;
 
   int G = 0;
+  int split_rows = 0;  // 0 automatic, -1 never, m > 0 forced
   if (opts != nullptr) {
     if (opts->sample_mode < 0 || opts->sample_mode > 2) return TOPK_EINVAL;
     p.sample_mode = opts->sample_mode;
@@ -119,14 +150,52 @@ topk_status select_impl(const float* scores, int64_t stride, const int32_t* leng
     if (opts->probe_wait_us > 5000000u) return TOPK_EINVAL;  // the probe wait stays short
     p.probe_stage = opts->probe_stage - 1;
     p.probe_wait_us = opts->probe_wait_us;
+    if (opts->split_rows < -1 || opts->split_rows > B) return TOPK_EINVAL;
+    split_rows = opts->split_rows;
+    if (split_rows > 0 && G > 1) return TOPK_EINVAL;
+    if (workspace != nullptr && opts->workspace != nullptr) return TOPK_EINVAL;
+    if (opts->workspace != nullptr) {
+      workspace = opts->workspace;
+      workspace_bytes = opts->workspace_bytes;
+    }
+  }
+  if (workspace != nullptr) {
+    if ((reinterpret_cast<uintptr_t>(workspace) & 15u) != 0 || workspace_bytes < kWsHeaderBytes)
+      return TOPK_EINVAL;
+  } else if (split_rows > 0) {
+    return TOPK_EINVAL;
   }
 
   int dev = 0;
   DeviceInfo* info = nullptr;
   const topk_status st = device_info(&dev, &info);
   if (st != TOPK_OK) return st;
+  if (split_rows > 0) G = 1;
   if (G == 0) G = auto_cluster_size(B, stride, info->sm_count);
   if (static_cast<int64_t>(B) * G > INT32_MAX) return TOPK_EINVAL;
+
+  // Split rows: the last m rows each run as two independent CTAs.
+  if (workspace != nullptr && G == 1 && split_rows >= 0) {
+    const int64_t room = static_cast<int64_t>((workspace_bytes - kWsHeaderBytes) /
+                                              (static_cast<size_t>(k) * 16));
+    const int64_t hold = room < kMaxSplitRows ? room : kMaxSplitRows;
+    int64_t m = split_rows;
+    if (m == 0) {
+      m = auto_split_rows(B, stride, info->sm_count);
+      if (m > hold) m = hold;
+    } else if (m > hold) {
+      return TOPK_EINVAL;
+    }
+    if (static_cast<int64_t>(B) + m > INT32_MAX) return TOPK_EINVAL;
+    if (m > 0) {
+      unsigned char* ws = static_cast<unsigned char*>(workspace);
+      p.split_first = B - static_cast<int32_t>(m);
+      p.ws_ctr = reinterpret_cast<uint32_t*>(ws);
+      p.ws_cnt = reinterpret_cast<uint32_t*>(ws + kWsCounterBytes);
+      p.ws_key = reinterpret_cast<uint32_t*>(ws + kWsHeaderBytes);
+      p.ws_idx = p.ws_key + static_cast<size_t>(m) * 2 * static_cast<size_t>(k);
+    }
+  }
 
   const bool paged = page_table != nullptr;
   switch (kmax) {
@@ -145,8 +214,40 @@ extern "C" {
 
 topk_status topk_ragged(const float* scores, int64_t stride, const int32_t* lengths, int32_t B,
                         int32_t k, int32_t* out, topk_stream_t stream) {
-  return select_impl(scores, stride, lengths, B, k, nullptr, 0, 0, out, nullptr,
+  return select_impl(scores, stride, lengths, B, k, nullptr, 0, 0, out, nullptr, 0, nullptr,
                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+topk_status topk_ragged_ws(const float* scores, int64_t stride, const int32_t* lengths, int32_t B,
+                           int32_t k, int32_t* out, void* workspace, size_t workspace_bytes,
+                           topk_stream_t stream) {
+  return select_impl(scores, stride, lengths, B, k, nullptr, 0, 0, out, workspace,
+                     workspace_bytes, nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+topk_status topk_paged_ws(const float* scores, int64_t stride, const int32_t* lengths, int32_t B,
+                          int32_t k, const int32_t* page_table, int64_t pt_stride,
+                          int32_t page_size, int32_t* out, void* workspace,
+                          size_t workspace_bytes, topk_stream_t stream) {
+  if (page_table == nullptr && B > 0) return TOPK_EINVAL;
+  if (page_size < 1 || pt_stride < 1) return TOPK_EINVAL;
+  return select_impl(scores, stride, lengths, B, k, page_table, pt_stride, page_size, out,
+                     workspace, workspace_bytes, nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+topk_status topk_workspace_bytes(int32_t k, int32_t max_split_rows, size_t* bytes) {
+  if (k < 1 || k > TOPK_MAX_K) return TOPK_EUNSUPPORTED_K;
+  if (bytes == nullptr || max_split_rows < 0 || max_split_rows > kMaxSplitRows) return TOPK_EINVAL;
+  int64_t m = max_split_rows;
+  if (m == 0) {
+    int dev = 0;
+    DeviceInfo* info = nullptr;
+    const topk_status st = device_info(&dev, &info);
+    if (st != TOPK_OK) return st;
+    m = info->sm_count < kMaxSplitRows ? info->sm_count : kMaxSplitRows;
+  }
+  *bytes = ws_bytes_for(k, m);
+  return TOPK_OK;
 }
 
 topk_status topk_paged(const float* scores, int64_t stride, const int32_t* lengths, int32_t B,
@@ -155,15 +256,15 @@ topk_status topk_paged(const float* scores, int64_t stride, const int32_t* lengt
   if (page_table == nullptr && B > 0) return TOPK_EINVAL;
   if (page_size < 1 || pt_stride < 1) return TOPK_EINVAL;
   return select_impl(scores, stride, lengths, B, k, page_table, pt_stride, page_size, out,
-                     nullptr, reinterpret_cast<cudaStream_t>(stream));
+                     nullptr, 0, nullptr, reinterpret_cast<cudaStream_t>(stream));
 }
 
 topk_status topk_select_ex(const float* scores, int64_t stride, const int32_t* lengths, int32_t B,
                            int32_t k, const int32_t* page_table, int64_t pt_stride,
                            int32_t page_size, int32_t* out, const topk_debug_opts* opts,
                            topk_stream_t stream) {
-  return select_impl(scores, stride, lengths, B, k, page_table, pt_stride, page_size, out, opts,
-                     reinterpret_cast<cudaStream_t>(stream));
+  return select_impl(scores, stride, lengths, B, k, page_table, pt_stride, page_size, out,
+                     nullptr, 0, opts, reinterpret_cast<cudaStream_t>(stream));
 }
 
 const char* topk_status_string(topk_status status) {
@@ -177,6 +278,6 @@ const char* topk_status_string(topk_status status) {
   }
 }
 
-int32_t topk_abi_version(void) { return 1; }
+int32_t topk_abi_version(void) { return 2; }
 
 }  // extern "C"

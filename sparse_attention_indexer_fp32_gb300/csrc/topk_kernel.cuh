@@ -56,7 +56,8 @@ constexpr int kSampleVec4 = 1024;                    // 4096 sampled scores ...
 constexpr int kSampleChunkVec4 = 64;                 // ... in 16 chunks of 256
 constexpr int kSampleChunks = kSampleVec4 / kSampleChunkVec4;
 constexpr int kBins = 2048;
-constexpr int kRoundEntries = 4 * kThreads;          // stash entries per emission round
+constexpr int kRoundPerThread = 4;                    // stash entries per thread per round ...
+constexpr int kRoundEntries = kRoundPerThread * kThreads;  // ... of emission and histograms
 constexpr uint64_t kWaitLimitNs = 2000000000ull;     // 2 s: far beyond any stage latency
 // Packed per-warp hit counts of a pair of stages: stage A in bits [0, 13),
 // stage B in bits [17, 30) (each at most one stage, 4096 < 2^13), and the
@@ -77,14 +78,22 @@ enum : int {
   kCntCompactions = 4,
   kCntDeviceErrors = 5,
   kCntClusterRows = 6,
+  kCntSplitRows = 7,
 };
+
+// Entry count a split-row half hands over when one of its waits timed out.
+constexpr uint32_t kHalfFailed = 0xffffffffu;
 
 template <int KMAX>
 struct StashCap {
+  // (a multiple of kRoundPerThread, as the round reads assume)
   // Room for k kept candidates plus the new ones of one stage, at most 5120
   // entries so that two CTAs with a four-stage ring fit on an SM.
   static constexpr int value = KMAX + kStageFloats < 5120 ? KMAX + kStageFloats : 5120;
 };
+static_assert(StashCap<512>::value % kRoundPerThread == 0 && StashCap<1024>::value % kRoundPerThread == 0 &&
+                  StashCap<2048>::value % kRoundPerThread == 0,
+              "round reads must stay inside the stash");
 // Smallest stash capacity beyond k: the hits of half a CTA on one stage.
 constexpr int kMinStashRoom = kStageFloats / 2;
 
@@ -122,6 +131,14 @@ struct Params {
   uint32_t* counters;    // optional diagnostics
   int32_t probe_stage;   // test only: >= 0 makes that stage's wait run out on a barrier
   uint32_t probe_wait_us;  // that nothing completes, after this many microseconds
+  // Split rows (G == 1 only): rows >= split_first are each streamed by two
+  // independent CTAs, blocks split_first + 2*(row - split_first) + half.
+  // Each half leaves its exact top-k in the workspace; the later one merges.
+  int32_t split_first;   // >= B: no split rows
+  uint32_t* ws_ctr;      // per split row: halves arrived (zero on entry, reset to zero by the merger)
+  uint32_t* ws_cnt;      // per split row and half: entries handed over, or kHalfFailed
+  uint32_t* ws_key;      // per split row and half: k keys ...
+  uint32_t* ws_idx;      // ... and indices, in index order
 };
 
 // Cutoff description: an entry is selected if (key >> shift) > P, or if
@@ -270,18 +287,33 @@ __device__ uint32_t merged_find(Smem<C>& S, uint32_t target, uint32_t* above, ui
   }
 }
 
+// This thread's kRoundPerThread consecutive stash words from `base` (zeros
+// when base >= n). The stash capacity is a multiple of kRoundPerThread, so
+// the vector reads never pass its end.
+__device__ __forceinline__ void load_round(const uint32_t* a, int base, int n,
+                                           uint32_t (&v)[kRoundPerThread]) {
+#pragma unroll
+  for (int q = 0; q < kRoundPerThread / 4; ++q) {
+    uint4 x = make_uint4(0, 0, 0, 0);
+    if (base < n) x = *reinterpret_cast<const uint4*>(&a[base + 4 * q]);
+    v[4 * q + 0] = x.x;
+    v[4 * q + 1] = x.y;
+    v[4 * q + 2] = x.z;
+    v[4 * q + 3] = x.w;
+  }
+}
+
 // Histogram of stash keys: entries e < n with (key >> fshift) == fval (all
 // entries when !filter) add one to bin (key >> dshift) & dmask.
 template <int C>
 __device__ void stash_hist(Smem<C>& S, int n, bool filter, uint32_t fshift, uint32_t fval,
                            uint32_t dshift, uint32_t dmask) {
   for (int base0 = 0; base0 < n; base0 += kRoundEntries) {
-    const int base = base0 + 4 * threadIdx.x;
-    uint4 k4 = make_uint4(0, 0, 0, 0);
-    if (base < n) k4 = *reinterpret_cast<const uint4*>(&S.skey[base]);
-    const uint32_t kv[4] = {k4.x, k4.y, k4.z, k4.w};
+    const int base = base0 + kRoundPerThread * threadIdx.x;
+    uint32_t kv[kRoundPerThread];
+    load_round(S.skey, base, n, kv);
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < kRoundPerThread; ++c) {
       const uint32_t key = kv[c];
       const bool ok = (base + c < n) && (!filter || (key >> fshift) == fval);
       hist_add(S.hist, ok ? ((key >> dshift) & dmask) : 0xffffffffu);
@@ -323,17 +355,13 @@ __device__ void emit_rounds(Smem<C>& S, int n, Cut cut, uint32_t gt0, uint32_t e
   uint32_t run_gt = gt0, run_eq = eq0;
   int par = 0;
   for (int base0 = 0; base0 < n; base0 += kRoundEntries, par ^= 1) {
-    const int base = base0 + 4 * threadIdx.x;
-    uint4 k4 = make_uint4(0, 0, 0, 0), i4 = make_uint4(0, 0, 0, 0);
-    if (base < n) {
-      k4 = *reinterpret_cast<const uint4*>(&S.skey[base]);
-      i4 = *reinterpret_cast<const uint4*>(&S.sidx[base]);
-    }
-    const uint32_t kv[4] = {k4.x, k4.y, k4.z, k4.w};
-    const uint32_t iv[4] = {i4.x, i4.y, i4.z, i4.w};
+    const int base = base0 + kRoundPerThread * threadIdx.x;
+    uint32_t kv[kRoundPerThread], iv[kRoundPerThread];
+    load_round(S.skey, base, n, kv);
+    load_round(S.sidx, base, n, iv);
     uint32_t gtm = 0, eqm = 0, pgt = 0, peq = 0, wgt = 0, weq = 0;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < kRoundPerThread; ++c) {
       const bool valid = base + c < n;
       const uint32_t hi = kv[c] >> cut.shift;
       const bool gt = valid && hi > cut.P;
@@ -356,7 +384,7 @@ __device__ void emit_rounds(Smem<C>& S, int n, Cut cut, uint32_t gt0, uint32_t e
     uint32_t gb = run_gt + (before >> 16) + pgt;
     uint32_t eb = run_eq + (before & 0xffffu) + peq;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < kRoundPerThread; ++c) {
       const bool gt = (gtm >> c) & 1u, eq = (eqm >> c) & 1u;
       if (gt || (eq && eb < cut.r)) sink(gb + min(eb, cut.r), kv[c], iv[c]);
       gb += gt;
@@ -376,14 +404,29 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
   Smem<C>& S = *reinterpret_cast<Smem<C>*>(smem_raw);
 
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
-  const int row = static_cast<int>(blockIdx.x) / G;
-  const int rank = (G > 1) ? static_cast<int>(cluster_ctarank()) : 0;
+  // The row, and which of its `parts` contiguous slices this CTA streams:
+  // the cluster rank for G > 1, the half of a split row, or the whole row.
+  int row, part = 0, parts = 1;
+  if constexpr (G > 1) {
+    row = static_cast<int>(blockIdx.x) / G;
+    part = static_cast<int>(cluster_ctarank());
+    parts = G;
+  } else if (static_cast<int>(blockIdx.x) < p.split_first) {
+    row = static_cast<int>(blockIdx.x);
+  } else {
+    const int q = static_cast<int>(blockIdx.x) - p.split_first;
+    row = p.split_first + (q >> 1);
+    part = q & 1;
+    parts = 2;
+  }
+  const int rank = (G > 1) ? part : 0;  // rank in the cluster
+  const bool split = (G == 1) && parts == 2;
 
   const int64_t len_raw = p.lengths[row];
   const int n = static_cast<int>(len_raw < 0 ? 0 : (len_raw > p.stride ? p.stride : len_raw));
   int32_t* out_row = p.out + static_cast<int64_t>(row) * p.k;
   const int32_t* pt_row = PAGED ? p.page_table + static_cast<int64_t>(row) * p.pt_stride : nullptr;
-  const bool leader = (t == 0 && rank == 0);
+  const bool leader = (t == 0 && part == 0);
 
   auto map_index = [&](uint32_t i) -> int32_t {
     if constexpr (!PAGED) return static_cast<int32_t>(i);
@@ -399,6 +442,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
 
   // ---- rows with no more than k scores: every index is selected -----------
   if (n <= p.k) {
+    if (split && part == 1) return;  // the first half writes the row
     for (int j = rank * kThreads + t; j < p.k; j += kThreads * G)
       out_row[j] = (j < n) ? map_index(static_cast<uint32_t>(j)) : -1;
     if (p.counters != nullptr && leader) atomicAdd(&p.counters[kCntTrivial], 1u);
@@ -415,21 +459,29 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
   const int tail = n - h - nb;
   const float* body = rp + h;
   const int nstages = (nb + kStageFloats - 1) / kStageFloats;
-  const int s0 = static_cast<int>(static_cast<int64_t>(nstages) * rank / G);
-  const int s1 = static_cast<int>(static_cast<int64_t>(nstages) * (rank + 1) / G);
+  const int s0 = static_cast<int>(static_cast<int64_t>(nstages) * part / parts);
+  const int s1 = static_cast<int>(static_cast<int64_t>(nstages) * (part + 1) / parts);
+  // This part's scores: its stages of the body, plus the head / the tail.
+  const int b0 = s0 * kStageFloats, b1 = min(s1 * kStageFloats, nb);
+  const int n_part = (part == 0 ? h : 0) + (b1 - b0) + (part == parts - 1 ? tail : 0);
+  // The sampled region: the whole body for one CTA or a cluster (whose CTAs
+  // share one cutoff), this half's stages for a split row.
+  const float* sbody = split ? body + b0 : body;
+  const int snb = split ? b1 - b0 : nb;
+  const int sn = split ? n_part : n;
 
-  // ---- sampled cutoff: decision and sample loads (issued before the ring
-  // setup so their latency overlaps it) ---------------------------------------
+  // ---- sampled cutoff: decision and sample loads (issued first, and only
+  // consumed after the ring setup, so that their latency overlaps it) ---------
   uint32_t thr = 0;
   bool sampled = false;
   uint32_t target = 0;
-  uint32_t sk[16];
+  float4 sx[4];
   uint32_t smask = 0;
   {
-    const bool long_enough = nb >= 2 * 4 * kSampleVec4;
-    const bool want = long_enough && (p.sample_mode == 2 || (p.sample_mode == 0 && n >= p.sample_min_n));
+    const bool long_enough = snb >= 2 * 4 * kSampleVec4;
+    const bool want = long_enough && (p.sample_mode == 2 || (p.sample_mode == 0 && sn >= p.sample_min_n));
     if (want) {
-      const float mu = static_cast<float>(kk) * (4.0f * kSampleVec4) / static_cast<float>(n);
+      const float mu = static_cast<float>(kk) * (4.0f * kSampleVec4) / static_cast<float>(sn);
       float rf = ceilf(mu + p.sample_z * sqrtf(mu)) + 1.0f;
       rf = fmaxf(rf, 1.0f);
       if (rf < 4.0f * kSampleVec4) {
@@ -438,9 +490,9 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
       }
     }
 #pragma unroll
-    for (int v = 0; v < 4; ++v) sk[4 * v + 0] = sk[4 * v + 1] = sk[4 * v + 2] = sk[4 * v + 3] = 0;
+    for (int v = 0; v < 4; ++v) sx[v] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     if (sampled) {
-      const int nb4 = nb >> 2;
+      const int nb4 = snb >> 2;
       constexpr int per_rank = kSampleVec4 / G;
 #pragma unroll
       for (int v = 0; v < 4; ++v) {
@@ -450,29 +502,12 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
           const int chunk = gf / kSampleChunkVec4, within = gf % kSampleChunkVec4;
           const int64_t off4 =
               static_cast<int64_t>(chunk) * (nb4 - kSampleChunkVec4) / (kSampleChunks - 1) + within;
-          const float4 x = __ldg(reinterpret_cast<const float4*>(body) + off4);
-          sk[4 * v + 0] = order_key(x.x);
-          sk[4 * v + 1] = order_key(x.y);
-          sk[4 * v + 2] = order_key(x.z);
-          sk[4 * v + 3] = order_key(x.w);
+          sx[v] = __ldg(reinterpret_cast<const float4*>(sbody) + off4);
           smask |= 0xfu << (4 * v);
         }
       }
     }
   }
-
-  if (t == 0) {
-#pragma unroll
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&S.full[s], 1);
-      S.rel[s] = 0;
-    }
-    mbar_init(&S.never, 1);
-    S.issued = 0;
-    fence_mbar_init();
-  }
-  for (int i = t; i < kBins; i += kThreads) S.hist[i] = 0;
-  __syncthreads();
 
   // Ring bookkeeping. Stage j of a pass goes to slot (pass start + j - s0) %
   // kStages; `consumed` (stages taken from the ring so far) is uniform.
@@ -516,11 +551,31 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
       }
     }
   };
-  prime();  // the first stages are in flight while the sample is examined
+  if (t == 0) {
+#pragma unroll
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&S.full[s], 1);
+      S.rel[s] = 0;
+    }
+    mbar_init(&S.never, 1);
+    S.issued = 0;
+    fence_mbar_init();
+  }
+  prime();  // the first stages are in flight during the setup and the sample passes
+  for (int i = t; i < kBins; i += kThreads) S.hist[i] = 0;
+  __syncthreads();
 
   // ---- sampled cutoff: two 11-bit radix passes over the sample ---------------
   if (sampled) {
     uint32_t above, inbin;
+    uint32_t sk[16];
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      sk[4 * v + 0] = order_key(sx[v].x);
+      sk[4 * v + 1] = order_key(sx[v].y);
+      sk[4 * v + 2] = order_key(sx[v].z);
+      sk[4 * v + 3] = order_key(sx[v].w);
+    }
 #pragma unroll
     for (int i = 0; i < 16; ++i) hist_add(S.hist, ((smask >> i) & 1u) ? (sk[i] >> 21) : 0xffffffffu);
     const uint32_t b1 = merged_find<G, 8>(S, target, &above, &inbin);
@@ -750,7 +805,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
 
   auto stream_pass = [&]() {
     const int rot = (t >> 1) & 3;  // rotates the float4 order: conflict-free shared loads
-    if (rank == 0 && h > 0) scalar_group(0, h);
+    if (part == 0 && h > 0) scalar_group(0, h);
     for (int j = s0; j < s1; j += 2) {
       const bool two = j + 1 < s1;
       bool err = false;
@@ -761,12 +816,14 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
       process_group(tsA, tsB, 0.0f, rot, validA, validB, idxA, idxA + kStageFloats, err);
       release_slots(j, slotA, two);
     }
-    if (rank == G - 1 && tail > 0) scalar_group(h + nb, tail);
+    if (part == parts - 1 && tail > 0) scalar_group(h + nb, tail);
   };
 
   stream_pass();
 
   // ---- underflow: the sampled cutoff kept fewer than k candidates -----------
+  // (fewer than min(k, its scores) for the half of a split row)
+  const uint32_t need = split ? min(kk, static_cast<uint32_t>(n_part)) : kk;
   if (sampled) {
     uint32_t total = n_st;
     if constexpr (G > 1) {
@@ -776,8 +833,8 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
       for (int r = 0; r < G; ++r) total += ld_dsmem_u32(map_rank(smem_addr(&S.pub[0]), r));
       cluster_sync();
     }
-    if (total < kk) {  // uniform over the cluster
-      if (p.counters != nullptr && leader) atomicAdd(&p.counters[kCntRescan], 1u);
+    if (total < need) {  // uniform over the cluster
+      if (p.counters != nullptr && t == 0 && rank == 0) atomicAdd(&p.counters[kCntRescan], 1u);
       thr = 0;
       bound = prefilter_bound(thr);
       n_st = 0;
@@ -786,6 +843,85 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
       prime();
       stream_pass();
     }
+  }
+
+  // A wait timed out: let copies still in flight land (bounded) before the
+  // CTA leaves, so that no bulk copy writes into shared memory it no longer owns.
+  auto drain = [&]() {
+    if (abort && t == 0) {
+      for (uint32_t u = t0_seen; u < S.issued; ++u)
+        (void)mbar_wait_bounded(&S.full[u % kStages], (u / kStages) & 1u, kWaitLimitNs);
+      if (p.counters != nullptr) atomicAdd(&p.counters[kCntDeviceErrors], 1u);
+    }
+  };
+  auto poison_row = [&]() {  // marks the row as failed: no result can be mistaken for one
+    for (int j = t; j < p.k; j += kThreads) out_row[j] = static_cast<int32_t>(0x80000000u);
+  };
+
+  if (split) {
+    // ---- split row: this half's exact top-k goes to the workspace; the half
+    // that finishes second merges both (no CTA ever waits for another) -------
+    const int slot = row - p.split_first;
+    const size_t off = static_cast<size_t>(2 * slot + part) * kk;
+    uint32_t handed = 0;
+    if (!abort) {
+      if (n_st > need) {
+        const Cut c = select_stash<1>(S, static_cast<int>(n_st), need);
+        emit_rounds(S, static_cast<int>(n_st), c, 0u, 0u, [&](uint32_t pos, uint32_t key, uint32_t idx) {
+          if (pos < need) {
+            p.ws_key[off + pos] = key;
+            p.ws_idx[off + pos] = idx;
+          }
+        });
+        handed = need;
+      } else {
+        for (int e = t; e < static_cast<int>(n_st); e += kThreads) {
+          p.ws_key[off + e] = S.skey[e];
+          p.ws_idx[off + e] = S.sidx[e];
+        }
+        handed = n_st;
+      }
+    }
+    drain();
+    if (p.counters != nullptr && t == 0) {
+      if (compactions) atomicAdd(&p.counters[kCntCompactions], compactions);
+      if (part == 0 && sampled) atomicAdd(&p.counters[kCntSampled], 1u);
+    }
+    if (t == 0) p.ws_cnt[2 * slot + part] = abort ? kHalfFailed : handed;
+    __threadfence();  // the hand-over is visible before the arrival is counted
+    __syncthreads();
+    if (t == 0) S.res[3] = atomicAdd(&p.ws_ctr[slot], 1u);
+    __syncthreads();
+    if (S.res[3] == 0u) return;  // first to finish: the other half merges
+    __threadfence();
+    if (t == 0) p.ws_ctr[slot] = 0u;  // both halves have arrived: ready for the next call
+    const uint32_t c0 = __ldcg(&p.ws_cnt[2 * slot]), c1 = __ldcg(&p.ws_cnt[2 * slot + 1]);
+    if (c0 == kHalfFailed || c1 == kHalfFailed) {
+      poison_row();
+      return;
+    }
+    if (PAGED) {  // as below, for the whole row
+      const int p1 = (n + p.page_size - 1) / p.page_size;
+      for (int q = 32 * t; q < p1; q += 32 * kThreads) prefetch_l2(pt_row + q);
+      if (t == 0) prefetch_l2(pt_row + p1 - 1);
+    }
+    for (int i = t; i < kBins; i += kThreads) S.hist[i] = 0;
+    __syncthreads();  // the local emission has read the stash; the histogram is clear
+    // Half 0's entries precede half 1's: the merged stash is in index order.
+    const size_t base0 = static_cast<size_t>(2 * slot) * kk;
+    for (int e = t; e < static_cast<int>(c0 + c1); e += kThreads) {
+      const size_t src = static_cast<uint32_t>(e) < c0 ? base0 + e : base0 + kk + (e - c0);
+      const uint32_t key = __ldcg(&p.ws_key[src]);
+      S.skey[e] = key;
+      S.sidx[e] = __ldcg(&p.ws_idx[src]);
+      atomicAdd(&S.hist[key >> 21], 1u);
+    }
+    const Cut c = select_stash<1>(S, static_cast<int>(c0 + c1), kk);
+    emit_rounds(S, static_cast<int>(c0 + c1), c, 0u, 0u, [&](uint32_t pos, uint32_t, uint32_t idx) {
+      if (pos < kk) out_row[pos] = map_index(idx);
+    });
+    if (p.counters != nullptr && t == 0) atomicAdd(&p.counters[kCntSplitRows], 1u);
+    return;
   }
 
   // ---- exact cutoff over the stash(es) and emission --------------------------
@@ -840,14 +976,8 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
     if (rank == 0 && sampled) atomicAdd(&p.counters[kCntSampled], 1u);
   }
   if (abort) {
-    // A wait timed out: let copies still in flight land (bounded), then mark
-    // the whole row as failed so the caller cannot mistake it for a result.
-    if (t == 0) {
-      for (uint32_t u = t0_seen; u < S.issued; ++u)
-        (void)mbar_wait_bounded(&S.full[u % kStages], (u / kStages) & 1u, kWaitLimitNs);
-      if (p.counters != nullptr) atomicAdd(&p.counters[kCntDeviceErrors], 1u);
-    }
-    for (int j = t; j < p.k; j += kThreads) out_row[j] = static_cast<int32_t>(0x80000000u);
+    drain();
+    poison_row();
   }
 }
 

@@ -33,7 +33,10 @@ topk_status launch_variant(const Params& p, int dev, cudaStream_t stream) {
     flags.fetch_or(bit, std::memory_order_acq_rel);
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(p.B) * G, 1, 1);
+  // G CTAs per row, or one per row plus one more per split row.
+  const unsigned grid = G > 1 ? static_cast<unsigned>(p.B) * G
+                              : static_cast<unsigned>(p.B) + static_cast<unsigned>(p.B - p.split_first);
+  cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;

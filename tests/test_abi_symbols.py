@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.topk_abi_version() == 1
+    assert lib.topk_abi_version() == 2
     for code in range(5):
         assert lib.topk_status_string(code)
     assert b"unknown" in lib.topk_status_string(99)
@@ -58,6 +58,33 @@ def test_argument_checks_need_no_gpu(lib):
     assert lib.topk_paged(some, 64, some, 2, 512, P(None), 4, 16, some, None) == tk.Status.EINVAL
     assert lib.topk_paged(some, 64, some, 2, 512, some, 4, 0, some, None) == tk.Status.EINVAL
     assert lib.topk_paged(some, 64, some, 2, 512, some, 3, 16, some, None) == tk.Status.EINVAL
+
+
+def test_workspace_checks_need_no_gpu(lib):
+    some = ctypes.c_void_p(0x1000)
+    ws, big = ctypes.c_void_p(0x100000), 1 << 24
+    # misaligned or too small to hold the counters
+    assert lib.topk_ragged_ws(some, 64, some, 2, 512, some, ctypes.c_void_p(0x100008), big,
+                              None) == tk.Status.EINVAL
+    assert lib.topk_ragged_ws(some, 64, some, 2, 512, some, ws, 12287, None) == tk.Status.EINVAL
+    assert lib.topk_paged_ws(some, 64, some, 2, 512, some, 3, 16, some, ws, big,
+                             None) == tk.Status.EINVAL
+    assert lib.topk_ragged_ws(some, 64, some, 0, 512, some, ws, big, None) == tk.Status.OK
+    assert lib.topk_ragged_ws(some, 64, some, 2, 4096, some, ws, big, None) == \
+        tk.Status.EUNSUPPORTED_K
+
+
+def test_workspace_bytes(lib):
+    out = ctypes.c_size_t(0)
+    # 12 KiB of counters, then per split row and half k keys and k indices
+    assert lib.topk_workspace_bytes(512, 10, ctypes.byref(out)) == tk.Status.OK
+    assert out.value == 12288 + 10 * 2 * 512 * 8
+    assert lib.topk_workspace_bytes(2048, 1024, ctypes.byref(out)) == tk.Status.OK
+    assert out.value == 12288 + 1024 * 2 * 2048 * 8
+    assert lib.topk_workspace_bytes(0, 10, ctypes.byref(out)) == tk.Status.EUNSUPPORTED_K
+    assert lib.topk_workspace_bytes(512, -1, ctypes.byref(out)) == tk.Status.EINVAL
+    assert lib.topk_workspace_bytes(512, 1025, ctypes.byref(out)) == tk.Status.EINVAL
+    assert lib.topk_workspace_bytes(512, 10, None) == tk.Status.EINVAL
 
 
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):

@@ -46,7 +46,9 @@ def test_full_size_workload(config):
     ragged = tk.topk_ragged(s, l, w.k).cpu().numpy()
     _properties_all_rows(w.scores, w.lengths, w.k, ragged)
 
-    rows = np.random.default_rng(config).choice(w.B, SAMPLED_ROWS, replace=False)
+    # the last rows of the batch are the ones split over two CTAs
+    rows = np.concatenate([np.random.default_rng(config).choice(w.B - 8, SAMPLED_ROWS, replace=False),
+                           np.arange(w.B - 8, w.B)])
     want = run_oracle(w.scores[rows], w.lengths[rows], w.k)
     assert_parity(w.scores[rows], w.lengths[rows], w.k, ragged[rows], want, rows=rows)
 
@@ -57,6 +59,8 @@ def test_full_size_workload(config):
         want_p = run_oracle(w.scores[rows], w.lengths[rows], w.k, w.page_table[rows], w.page_size)
         assert_parity(w.scores[rows], w.lengths[rows], w.k, paged[rows], want_p, rows=rows,
                       page_table=w.page_table)
-    # the same answer on a second call
+    # the same answer on a second call, and without splitting any row
     again = tk.topk_ragged(s, l, w.k).cpu().numpy()
     assert np.array_equal(again, ragged)
+    unsplit = tk.topk_ragged(s, l, w.k, split=False).cpu().numpy()
+    assert np.array_equal(unsplit, ragged)

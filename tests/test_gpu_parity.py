@@ -110,6 +110,101 @@ def test_sampled_rows_are_counted():
     assert int(cnt[tk.Counter.DEVICE_ERRORS]) == 0
 
 
+# ------------------------------------------------------------ split rows
+
+
+def _workspace(k, rows):
+    return torch.zeros(tk.workspace_bytes(k, rows), dtype=torch.uint8, device="cuda:0")
+
+
+def _nontrivial(lengths, stride, k):
+    n = np.clip(lengths.astype(np.int64), 0, stride)
+    return int(np.sum(n > k))
+
+
+@pytest.mark.parametrize("k", [512, 1024, 2048])
+@pytest.mark.parametrize("sample_mode", [0, 1, 2])
+def test_split_rows_forced(k, sample_mode):
+    """Every row streamed by two independent CTAs that meet in the workspace:
+    rows of every kind, lengths at the head/tail and stage boundaries, halves
+    with no stage at all."""
+    scores, lengths = _mixed_rows()
+    B = scores.shape[0]
+    ws = _workspace(k, B)
+    cnt = counters_tensor()
+    check_against_oracle(scores, lengths, k, sample_mode=sample_mode, split_rows=B,
+                         workspace=ws, counters=cnt)
+    assert int(cnt[tk.Counter.SPLIT_ROWS]) == _nontrivial(lengths, scores.shape[1], k)
+    assert not torch.any(ws[:4096]), "arrival counters must be left at zero"
+
+
+@pytest.mark.parametrize("k", [512, 2048])
+def test_split_rows_compaction_and_rescan(k):
+    """Halves that compact their own candidate buffer (smallest capacity), and
+    halves whose sampled cutoff keeps too few (forced rescan)."""
+    scores, lengths = _mixed_rows()
+    B = scores.shape[0]
+    ws = _workspace(k, B)
+    cnt = counters_tensor()
+    check_against_oracle(scores, lengths, k, sample_mode=1, stash_capacity=k + 2048,
+                         split_rows=B, workspace=ws, counters=cnt)
+    assert int(cnt[tk.Counter.COMPACTIONS]) > 0
+    w = make_workload(3, B=6)
+    cnt = counters_tensor()
+    check_against_oracle(w.scores, w.lengths, w.k, sample_mode=2, sample_z=-1e4, split_rows=6,
+                         workspace=_workspace(w.k, 6), counters=cnt)
+    assert int(cnt[tk.Counter.RESCAN]) == 12  # both halves of every row
+
+
+def test_split_rows_partial_and_paged():
+    """Only the last m rows split (m < B); paged output through the merge."""
+    w = make_workload(4, B=20)
+    ws = _workspace(w.k, 20)
+    for m in (1, 7, 20):
+        cnt = counters_tensor()
+        check_against_oracle(w.scores, w.lengths, w.k, w.page_table, w.page_size, split_rows=m,
+                             workspace=ws, counters=cnt)
+        assert int(cnt[tk.Counter.SPLIT_ROWS]) == m
+    assert not torch.any(ws[:4096])
+
+
+def test_split_rows_workspace_reused_and_too_small():
+    """Calls in a row on one workspace (the counters return to zero after
+    each); a workspace that holds fewer rows than forced is refused, and
+    automatic splitting splits only what fits."""
+    w = make_workload(5, B=30)
+    ws = _workspace(w.k, 30)
+    first = run_gpu(w.scores, w.lengths, w.k, split_rows=30, workspace=ws)
+    for _ in range(3):
+        assert np.array_equal(run_gpu(w.scores, w.lengths, w.k, split_rows=30, workspace=ws), first)
+    assert_parity(w.scores, w.lengths, w.k, first, run_oracle(w.scores, w.lengths, w.k))
+    small = _workspace(w.k, 4)
+    with pytest.raises(tk.TopkError) as e:
+        run_gpu(w.scores, w.lengths, w.k, split_rows=5, workspace=small)
+    assert e.value.status == tk.Status.EINVAL
+    # rows wide enough to be split automatically: only as many as the workspace holds
+    w4 = make_workload(4, B=30)
+    cnt = counters_tensor()
+    got = run_gpu(w4.scores, w4.lengths, w4.k, cluster_size=1, workspace=_workspace(w4.k, 4),
+                  counters=cnt)
+    assert int(cnt[tk.Counter.SPLIT_ROWS]) == 4
+    assert_parity(w4.scores, w4.lengths, w4.k, got, run_oracle(w4.scores, w4.lengths, w4.k))
+
+
+def test_split_rows_wait_limit():
+    """A half whose wait runs out hands over a failure; the merging half marks
+    the row failed, and the workspace is left ready for the next call."""
+    w = make_workload(3, B=4)
+    ws = _workspace(w.k, 4)
+    cnt = counters_tensor()
+    out = run_gpu(w.scores, w.lengths, w.k, split_rows=4, workspace=ws, counters=cnt,
+                  probe_stage=2, probe_wait_us=2000)
+    assert np.all(out == tk.DEVICE_ERROR_INDEX)
+    assert int(cnt[tk.Counter.DEVICE_ERRORS]) == 8
+    assert not torch.any(ws[:4096])
+    check_against_oracle(w.scores, w.lengths, w.k, split_rows=4, workspace=ws)
+
+
 # ------------------------------------------------------------ edge cases
 
 
@@ -263,11 +358,12 @@ def test_wait_limit_reports_device_error(cluster):
     check_against_oracle(w.scores, w.lengths, w.k, cluster_size=cluster)
 
 
-@pytest.mark.parametrize("paged", [False, True])
-def test_cuda_graph_replay_with_mutated_lengths(paged):
+@pytest.mark.parametrize("paged,split", [(False, False), (True, False), (False, True)])
+def test_cuda_graph_replay_with_mutated_lengths(paged, split):
     """One captured call replayed with the row lengths (and once the scores)
     rewritten in place between replays, as a decode step would: every replay
-    matches the oracle on the inputs current at that replay."""
+    matches the oracle on the inputs current at that replay. The split case
+    streams every row with two CTAs that meet in a workspace."""
     rng = np.random.default_rng(21)
     B, stride, k, ps = 6, 98307 + 3, 1024, 64
     scores = rng.standard_normal((B, stride)).astype(np.float32)
@@ -275,16 +371,24 @@ def test_cuda_graph_replay_with_mutated_lengths(paged):
     s, l = to_dev(scores), to_dev(np.full(B, stride, np.int32))
     dpt = to_dev(pt) if paged else None
     out = torch.empty((B, k), dtype=torch.int32, device="cuda:0")
-    stream = torch.cuda.Stream()
-    with torch.cuda.stream(stream):  # warm the library (attributes, device query) first
-        tk.topk_ragged(s, l, k, out=out) if not paged else tk.topk_paged(s, l, k, dpt, ps, out=out)
-    stream.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        if paged:
+    ws = _workspace(k, B) if split else None
+    torch.cuda.synchronize()  # the workspace is zeroed on another stream
+
+    def call():
+        if split:
+            tk.topk_select_ex(s, l, k, out=out, split_rows=B, workspace=ws)
+        elif paged:
             tk.topk_paged(s, l, k, dpt, ps, out=out)
         else:
             tk.topk_ragged(s, l, k, out=out)
+
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):  # warm the library (attributes, device query) first
+        call()
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        call()
     boundary = [-1, 0, 1, k - 1, k, 32769, 65535, 98307, stride, stride + 17]
     for rep in range(4):
         lengths = np.array([boundary[(rep * B + i) % len(boundary)] for i in range(B)], np.int32)
