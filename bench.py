@@ -40,10 +40,15 @@ PAGE_LATENCY_US = {3: 207.06, 4: 301.72}
 WORKLOADS = {"w262144_k512_paged": 4, "w131072_k2048_ragged": 3}
 
 
+# The files that make up the kernel's device code and launch shape; DRAM
+# counters taken on other sources are not reported as this kernel's traffic.
+KERNEL_SOURCES = ("ptx.cuh", "topk_kernel.cuh", "topk_launch.cuh")
+
+
 def kernel_source_hash() -> str:
     csrc = os.path.join(ROOT, "sparse_attention_indexer_fp32_gb300", "csrc")
     h = hashlib.sha256()
-    for name in sorted(os.listdir(csrc)):
+    for name in KERNEL_SOURCES:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
