@@ -67,7 +67,8 @@ typedef enum topk_status {
   TOPK_EINVAL = 1,          /* null pointer, misalignment, negative B, bad stride/page size */
   TOPK_EUNSUPPORTED_K = 2,  /* k outside [1, TOPK_MAX_K] */
   TOPK_ECUDA = 3,           /* a CUDA runtime call failed */
-  TOPK_EDEVICE = 4          /* no usable sm_103 device is current */
+  TOPK_EDEVICE = 4,         /* no usable sm_103 device is current */
+  TOPK_ESCRATCH = 5         /* topk_select_noalloc: more scratch needed than its static array holds */
 } topk_status;
 
 /* Largest supported k. The decode-step indexer uses k = 512, 1024 or 2048. */
@@ -150,6 +151,34 @@ topk_status topk_paged_ws(const float* scores, int64_t stride, const int32_t* le
  * TOPK_ECUDA / TOPK_EDEVICE (device query).
  */
 topk_status topk_workspace_bytes(int32_t k, int32_t max_split_rows, size_t* bytes);
+
+/*
+ * topk_select_noalloc - the same operation as topk_ragged (page_table NULL)
+ * or topk_paged, for callers that cannot allocate device memory: for
+ * instance a serving engine that reserves nearly all of HBM for its KV cache
+ * at start-up and forbids allocation on the decode path (cudaMalloc can fail
+ * there, and it synchronises the device), or a plugin that runs inside a
+ * host framework without access to its allocator. The pages have no
+ * counterpart of this call.
+ *
+ * It allocates nothing and takes no workspace: the scratch for split rows
+ * (see topk_ragged_ws) is a fixed 4 MiB + 12 KiB array in the library's own
+ * device memory, which every GPU that loads the library holds until the
+ * process exits. That is room for 128 split rows at k = 2048, 512 at k = 512.
+ * A call that would split more rows than that returns TOPK_ESCRATCH before
+ * anything is enqueued.
+ *
+ * The first call on a device looks up the array's device address and clears
+ * its counters (a synchronous cudaMemset); make that first call before any
+ * stream capture. Every call shares the one array: calls that may run at the
+ * same time on the GPU (other streams, other host threads) race on it, so
+ * serialise them. The caller still passes inputs and outputs as for
+ * topk_ragged / topk_paged, with the same contract.
+ */
+topk_status topk_select_noalloc(const float* scores, int64_t stride, const int32_t* lengths,
+                                int32_t B, int32_t k, const int32_t* page_table,
+                                int64_t pt_stride, int32_t page_size, int32_t* out,
+                                topk_stream_t stream);
 
 /* Static, human-readable description of a status code. */
 const char* topk_status_string(topk_status status);

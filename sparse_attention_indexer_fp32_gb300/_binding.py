@@ -30,6 +30,7 @@ class Status(enum.IntEnum):
     EUNSUPPORTED_K = 2
     ECUDA = 3
     EDEVICE = 4
+    ESCRATCH = 5
 
 
 class Counter(enum.IntEnum):
@@ -92,6 +93,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.topk_paged_ws.restype = ctypes.c_int
         lib.topk_workspace_bytes.argtypes = [i32, i32, ctypes.POINTER(sz)]
         lib.topk_workspace_bytes.restype = ctypes.c_int
+        lib.topk_select_noalloc.argtypes = [vp, i64, vp, i32, i32, vp, i64, i32, vp, vp]
+        lib.topk_select_noalloc.restype = ctypes.c_int
         lib.topk_status_string.argtypes = [ctypes.c_int]
         lib.topk_status_string.restype = ctypes.c_char_p
         lib.topk_abi_version.restype = ctypes.c_int32

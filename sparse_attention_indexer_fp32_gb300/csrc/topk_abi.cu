@@ -208,6 +208,36 @@ topk_status select_impl(const float* scores, int64_t stride, const int32_t* leng
   }
 }
 
+// ---- allocation-free entry point ---------------------------------------------
+// Scratch of topk_select_noalloc: a fixed array in the library's own device
+// memory, which every GPU that loads the library keeps until the process
+// exits. 12 KiB of arrival counters and hand-over counts, then room for 128
+// split rows at k = 2048 (512 at k = 512): 4 MiB + 12 KiB.
+constexpr size_t kStaticWsBytes = kWsHeaderBytes + static_cast<size_t>(4) * 1024 * 1024;
+static __device__ __align__(256) unsigned char g_static_ws[kStaticWsBytes];
+
+struct StaticWs {
+  std::once_flag once;
+  cudaError_t err = cudaSuccess;
+  void* ptr = nullptr;
+};
+StaticWs g_static_ws_state[kMaxDevices];
+
+// Device address of g_static_ws on device `dev` (current). In host code the
+// array's name only stands in for it, so the address is looked up once per
+// device; the arrival counters are cleared then, and every call that
+// completes leaves them clear again.
+topk_status static_workspace(int dev, void** ptr) {
+  StaticWs& st = g_static_ws_state[dev];
+  std::call_once(st.once, [&]() {
+    st.err = cudaGetSymbolAddress(&st.ptr, g_static_ws);
+    if (st.err == cudaSuccess) st.err = cudaMemset(st.ptr, 0, kWsCounterBytes);
+  });
+  if (st.err != cudaSuccess) return TOPK_ECUDA;
+  *ptr = st.ptr;
+  return TOPK_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -267,6 +297,29 @@ topk_status topk_select_ex(const float* scores, int64_t stride, const int32_t* l
                      nullptr, 0, opts, reinterpret_cast<cudaStream_t>(stream));
 }
 
+topk_status topk_select_noalloc(const float* scores, int64_t stride, const int32_t* lengths,
+                                int32_t B, int32_t k, const int32_t* page_table,
+                                int64_t pt_stride, int32_t page_size, int32_t* out,
+                                topk_stream_t stream) {
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (B <= 0 || stride < 1 || k < 1 || k > TOPK_MAX_K)  // the plain checks decide these cases
+    return select_impl(scores, stride, lengths, B, k, page_table, pt_stride, page_size, out,
+                       nullptr, 0, nullptr, cs);
+  int dev = 0;
+  DeviceInfo* info = nullptr;
+  topk_status st = device_info(&dev, &info);
+  if (st != TOPK_OK) return st;
+  // The scratch this call would use, against the fixed array.
+  const int G = auto_cluster_size(B, stride, info->sm_count);
+  const int m = G == 1 ? auto_split_rows(B, stride, info->sm_count) : 0;
+  if (ws_bytes_for(k, m) > kStaticWsBytes) return TOPK_ESCRATCH;
+  void* ws = nullptr;
+  st = static_workspace(dev, &ws);
+  if (st != TOPK_OK) return st;
+  return select_impl(scores, stride, lengths, B, k, page_table, pt_stride, page_size, out, ws,
+                     kStaticWsBytes, nullptr, cs);
+}
+
 const char* topk_status_string(topk_status status) {
   switch (status) {
     case TOPK_OK: return "success";
@@ -274,6 +327,7 @@ const char* topk_status_string(topk_status status) {
     case TOPK_EUNSUPPORTED_K: return "k outside [1, TOPK_MAX_K]";
     case TOPK_ECUDA: return "a CUDA runtime call failed";
     case TOPK_EDEVICE: return "current device is not an sm_103 GPU";
+    case TOPK_ESCRATCH: return "the call needs more scratch than the static workspace of topk_select_noalloc holds";
     default: return "unknown status";
   }
 }
