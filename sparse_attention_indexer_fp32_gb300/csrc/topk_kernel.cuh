@@ -154,30 +154,13 @@ __device__ __forceinline__ uint32_t order_key(float x) {
   return u ^ (static_cast<uint32_t>(static_cast<int32_t>(u) >> 31) | 0x80000000u);
 }
 
-// Largest float b with  order_key(x) >= thr  =>  x >= b  (float compare).
-// Float comparison equates -0 and +0, so `x >= b` is a superset test that
-// lets the exact key comparison run only on the few scores that pass it.
-__device__ __forceinline__ float prefilter_bound(uint32_t thr) {
+// The float b whose key is thr: for every non-NaN score x,
+// order_key(x) >= thr  <=>  x >= b  (float compare), except when b is a zero,
+// where the float compare cannot tell -0 from +0 and the keys must decide.
+__device__ __forceinline__ float float_bound(uint32_t thr) {
   if (thr <= 0x007fffffu) return -__int_as_float(0x7f800000);  // every score passes: -inf
   const uint32_t u = (thr & 0x80000000u) ? (thr ^ 0x80000000u) : ~thr;
   return __uint_as_float(u);
-}
-
-// Three-input maximum (one instruction on sm_100 and later).
-__device__ __forceinline__ float max3f(float a, float b, float c) {
-  float r;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-  return r;
-}
-
-// Maximum of the 16 scores held in v.
-__device__ __forceinline__ float max16(const float4 (&v)[4]) {
-  const float a = max3f(v[0].x, v[0].y, v[0].z);
-  const float b = max3f(v[0].w, v[1].x, v[1].y);
-  const float c = max3f(v[1].z, v[1].w, v[2].x);
-  const float d = max3f(v[2].y, v[2].z, v[2].w);
-  const float e = max3f(v[3].x, v[3].y, v[3].z);
-  return max3f(max3f(a, b, c), max3f(d, e, v[3].w), -__int_as_float(0x7f800000));
 }
 
 // Inclusive prefix sum over lanes [0, LANES) of the warp (lanes past LANES
@@ -322,13 +305,17 @@ __device__ void stash_hist(Smem<C>& S, int n, bool filter, uint32_t fshift, uint
 }
 
 // Exact cutoff of the target-th largest key over the stash (merged over the
-// cluster when G > 1). 1 <= target <= total entries. The coarse (key >> 21)
-// histogram of the stash is kept up to date by the inserts, so the first
-// pass only reads it. The histogram is all zero on return.
+// cluster when G > 1). 1 <= target <= total entries. Three radix passes: the
+// coarse (key >> 21) histogram of the whole stash, then 11 and 10 bits under
+// the prefix found, with an early exit once the remaining rank fills a bin.
+// (Inserts do not keep the coarse histogram current: the hits of a stage
+// share a few coarse bins, and their shared atomics would serialise in the
+// streaming loop.) The histogram is all zero on entry and on return.
 template <int G, int C>
 __device__ Cut select_stash(Smem<C>& S, int n, uint32_t target) {
   uint32_t above, inbin;
   __syncthreads();  // the last stash writes of every thread are visible
+  stash_hist(S, n, false, 0, 0, 21, 0x7ff);
   const uint32_t b1 = merged_find<G, 8>(S, target, &above, &inbin);
   uint32_t rem = target - above;
   if (rem == inbin) return Cut{21, b1, rem};
@@ -597,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
   uint32_t n_st = 0;        // stash entries (uniform)
   uint32_t grp = 0;         // groups processed (uniform), selects the count table half
   uint32_t compactions = 0;
-  float bound = prefilter_bound(thr);
+  float bound = float_bound(thr);
 
   auto compact = [&]() {
     const Cut cut = select_stash<1>(S, static_cast<int>(n_st), kk);
@@ -605,13 +592,12 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
       if (pos < kk) {  // exactly kk entries are selected; the guard only bounds a corrupted cut
         S.skey[pos] = key;
         S.sidx[pos] = idx;
-        atomicAdd(&S.hist[key >> 21], 1u);  // coarse histogram of the kept entries
       }
     });
     __syncthreads();
     n_st = kk;
     thr = max(thr, (cut.P << cut.shift) + 1u);
-    bound = prefilter_bound(thr);
+    bound = float_bound(thr);
     ++compactions;
   };
 
@@ -646,6 +632,8 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
   // Hit mask of this thread's 16 scores of a ring stage (ts points at them;
   // scores past the stage's end are stale and masked off by `valid`). The
   // float4 reads are rotated by `rot` so that they are bank-conflict free.
+  // (No per-thread maximum is tested first: in a warp of 512 scores some
+  // lane nearly always passes, so such a prefilter only added work.)
   // A scalar group (ts == nullptr) has one score, sx, present when bit 0 of
   // `valid` is set.
   auto group_mask = [&](const float* ts, float sx, int rot, uint32_t valid) -> uint32_t {
@@ -653,7 +641,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
     float4 v[4];
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) v[jj] = *reinterpret_cast<const float4*>(ts + 4 * ((jj + rot) & 3));
-    return (max16(v) >= bound) ? hit_mask(v, rot, valid) : 0u;
+    return hit_mask(v, rot, valid);
   };
 
   // Base (lower warps) and total of the packed per-warp counts in table half `par`.
@@ -698,12 +686,10 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
       const uint32_t k0 = order_key(x0), k1 = order_key(x1);
       S.skey[pos] = k0;
       S.sidx[pos] = idx0 + e0;
-      atomicAdd(&S.hist[k0 >> 21], 1u);  // coarse histogram of the stash, kept current
       ++pos;
       if (two) {
         S.skey[pos] = k1;
         S.sidx[pos] = idx0 + e1;
-        atomicAdd(&S.hist[k1 >> 21], 1u);
         ++pos;
       }
     }
@@ -836,7 +822,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
     if (total < need) {  // uniform over the cluster
       if (p.counters != nullptr && t == 0 && rank == 0) atomicAdd(&p.counters[kCntRescan], 1u);
       thr = 0;
-      bound = prefilter_bound(thr);
+      bound = float_bound(thr);
       n_st = 0;
       for (int i = t; i < kBins; i += kThreads) S.hist[i] = 0;  // forget the first pass
       __syncthreads();
@@ -914,7 +900,6 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
       const uint32_t key = __ldcg(&p.ws_key[src]);
       S.skey[e] = key;
       S.sidx[e] = __ldcg(&p.ws_idx[src]);
-      atomicAdd(&S.hist[key >> 21], 1u);
     }
     const Cut c = select_stash<1>(S, static_cast<int>(c0 + c1), kk);
     emit_rounds(S, static_cast<int>(c0 + c1), c, 0u, 0u, [&](uint32_t pos, uint32_t, uint32_t idx) {
