@@ -147,6 +147,7 @@ struct Cut {
   uint32_t shift;
   uint32_t P;
   uint32_t r;
+  bool all_ties;  // r equals the number of entries with (key >> shift) == P
 };
 
 __device__ __forceinline__ uint32_t order_key(float x) {
@@ -318,16 +319,16 @@ __device__ Cut select_stash(Smem<C>& S, int n, uint32_t target) {
   stash_hist(S, n, false, 0, 0, 21, 0x7ff);
   const uint32_t b1 = merged_find<G, 8>(S, target, &above, &inbin);
   uint32_t rem = target - above;
-  if (rem == inbin) return Cut{21, b1, rem};
+  if (rem == inbin) return Cut{21, b1, rem, true};
   stash_hist(S, n, true, 21, b1, 10, 0x7ff);
   const uint32_t b2 = merged_find<G, 8>(S, rem, &above, &inbin);
   const uint32_t p2 = (b1 << 11) | b2;
   rem -= above;
-  if (rem == inbin) return Cut{10, p2, rem};
+  if (rem == inbin) return Cut{10, p2, rem, true};
   stash_hist(S, n, true, 10, p2, 0, 0x3ff);
   const uint32_t b3 = merged_find<G, 4>(S, rem, &above, &inbin);
   rem -= above;
-  return Cut{0, (p2 << 10) | b3, rem};
+  return Cut{0, (p2 << 10) | b3, rem, rem == inbin};
 }
 
 // Walks stash entries [0, n) in order and calls sink(pos, key, idx) for each
@@ -339,6 +340,38 @@ template <int C, class Sink>
 __device__ void emit_rounds(Smem<C>& S, int n, Cut cut, uint32_t gt0, uint32_t eq0, Sink sink) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const uint32_t lt_mask = (1u << lane) - 1u;
+  if (cut.all_ties) {
+    // Every entry at the cutoff is selected: selection is (key >> shift) >= P,
+    // and an entry's slot is the number of selected entries before it.
+    uint32_t run = gt0 + eq0;
+    int par = 0;
+    for (int base0 = 0; base0 < n; base0 += kRoundEntries, par ^= 1) {
+      const int base = base0 + kRoundPerThread * threadIdx.x;
+      uint32_t kv[kRoundPerThread], iv[kRoundPerThread];
+      load_round(S.skey, base, n, kv);
+      load_round(S.sidx, base, n, iv);
+      uint32_t selm = 0, psel = 0, wsel = 0;
+#pragma unroll
+      for (int c = 0; c < kRoundPerThread; ++c) {
+        const bool sel = base + c < n && (kv[c] >> cut.shift) >= cut.P;
+        selm |= static_cast<uint32_t>(sel) << c;
+        const uint32_t m = __ballot_sync(0xffffffffu, sel);
+        psel += __popc(m & lt_mask);
+        wsel += __popc(m);
+      }
+      if (lane == 0) S.rtab[par][w] = wsel;
+      __syncthreads();
+      const uint32_t e = lane < kWarps ? S.rtab[par][lane] : 0u;
+      const uint32_t incl = warp_incl_scan(e);
+      uint32_t pos = run + __shfl_sync(0xffffffffu, incl - e, w) + psel;
+#pragma unroll
+      for (int c = 0; c < kRoundPerThread; ++c) {
+        if ((selm >> c) & 1u) sink(pos++, kv[c], iv[c]);
+      }
+      run += __shfl_sync(0xffffffffu, incl, kWarps - 1);
+    }
+    return;
+  }
   uint32_t run_gt = gt0, run_eq = eq0;
   int par = 0;
   for (int base0 = 0; base0 < n; base0 += kRoundEntries, par ^= 1) {
@@ -446,8 +479,9 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
   const int tail = n - h - nb;
   const float* body = rp + h;
   const int nstages = (nb + kStageFloats - 1) / kStageFloats;
-  const int s0 = static_cast<int>(static_cast<int64_t>(nstages) * part / parts);
-  const int s1 = static_cast<int>(static_cast<int64_t>(nstages) * (part + 1) / parts);
+  const int lg_parts = __ffs(parts) - 1;  // parts is 1, 2, 4 or 8
+  const int s0 = (nstages * part) >> lg_parts;
+  const int s1 = (nstages * (part + 1)) >> lg_parts;
   // This part's scores: its stages of the body, plus the head / the tail.
   const int b0 = s0 * kStageFloats, b1 = min(s1 * kStageFloats, nb);
   const int n_part = (part == 0 ? h : 0) + (b1 - b0) + (part == parts - 1 ? tail : 0);
@@ -468,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
     const bool long_enough = snb >= 2 * 4 * kSampleVec4;
     const bool want = long_enough && (p.sample_mode == 2 || (p.sample_mode == 0 && sn >= p.sample_min_n));
     if (want) {
-      const float mu = static_cast<float>(kk) * (4.0f * kSampleVec4) / static_cast<float>(sn);
+      const float mu = static_cast<float>(kk) * (4.0f * kSampleVec4) * __frcp_rn(static_cast<float>(sn));
       float rf = ceilf(mu + p.sample_z * sqrtf(mu)) + 1.0f;
       rf = fmaxf(rf, 1.0f);
       if (rf < 4.0f * kSampleVec4) {
@@ -480,6 +514,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
     for (int v = 0; v < 4; ++v) sx[v] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     if (sampled) {
       const int nb4 = snb >> 2;
+      const int step4 = (nb4 - kSampleChunkVec4) / (kSampleChunks - 1);  // float4s between chunk starts
       constexpr int per_rank = kSampleVec4 / G;
 #pragma unroll
       for (int v = 0; v < 4; ++v) {
@@ -487,8 +522,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
         if (f < per_rank) {
           const int gf = rank * per_rank + f;
           const int chunk = gf / kSampleChunkVec4, within = gf % kSampleChunkVec4;
-          const int64_t off4 =
-              static_cast<int64_t>(chunk) * (nb4 - kSampleChunkVec4) / (kSampleChunks - 1) + within;
+          const int off4 = chunk * step4 + within;
           sx[v] = __ldg(reinterpret_cast<const float4*>(sbody) + off4);
           smask |= 0xfu << (4 * v);
         }
@@ -503,9 +537,10 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
   uint32_t consumed = 0, t0_seen = 0;
   bool abort = false;
 
-  auto issue_stage = [&](int j, uint32_t slot) {  // one thread
+  // One thread; the caller has made the slot's earlier shared-memory reads
+  // visible to the bulk copy (fence_proxy_async_smem).
+  auto issue_stage = [&](int j, uint32_t slot) {
     const int cnt = min(kStageFloats, nb - j * kStageFloats);
-    fence_proxy_async_smem();
     mbar_arrive_expect_tx(&S.full[slot], static_cast<uint32_t>(cnt) * 4u);
     bulk_load(&S.ring[slot][0], body + static_cast<int64_t>(j) * kStageFloats,
               static_cast<uint32_t>(cnt) * 4u, &S.full[slot]);
@@ -513,6 +548,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
   auto prime = [&]() {
     if (t == 0 && !abort) {
       const int m = min(s1 - s0, kStages);
+      fence_proxy_async_smem();
       for (int u = 0; u < m; ++u) issue_stage(s0 + u, (consumed + u) % kStages);
       S.issued += m;
     }
@@ -524,17 +560,15 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
     __syncwarp();
     if (lane == 0 && atom_add_acq_rel_cta(&S.rel[slot], 1u) == kWarps - 1) {
       S.rel[slot] = 0;
-      if (!abort) {
-        uint32_t m = 0;
-        if (j + kStages < s1) {
-          issue_stage(j + kStages, slot);
-          ++m;
-        }
+      if (!abort && j + kStages < s1) {
+        fence_proxy_async_smem();
+        issue_stage(j + kStages, slot);
+        uint32_t m = 1;
         if (two && j + 1 + kStages < s1) {
           issue_stage(j + 1 + kStages, (slot + 1) % kStages);
           ++m;
         }
-        if (m != 0) atomicAdd(&S.issued, m);
+        atomicAdd(&S.issued, m);
       }
     }
   };
@@ -606,27 +640,27 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
   // comparison is exact unless bound is a zero, where -0 < +0 must come from
   // the keys.
   auto hit_mask = [&](const float4 (&v)[4], int rot, uint32_t valid) -> uint32_t {
-    uint32_t pm = 0;
+    uint32_t pl = 0;  // in load order: v[j] at bits 4j .. 4j + 3
     if (bound != 0.0f) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const uint32_t b = static_cast<uint32_t>(v[j].x >= bound) |
-                           (static_cast<uint32_t>(v[j].y >= bound) << 1) |
-                           (static_cast<uint32_t>(v[j].z >= bound) << 2) |
-                           (static_cast<uint32_t>(v[j].w >= bound) << 3);
-        pm |= b << (4 * ((j + rot) & 3));
+        pl |= (static_cast<uint32_t>(v[j].x >= bound) | (static_cast<uint32_t>(v[j].y >= bound) << 1) |
+               (static_cast<uint32_t>(v[j].z >= bound) << 2) | (static_cast<uint32_t>(v[j].w >= bound) << 3))
+              << (4 * j);
       }
     } else {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const uint32_t b = static_cast<uint32_t>(order_key(v[j].x) >= thr) |
-                           (static_cast<uint32_t>(order_key(v[j].y) >= thr) << 1) |
-                           (static_cast<uint32_t>(order_key(v[j].z) >= thr) << 2) |
-                           (static_cast<uint32_t>(order_key(v[j].w) >= thr) << 3);
-        pm |= b << (4 * ((j + rot) & 3));
+        pl |= (static_cast<uint32_t>(order_key(v[j].x) >= thr) |
+               (static_cast<uint32_t>(order_key(v[j].y) >= thr) << 1) |
+               (static_cast<uint32_t>(order_key(v[j].z) >= thr) << 2) |
+               (static_cast<uint32_t>(order_key(v[j].w) >= thr) << 3))
+              << (4 * j);
       }
     }
-    return pm & valid;
+    // v[j] holds the scores 4 * ((j + rot) & 3) ..: rotate the 16 bits left by 4 * rot
+    const uint32_t pl2 = pl | (pl << 16);
+    return (pl2 >> (16 - 4 * rot)) & valid;
   };
 
   // Hit mask of this thread's 16 scores of a ring stage (ts points at them;
