@@ -107,7 +107,7 @@ struct __align__(128) Smem {
   uint64_t never;                   // an mbarrier nothing arrives on (the wait-limit test)
   uint32_t rel[kStages];            // warps done with each ring slot (the last one refills it)
   uint32_t issued;                  // stages issued into the ring (for the error drain)
-  alignas(16) uint32_t tab[2][kWarps];  // per-group per-warp hit counts; bit 31 = a wait timed out
+  uint32_t tab[2][kWarps];          // per-group per-warp packed hit counts and wait-error flags
   uint32_t rtab[2][kWarps];         // per-round per-warp (above << 16 | tied) counts
   uint32_t scan[kWarps];
   uint32_t res[4];
@@ -183,10 +183,8 @@ __device__ __forceinline__ uint32_t block_incl_scan(uint32_t v, Smem<C>& S) {
   v = warp_incl_scan(v);
   if (lane == 31) S.scan[w] = v;
   __syncthreads();
-  uint32_t add = 0;
-#pragma unroll
-  for (int i = 0; i < kWarps; ++i) add += (i < w) ? S.scan[i] : 0u;
-  return v + add;
+  const uint32_t e = lane < kWarps ? S.scan[lane] : 0u;  // warp totals
+  return v + __reduce_add_sync(0xffffffffu, lane < w ? e : 0u);
 }
 
 // Shared-memory histogram increment; `bin` = 0xffffffff means "no increment".
@@ -361,14 +359,13 @@ __device__ void emit_rounds(Smem<C>& S, int n, Cut cut, uint32_t gt0, uint32_t e
       }
       if (lane == 0) S.rtab[par][w] = wsel;
       __syncthreads();
-      const uint32_t e = lane < kWarps ? S.rtab[par][lane] : 0u;
-      const uint32_t incl = warp_incl_scan(e);
-      uint32_t pos = run + __shfl_sync(0xffffffffu, incl - e, w) + psel;
+      const uint32_t e = lane < kWarps ? S.rtab[par][lane] : 0u;  // per-warp counts
+      uint32_t pos = run + __reduce_add_sync(0xffffffffu, lane < w ? e : 0u) + psel;
 #pragma unroll
       for (int c = 0; c < kRoundPerThread; ++c) {
         if ((selm >> c) & 1u) sink(pos++, kv[c], iv[c]);
       }
-      run += __shfl_sync(0xffffffffu, incl, kWarps - 1);
+      run += __reduce_add_sync(0xffffffffu, e);
     }
     return;
   }
@@ -397,10 +394,9 @@ __device__ void emit_rounds(Smem<C>& S, int n, Cut cut, uint32_t gt0, uint32_t e
     }
     if (lane == 0) S.rtab[par][w] = (wgt << 16) | weq;
     __syncthreads();
-    const uint32_t e = lane < kWarps ? S.rtab[par][lane] : 0u;
-    const uint32_t incl = warp_incl_scan(e);
-    const uint32_t before = __shfl_sync(0xffffffffu, incl - e, w);
-    const uint32_t total = __shfl_sync(0xffffffffu, incl, kWarps - 1);
+    const uint32_t e = lane < kWarps ? S.rtab[par][lane] : 0u;  // per-warp packed counts
+    const uint32_t before = __reduce_add_sync(0xffffffffu, lane < w ? e : 0u);
+    const uint32_t total = __reduce_add_sync(0xffffffffu, e);
     uint32_t gb = run_gt + (before >> 16) + pgt;
     uint32_t eb = run_eq + (before & 0xffffu) + peq;
 #pragma unroll
@@ -479,6 +475,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
   const int tail = n - h - nb;
   const float* body = rp + h;
   const int nstages = (nb + kStageFloats - 1) / kStageFloats;
+  const int nfull = nb / kStageFloats;  // stages of a full kStageFloats scores
   const int lg_parts = __ffs(parts) - 1;  // parts is 1, 2, 4 or 8
   const int s0 = (nstages * part) >> lg_parts;
   const int s1 = (nstages * (part + 1)) >> lg_parts;
@@ -680,16 +677,9 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
 
   // Base (lower warps) and total of the packed per-warp counts in table half `par`.
   auto read_table = [&](int par, uint32_t& base, uint32_t& total) {
-    const uint4 a = *reinterpret_cast<const uint4*>(&S.tab[par][0]);
-    const uint4 b = *reinterpret_cast<const uint4*>(&S.tab[par][4]);
-    const uint32_t e[kWarps] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-    base = 0;
-    total = 0;
-#pragma unroll
-    for (int i = 0; i < kWarps; ++i) {
-      base += (i < w) ? e[i] : 0u;
-      total += e[i];
-    }
+    const uint32_t e = lane < kWarps ? S.tab[par][lane] : 0u;  // lane i: warp i's word
+    base = __reduce_add_sync(0xffffffffu, lane < w ? e : 0u);
+    total = __reduce_add_sync(0xffffffffu, e);
   };
 
   // Publishes this warp's packed count and error flag and synchronises the
@@ -817,9 +807,12 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
         err = true;
       }
     }
-    const int cnt = min(kStageFloats, nb - j * kStageFloats);
-    const int have = cnt - kPerThread * t;
-    valid = have >= kPerThread ? 0xffffu : (have <= 0 ? 0u : (1u << have) - 1u);
+    if (j < nfull) {
+      valid = 0xffffu;
+    } else {  // the last, partial stage
+      const int have = (nb - j * kStageFloats) - kPerThread * t;
+      valid = have >= kPerThread ? 0xffffu : (have <= 0 ? 0u : (1u << have) - 1u);
+    }
     return &S.ring[slot][kPerThread * t];
   };
 
