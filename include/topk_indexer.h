@@ -153,6 +153,21 @@ topk_status topk_paged_ws(const float* scores, int64_t stride, const int32_t* le
 topk_status topk_workspace_bytes(int32_t k, int32_t max_split_rows, size_t* bytes);
 
 /*
+ * topk_select_bf16 - the same operation over BF16 scores (raw 16-bit
+ * patterns, 2-byte aligned), for rows of at most 16384 scores: `stride` must
+ * be <= 16384 (TOPK_EINVAL otherwise). page_table NULL selects the ragged
+ * output, otherwise the paged one as in topk_paged. A BF16 value converts
+ * exactly to FP32, so the ranking (-0 below +0), the tie rule and the
+ * contract are those of topk_ragged / topk_paged on the converted scores.
+ * This is the small-row bf16 top-k of the sglang PR 39648 report (实现拆解 2,
+ * `topk_transform_bf16_small`: rows <= 16384, k <= 2048, fused page-table
+ * transform, NaN unsupported).
+ */
+topk_status topk_select_bf16(const uint16_t* scores, int64_t stride, const int32_t* lengths,
+                             int32_t B, int32_t k, const int32_t* page_table, int64_t pt_stride,
+                             int32_t page_size, int32_t* out, topk_stream_t stream);
+
+/*
  * topk_select_noalloc - the same operation as topk_ragged (page_table NULL)
  * or topk_paged, for callers that cannot allocate device memory: for
  * instance a serving engine that reserves nearly all of HBM for its KV cache
@@ -218,6 +233,11 @@ int32_t topk_abi_version(void);
  *                   CTA per row, so cluster_size must be 0 or 1)
  *   workspace,      as for topk_ragged_ws; NULL = none (no row is split, and
  *   workspace_bytes split_rows must be 0 or -1)
+ *   short_rows      0 automatic (rows of width <= 16384 take the short-row
+ *                   kernel unless cluster_size, stash_capacity, probe_stage or
+ *                   split_rows > 0 is given); -1 never; 1 always (width <= 16384
+ *                   and none of those options). In the short-row kernel
+ *                   sample_mode 1 selects its exact register path.
  */
 typedef enum topk_counter {
   TOPK_CNT_ROWS = 0,          /* rows handled */
@@ -228,7 +248,9 @@ typedef enum topk_counter {
   TOPK_CNT_DEVICE_ERRORS = 5, /* CTAs whose waits timed out */
   TOPK_CNT_CLUSTER_ROWS = 6,  /* rows split over a cluster of CTAs */
   TOPK_CNT_SPLIT_ROWS = 7,    /* rows streamed by two independent CTAs and merged */
-  TOPK_NUM_COUNTERS = 8
+  TOPK_CNT_SHORT_ROWS = 8,    /* rows taken by the short-row kernel */
+  TOPK_CNT_SHORT_EXACT = 9,   /* of them, rows that took its exact register path */
+  TOPK_NUM_COUNTERS = 16
 } topk_counter;
 
 typedef struct topk_debug_opts {
@@ -242,6 +264,7 @@ typedef struct topk_debug_opts {
   int32_t split_rows;
   void* workspace;
   size_t workspace_bytes;
+  int32_t short_rows;
 } topk_debug_opts;
 
 topk_status topk_select_ex(const float* scores, int64_t stride, const int32_t* lengths,

@@ -22,11 +22,13 @@ from ._binding import (  # noqa: F401
     raw_library,
     topk_paged,
     topk_ragged,
+    topk_select_bf16,
     topk_select_ex,
     workspace_bytes,
 )
 
-__all__ = ["topk_ragged", "topk_paged", "topk_select_ex", "workspace_bytes", "TopkError",
+__all__ = ["topk_ragged", "topk_paged", "topk_select_ex", "topk_select_bf16", "workspace_bytes",
+           "TopkError",
            "Status", "Counter",
            "load_library", "raw_library", "LIB_PATH", "TOPK_MAX_K", "NUM_COUNTERS",
            "DEVICE_ERROR_INDEX"]

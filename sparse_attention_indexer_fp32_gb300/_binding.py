@@ -42,9 +42,11 @@ class Counter(enum.IntEnum):
     DEVICE_ERRORS = 5
     CLUSTER_ROWS = 6
     SPLIT_ROWS = 7
+    SHORT_ROWS = 8
+    SHORT_EXACT = 9
 
 
-NUM_COUNTERS = 8
+NUM_COUNTERS = 16
 
 
 class TopkError(RuntimeError):
@@ -58,7 +60,8 @@ class _DebugOpts(ctypes.Structure):
                 ("stash_capacity", ctypes.c_int32), ("sample_z", ctypes.c_float),
                 ("counters", ctypes.c_void_p), ("probe_stage", ctypes.c_int32),
                 ("probe_wait_us", ctypes.c_uint32), ("split_rows", ctypes.c_int32),
-                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+                ("short_rows", ctypes.c_int32)]
 
 
 _lib = None
@@ -95,6 +98,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.topk_workspace_bytes.restype = ctypes.c_int
         lib.topk_select_noalloc.argtypes = [vp, i64, vp, i32, i32, vp, i64, i32, vp, vp]
         lib.topk_select_noalloc.restype = ctypes.c_int
+        lib.topk_select_bf16.argtypes = [vp, i64, vp, i32, i32, vp, i64, i32, vp, vp]
+        lib.topk_select_bf16.restype = ctypes.c_int
         lib.topk_status_string.argtypes = [ctypes.c_int]
         lib.topk_status_string.restype = ctypes.c_char_p
         lib.topk_abi_version.restype = ctypes.c_int32
@@ -211,7 +216,8 @@ def topk_select_ex(scores: torch.Tensor, lengths: torch.Tensor, k: int,
                    cluster_size: int = 0, stash_capacity: int = 0, sample_z: float = 0.0,
                    counters: Optional[torch.Tensor] = None, probe_stage: int = 0,
                    probe_wait_us: int = 0, split_rows: int = 0,
-                   workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                   workspace: Optional[torch.Tensor] = None, short_rows: int = 0,
+                   stream=None) -> torch.Tensor:
     """Diagnostic variant: same result, with the internal path forced (see the
     header's ``topk_debug_opts``). ``counters`` is an optional int32/uint32
     CUDA tensor of ``NUM_COUNTERS`` entries that the kernel increments;
@@ -230,7 +236,7 @@ def topk_select_ex(scores: torch.Tensor, lengths: torch.Tensor, k: int,
     opts = _DebugOpts(sample_mode, cluster_size, stash_capacity, sample_z,
                       None if counters is None else counters.data_ptr(), probe_stage, probe_wait_us,
                       split_rows, None if workspace is None else workspace.data_ptr(),
-                      0 if workspace is None else workspace.numel())
+                      0 if workspace is None else workspace.numel(), short_rows)
     if counters is not None and (counters.numel() < NUM_COUNTERS or not counters.is_cuda
                                  or counters.element_size() != 4):
         raise ValueError("counters must be a 4-byte CUDA tensor of NUM_COUNTERS entries")
@@ -238,6 +244,37 @@ def topk_select_ex(scores: torch.Tensor, lengths: torch.Tensor, k: int,
         _check(lib.topk_select_ex(scores.data_ptr(), stride, lengths.data_ptr(), B, k, pt_ptr,
                                   pt_stride, page_size, out.data_ptr(), ctypes.byref(opts),
                                   _stream_handle(scores.device, stream)))
+    return out
+
+
+def topk_select_bf16(scores: torch.Tensor, lengths: torch.Tensor, k: int,
+                     page_table: Optional[torch.Tensor] = None, page_size: int = 0,
+                     out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Top-k over bfloat16 scores ``[B, stride]`` (``stride <= 16384``): the
+    indices, ``-1`` padded, or with ``page_table`` the mapped slots, as
+    :func:`topk_ragged` / :func:`topk_paged` on the scores converted to
+    float32."""
+    lib = load_library()
+    if not isinstance(scores, torch.Tensor) or scores.dim() != 2 or scores.dtype != torch.bfloat16 \
+            or not scores.is_cuda or not scores.is_contiguous():
+        raise ValueError("scores must be a contiguous bfloat16 CUDA tensor [B, stride]")
+    B, stride = scores.shape
+    if lengths.dtype != torch.int32 or lengths.device != scores.device or lengths.numel() != B \
+            or not lengths.is_contiguous():
+        raise ValueError("lengths must be a contiguous int32 tensor [B] on the scores' device")
+    if out is None:
+        out = torch.empty((B, max(int(k), 1)), dtype=torch.int32, device=scores.device)
+    pt_ptr, pt_stride = None, 0
+    if page_table is not None:
+        if (page_table.dtype != torch.int32 or page_table.device != scores.device
+                or page_table.dim() != 2 or page_table.shape[0] != B
+                or not page_table.is_contiguous()):
+            raise ValueError("page_table must be a contiguous int32 tensor [B, pages]")
+        pt_ptr, pt_stride = page_table.data_ptr(), page_table.shape[1]
+    with torch.cuda.device(scores.device):
+        _check(lib.topk_select_bf16(scores.data_ptr(), stride, lengths.data_ptr(), B, k, pt_ptr,
+                                    pt_stride, page_size, out.data_ptr(),
+                                    _stream_handle(scores.device, stream)))
     return out
 
 

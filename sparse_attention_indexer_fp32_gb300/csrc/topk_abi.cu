@@ -90,15 +90,45 @@ int auto_cluster_size(int32_t B, int64_t stride, int sm_count) {
 
 bool aligned4(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 3u) == 0; }
 
-topk_status select_impl(const float* scores, int64_t stride, const int32_t* lengths, int32_t B,
-                        int32_t k, const int32_t* page_table, int64_t pt_stride, int32_t page_size,
-                        int32_t* out, void* workspace, size_t workspace_bytes,
+// Launches the short-row kernel (rows of at most tki::kShortMaxRow scores,
+// FP32 or BF16), one CTA per row.
+topk_status launch_short(const void* scores, bool bf16, int64_t stride, const int32_t* lengths,
+                         int32_t B, int32_t k, const int32_t* page_table, int64_t pt_stride,
+                         int32_t page_size, int32_t* out, const topk_debug_opts* opts,
+                         cudaStream_t stream) {
+  tki::ShortParams p = {};
+  p.scores = scores;
+  p.stride = stride;
+  p.lengths = lengths;
+  p.B = B;
+  p.k = k;
+  p.out = out;
+  p.page_table = page_table;
+  p.pt_stride = page_table != nullptr ? pt_stride : 0;
+  p.page_size = page_table != nullptr ? page_size : 1;
+  p.sample_mode = opts != nullptr ? opts->sample_mode : 0;
+  p.sample_z = (opts != nullptr && opts->sample_z != 0.0f) ? opts->sample_z : kDefaultSampleZ;
+  p.counters = opts != nullptr ? opts->counters : nullptr;
+  int dev = 0;
+  DeviceInfo* info = nullptr;
+  const topk_status st = device_info(&dev, &info);
+  if (st != TOPK_OK) return st;
+  if (k <= 512) return tki::launch_short_k512(p, bf16, stream);
+  if (k <= 1024) return tki::launch_short_k1024(p, bf16, stream);
+  return tki::launch_short_k2048(p, bf16, stream);
+}
+
+topk_status select_impl(const void* scores, bool bf16, int64_t stride, const int32_t* lengths,
+                        int32_t B, int32_t k, const int32_t* page_table, int64_t pt_stride,
+                        int32_t page_size, int32_t* out, void* workspace, size_t workspace_bytes,
                         const topk_debug_opts* opts, cudaStream_t stream) {
   if (B < 0 || stride < 1 || stride > INT32_MAX) return TOPK_EINVAL;
   if (k < 1 || k > TOPK_MAX_K) return TOPK_EUNSUPPORTED_K;
   if (B == 0) return TOPK_OK;
   if (scores == nullptr || lengths == nullptr || out == nullptr) return TOPK_EINVAL;
-  if (!aligned4(scores) || !aligned4(lengths) || !aligned4(out)) return TOPK_EINVAL;
+  const uintptr_t score_align = bf16 ? 1u : 3u;
+  if ((reinterpret_cast<uintptr_t>(scores) & score_align) != 0 || !aligned4(lengths) || !aligned4(out))
+    return TOPK_EINVAL;
   if (page_table != nullptr) {
     if (page_size < 1 || pt_stride < 1 || !aligned4(page_table)) return TOPK_EINVAL;
     if (pt_stride < (stride + page_size - 1) / page_size) return TOPK_EINVAL;
@@ -110,7 +140,7 @@ topk_status select_impl(const float* scores, int64_t stride, const int32_t* leng
                                      : tki::StashCap<2048>::value;
 
   Params p = {};
-  p.scores = scores;
+  p.scores = static_cast<const float*>(scores);
   p.stride = stride;
   p.lengths = lengths;
   p.B = B;
@@ -165,6 +195,26 @@ topk_status select_impl(const float* scores, int64_t stride, const int32_t* leng
   } else if (split_rows > 0) {
     return TOPK_EINVAL;
   }
+
+  // Short rows: BF16 scores always, FP32 rows of at most kShortMaxRow scores
+  // unless an option of the streaming kernel is forced.
+  if (opts != nullptr) {
+    if (opts->short_rows < -1 || opts->short_rows > 1) return TOPK_EINVAL;
+    if (opts->sample_mode < 0 || opts->sample_mode > 2) return TOPK_EINVAL;
+    if (opts->counters != nullptr && !aligned4(opts->counters)) return TOPK_EINVAL;
+  }
+  const bool streaming_opts = opts != nullptr && (opts->cluster_size != 0 || opts->stash_capacity != 0 ||
+                                                  opts->probe_stage != 0 || opts->split_rows > 0);
+  const int short_rows = opts != nullptr ? opts->short_rows : 0;
+  const bool fits_short = stride <= tki::kShortMaxRow;
+  if (bf16 || short_rows == 1) {
+    if (!fits_short || streaming_opts || short_rows == -1) return TOPK_EINVAL;
+    return launch_short(scores, bf16, stride, lengths, B, k, page_table, pt_stride, page_size, out,
+                        opts, stream);
+  }
+  if (short_rows == 0 && fits_short && !streaming_opts)
+    return launch_short(scores, false, stride, lengths, B, k, page_table, pt_stride, page_size, out,
+                        opts, stream);
 
   int dev = 0;
   DeviceInfo* info = nullptr;
@@ -244,14 +294,14 @@ extern "C" {
 
 topk_status topk_ragged(const float* scores, int64_t stride, const int32_t* lengths, int32_t B,
                         int32_t k, int32_t* out, topk_stream_t stream) {
-  return select_impl(scores, stride, lengths, B, k, nullptr, 0, 0, out, nullptr, 0, nullptr,
+  return select_impl(scores, false, stride, lengths, B, k, nullptr, 0, 0, out, nullptr, 0, nullptr,
                      reinterpret_cast<cudaStream_t>(stream));
 }
 
 topk_status topk_ragged_ws(const float* scores, int64_t stride, const int32_t* lengths, int32_t B,
                            int32_t k, int32_t* out, void* workspace, size_t workspace_bytes,
                            topk_stream_t stream) {
-  return select_impl(scores, stride, lengths, B, k, nullptr, 0, 0, out, workspace,
+  return select_impl(scores, false, stride, lengths, B, k, nullptr, 0, 0, out, workspace,
                      workspace_bytes, nullptr, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -261,7 +311,7 @@ topk_status topk_paged_ws(const float* scores, int64_t stride, const int32_t* le
                           size_t workspace_bytes, topk_stream_t stream) {
   if (page_table == nullptr && B > 0) return TOPK_EINVAL;
   if (page_size < 1 || pt_stride < 1) return TOPK_EINVAL;
-  return select_impl(scores, stride, lengths, B, k, page_table, pt_stride, page_size, out,
+  return select_impl(scores, false, stride, lengths, B, k, page_table, pt_stride, page_size, out,
                      workspace, workspace_bytes, nullptr, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -285,7 +335,7 @@ topk_status topk_paged(const float* scores, int64_t stride, const int32_t* lengt
                        int32_t* out, topk_stream_t stream) {
   if (page_table == nullptr && B > 0) return TOPK_EINVAL;
   if (page_size < 1 || pt_stride < 1) return TOPK_EINVAL;
-  return select_impl(scores, stride, lengths, B, k, page_table, pt_stride, page_size, out,
+  return select_impl(scores, false, stride, lengths, B, k, page_table, pt_stride, page_size, out,
                      nullptr, 0, nullptr, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -293,8 +343,16 @@ topk_status topk_select_ex(const float* scores, int64_t stride, const int32_t* l
                            int32_t k, const int32_t* page_table, int64_t pt_stride,
                            int32_t page_size, int32_t* out, const topk_debug_opts* opts,
                            topk_stream_t stream) {
-  return select_impl(scores, stride, lengths, B, k, page_table, pt_stride, page_size, out,
+  return select_impl(scores, false, stride, lengths, B, k, page_table, pt_stride, page_size, out,
                      nullptr, 0, opts, reinterpret_cast<cudaStream_t>(stream));
+}
+
+topk_status topk_select_bf16(const uint16_t* scores, int64_t stride, const int32_t* lengths,
+                             int32_t B, int32_t k, const int32_t* page_table, int64_t pt_stride,
+                             int32_t page_size, int32_t* out, topk_stream_t stream) {
+  if (page_table != nullptr && (page_size < 1 || pt_stride < 1)) return TOPK_EINVAL;
+  return select_impl(scores, true, stride, lengths, B, k, page_table, pt_stride, page_size, out,
+                     nullptr, 0, nullptr, reinterpret_cast<cudaStream_t>(stream));
 }
 
 topk_status topk_select_noalloc(const float* scores, int64_t stride, const int32_t* lengths,
@@ -303,7 +361,7 @@ topk_status topk_select_noalloc(const float* scores, int64_t stride, const int32
                                 topk_stream_t stream) {
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   if (B <= 0 || stride < 1 || k < 1 || k > TOPK_MAX_K)  // the plain checks decide these cases
-    return select_impl(scores, stride, lengths, B, k, page_table, pt_stride, page_size, out,
+    return select_impl(scores, false, stride, lengths, B, k, page_table, pt_stride, page_size, out,
                        nullptr, 0, nullptr, cs);
   int dev = 0;
   DeviceInfo* info = nullptr;
@@ -316,7 +374,7 @@ topk_status topk_select_noalloc(const float* scores, int64_t stride, const int32
   void* ws = nullptr;
   st = static_workspace(dev, &ws);
   if (st != TOPK_OK) return st;
-  return select_impl(scores, stride, lengths, B, k, page_table, pt_stride, page_size, out, ws,
+  return select_impl(scores, false, stride, lengths, B, k, page_table, pt_stride, page_size, out, ws,
                      kStaticWsBytes, nullptr, cs);
 }
 
@@ -332,6 +390,6 @@ const char* topk_status_string(topk_status status) {
   }
 }
 
-int32_t topk_abi_version(void) { return 2; }
+int32_t topk_abi_version(void) { return 3; }
 
 }  // extern "C"

@@ -177,8 +177,11 @@ __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
   return v;
 }
 
-template <int C>
-__device__ __forceinline__ uint32_t block_incl_scan(uint32_t v, Smem<C>& S) {
+// The helpers below take any shared-memory layout SM with the members they
+// use (scan, res, hist, skey, sidx, rtab): the streaming kernel's Smem<C>
+// and the short-row kernel's layout.
+template <class SM>
+__device__ __forceinline__ uint32_t block_incl_scan(uint32_t v, SM& S) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   v = warp_incl_scan(v);
   if (lane == 31) S.scan[w] = v;
@@ -195,8 +198,8 @@ __device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t bin) {
 // Locates the bin holding the target-th largest element (1 <= target <= total).
 // Thread t owns BPT consecutive bins, given in DESCENDING bin order in c[].
 // Returns the bin; *above = elements in higher bins; *inbin = elements in it.
-template <int BPT, int C>
-__device__ uint32_t find_bin(const uint32_t (&c)[BPT], uint32_t target, Smem<C>& S,
+template <int BPT, class SM>
+__device__ uint32_t find_bin(const uint32_t (&c)[BPT], uint32_t target, SM& S,
                              uint32_t* above, uint32_t* inbin) {
   constexpr int nbins = BPT * kThreads;
   uint32_t s = 0;
@@ -225,8 +228,8 @@ __device__ uint32_t find_bin(const uint32_t (&c)[BPT], uint32_t target, Smem<C>&
 // G > 1, zeroes them, and finds the bin of the target-th largest element.
 // Must be called by every thread (of every CTA of the cluster) after the
 // histogram increments.
-template <int G, int BPT, int C>
-__device__ uint32_t merged_find(Smem<C>& S, uint32_t target, uint32_t* above, uint32_t* inbin) {
+template <int G, int BPT, class SM>
+__device__ uint32_t merged_find(SM& S, uint32_t target, uint32_t* above, uint32_t* inbin) {
   const int lo = (BPT * kThreads) - BPT * (threadIdx.x + 1);  // lowest owned bin
   uint32_t c[BPT];
   if constexpr (G == 1) {
@@ -287,8 +290,8 @@ __device__ __forceinline__ void load_round(const uint32_t* a, int base, int n,
 
 // Histogram of stash keys: entries e < n with (key >> fshift) == fval (all
 // entries when !filter) add one to bin (key >> dshift) & dmask.
-template <int C>
-__device__ void stash_hist(Smem<C>& S, int n, bool filter, uint32_t fshift, uint32_t fval,
+template <class SM>
+__device__ void stash_hist(SM& S, int n, bool filter, uint32_t fshift, uint32_t fval,
                            uint32_t dshift, uint32_t dmask) {
   for (int base0 = 0; base0 < n; base0 += kRoundEntries) {
     const int base = base0 + kRoundPerThread * threadIdx.x;
@@ -310,8 +313,8 @@ __device__ void stash_hist(Smem<C>& S, int n, bool filter, uint32_t fshift, uint
 // (Inserts do not keep the coarse histogram current: the hits of a stage
 // share a few coarse bins, and their shared atomics would serialise in the
 // streaming loop.) The histogram is all zero on entry and on return.
-template <int G, int C>
-__device__ Cut select_stash(Smem<C>& S, int n, uint32_t target) {
+template <int G, class SM>
+__device__ Cut select_stash(SM& S, int n, uint32_t target) {
   uint32_t above, inbin;
   __syncthreads();  // the last stash writes of every thread are visible
   stash_hist(S, n, false, 0, 0, 21, 0x7ff);
@@ -334,8 +337,8 @@ __device__ Cut select_stash(Smem<C>& S, int n, uint32_t target) {
 // the counts starting at gt0 / eq0 (entries of lower-ranked cluster CTAs).
 // Safe for in-place compaction: pos never exceeds the entry's own position
 // and a round's entries are all read before any of them is written.
-template <int C, class Sink>
-__device__ void emit_rounds(Smem<C>& S, int n, Cut cut, uint32_t gt0, uint32_t eq0, Sink sink) {
+template <class SM, class Sink>
+__device__ void emit_rounds(SM& S, int n, Cut cut, uint32_t gt0, uint32_t eq0, Sink sink) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const uint32_t lt_mask = (1u << lane) - 1u;
   if (cut.all_ties) {

@@ -9,6 +9,7 @@
 
 #include "topk_indexer.h"
 #include "topk_kernel.cuh"
+#include "topk_short.cuh"
 
 namespace tki {
 
@@ -63,6 +64,43 @@ topk_status launch_cluster(const Params& p, int G, int dev, cudaStream_t stream)
   }
 }
 
+
+// Short-row kernel variant (E scores per thread).
+template <int E, int KMAX, bool PAGED, typename T>
+topk_status launch_short_variant(const ShortParams& p, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.B), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, topk_short_kernel<E, KMAX, PAGED, T>, p) == cudaSuccess
+             ? TOPK_OK
+             : TOPK_ECUDA;
+}
+
+// Rows of at most 8192 scores take E = 32, longer ones (up to 16384) E = 64.
+template <int KMAX>
+topk_status launch_short_bucket(const ShortParams& p, bool bf16, cudaStream_t stream) {
+  const bool paged = p.page_table != nullptr;
+  const bool narrow = p.stride <= 32 * kThreads;
+  if (bf16) {
+    if (narrow)
+      return paged ? launch_short_variant<32, KMAX, true, uint16_t>(p, stream)
+                   : launch_short_variant<32, KMAX, false, uint16_t>(p, stream);
+    return paged ? launch_short_variant<64, KMAX, true, uint16_t>(p, stream)
+                 : launch_short_variant<64, KMAX, false, uint16_t>(p, stream);
+  }
+  if (narrow)
+    return paged ? launch_short_variant<32, KMAX, true, float>(p, stream)
+                 : launch_short_variant<32, KMAX, false, float>(p, stream);
+  return paged ? launch_short_variant<64, KMAX, true, float>(p, stream)
+               : launch_short_variant<64, KMAX, false, float>(p, stream);
+}
+
+// Defined in topk_short_k{512,1024,2048}.cu.
+topk_status launch_short_k512(const ShortParams& p, bool bf16, cudaStream_t stream);
+topk_status launch_short_k1024(const ShortParams& p, bool bf16, cudaStream_t stream);
+topk_status launch_short_k2048(const ShortParams& p, bool bf16, cudaStream_t stream);
 
 // Defined in topk_k{512,1024,2048}_{ragged,paged}.cu, one translation unit
 // each so that they compile in parallel.

@@ -1,0 +1,8 @@
+// Short-row kernel variants for k <= 1024 (FP32 and BF16 scores, ragged and paged).
+#include "topk_launch.cuh"
+
+namespace tki {
+topk_status launch_short_k1024(const ShortParams& p, bool bf16, cudaStream_t stream) {
+  return launch_short_bucket<1024>(p, bf16, stream);
+}
+}  // namespace tki

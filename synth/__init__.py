@@ -12,4 +12,6 @@ from .workloads import (  # noqa: F401
     make_workload,
     make_rows,
     config_seed,
+    to_bf16_bits,
+    bf16_bits_to_float,
 )

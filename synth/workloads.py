@@ -5,12 +5,15 @@ generator. Each row has its own stream, keyed by ``SeedSequence([seed, row])``,
 so any subset of rows can be regenerated bit-identically without drawing the
 others (the full-size parity tests use this to check sampled rows).
 
-The five shapes follow the decode-step workloads named for this path: the
+The first five shapes follow the decode-step workloads named for this path: the
 sampled-filter PR of vLLM (PR 56346, "执行摘要": B=1024, 80-100 % ragged,
 128K/k=2048 and 256K/k=512), the narrow-range and >65504 failure triggers of
 the vLLM issue "persistent_topk silently drops top-k candidates ..." (原因分析),
 and the boundary lengths and distributions of the same PR's graph test
-(实现拆解 4).
+(实现拆解 4). Shapes 6 and 7 are the prefill side of the same operation (many
+rows of at most 8192 / 16384 scores, the short-row regime the sampled-filter
+PR's dispatch sends to a separate path, 实现拆解 3), N(0,1) with lengths
+uniform in [0.8 w, w].
 
 Positions at and beyond a row's length are filled with ``PAD_VALUE`` (a quiet
 NaN). The selection contract never looks there, so any read past a row's
@@ -79,6 +82,9 @@ CONFIGS = {
     3: ConfigSpec(3, "B1024_w131072_k2048_ragged", 1024, 131072, 2048),
     4: ConfigSpec(4, "B1024_w262144_k512_paged64", 1024, 262144, 512, page_size=64),
     5: ConfigSpec(5, "B128_w98307_k1024_adversarial", 128, 98307, 1024),
+    # Prefill-shaped batches: many short rows (one per query token of a chunk).
+    6: ConfigSpec(6, "B16384_w8192_k512_prefill", 16384, 8192, 512),
+    7: ConfigSpec(7, "B8192_w16384_k2048_prefill", 8192, 16384, 2048),
 }
 
 
@@ -160,7 +166,13 @@ def _row_cfg5(rng, row, stride, k=1024):
     return x, n
 
 
-_ROW_FNS = {1: _row_cfg1, 2: _row_cfg2, 3: _row_cfg3, 4: _row_cfg4, 5: _row_cfg5}
+def _row_prefill(rng, row, stride):
+    n = _ragged_len(rng, stride)
+    return _normal(rng, stride), n
+
+
+_ROW_FNS = {1: _row_cfg1, 2: _row_cfg2, 3: _row_cfg3, 4: _row_cfg4, 5: _row_cfg5,
+            6: _row_prefill, 7: _row_prefill}
 
 
 def _page_table_cfg4(seed: int, B: int, pt_stride: int) -> np.ndarray:
@@ -190,6 +202,19 @@ def make_rows(config: int, rows: Sequence[int], seed: Optional[int] = None) -> W
         page_table = _page_table_cfg4(seed, spec.B, pt_stride)[rows]
     return Workload(spec.name, config, rows.size, spec.stride, spec.k, scores, lengths,
                     page_table, spec.page_size, rows)
+
+
+def to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """float32 -> bfloat16 bit patterns (uint16), rounding to nearest even;
+    inputs for the BF16 call (NaN is never produced by the generators)."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return r.astype(np.uint16)
+
+
+def bf16_bits_to_float(b: np.ndarray) -> np.ndarray:
+    """bfloat16 bit patterns -> the float32 values they denote (exact)."""
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
 
 
 def make_workload(config: int, seed: Optional[int] = None, B: Optional[int] = None) -> Workload:

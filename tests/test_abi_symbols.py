@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.topk_abi_version() == 2
+    assert lib.topk_abi_version() == 3
     for code in range(5):
         assert lib.topk_status_string(code)
     assert b"unknown" in lib.topk_status_string(99)
@@ -72,6 +72,17 @@ def test_workspace_checks_need_no_gpu(lib):
     assert lib.topk_ragged_ws(some, 64, some, 0, 512, some, ws, big, None) == tk.Status.OK
     assert lib.topk_ragged_ws(some, 64, some, 2, 4096, some, ws, big, None) == \
         tk.Status.EUNSUPPORTED_K
+
+
+def test_bf16_checks_need_no_gpu(lib):
+    some = ctypes.c_void_p(0x1000)
+    # rows wider than 16384 scores, an odd (misaligned) score pointer, k out of range
+    assert lib.topk_select_bf16(some, 16385, some, 2, 512, None, 0, 0, some, None) == tk.Status.EINVAL
+    assert lib.topk_select_bf16(ctypes.c_void_p(0x1001), 64, some, 2, 8, None, 0, 0, some,
+                                None) == tk.Status.EINVAL
+    assert lib.topk_select_bf16(some, 64, some, 2, 2049, None, 0, 0, some, None) == \
+        tk.Status.EUNSUPPORTED_K
+    assert lib.topk_select_bf16(some, 64, some, 0, 8, None, 0, 0, some, None) == tk.Status.OK
 
 
 def test_workspace_bytes(lib):

@@ -54,3 +54,29 @@ def test_config4_page_table_is_a_permutation():
     assert np.array_equal(full_pt[0], w.page_table[0])
     assert np.unique(w.page_table).size == 2 * 4096
     assert w.page_table.min() >= 0 and w.page_table.max() < 1024 * 4096
+
+
+def test_bf16_rounding_is_nearest_even():
+    """The BF16 inputs are the float32 scores rounded to the nearest bfloat16
+    (ties to even), checked against the two neighbouring bfloat16 values."""
+    from synth import bf16_bits_to_float, to_bf16_bits
+
+    rng = np.random.default_rng(0)
+    x = np.concatenate([rng.standard_normal(5000).astype(np.float32),
+                        np.array([1.00390625, 1.01171875, -2.0078125, 0.0, -0.0, 1e-40],
+                                 dtype=np.float32)])
+    b = to_bf16_bits(x)
+    got = bf16_bits_to_float(b).astype(np.float64)
+    lo = bf16_bits_to_float((x.view(np.uint32) >> 16).astype(np.uint16)).astype(np.float64)
+    hi = bf16_bits_to_float(((x.view(np.uint32) >> 16) + 1).astype(np.uint16)).astype(np.float64)
+    xv = x.astype(np.float64)
+    # the result is one of the two neighbours (truncation and one ulp further out) ...
+    assert np.all((got == lo) | (got == hi))
+    # ... the nearer one, and on an exact tie the one with an even last bit
+    d_lo, d_hi = np.abs(xv - lo), np.abs(xv - hi)
+    nearer = np.where(d_lo < d_hi, lo, np.where(d_hi < d_lo, hi, np.nan))
+    tie = np.isnan(nearer)
+    assert np.all(got[~tie] == nearer[~tie])
+    assert np.all((b[tie] & 1) == 0)
+    assert np.array_equal(bf16_bits_to_float(b[-6:-1]),
+                          np.array([1.0, 1.015625, -2.0, 0.0, -0.0], dtype=np.float32))
