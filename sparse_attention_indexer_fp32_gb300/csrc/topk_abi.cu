@@ -113,9 +113,9 @@ topk_status launch_short(const void* scores, bool bf16, int64_t stride, const in
   DeviceInfo* info = nullptr;
   const topk_status st = device_info(&dev, &info);
   if (st != TOPK_OK) return st;
-  if (k <= 512) return tki::launch_short_k512(p, bf16, stream);
-  if (k <= 1024) return tki::launch_short_k1024(p, bf16, stream);
-  return tki::launch_short_k2048(p, bf16, stream);
+  if (k <= 512) return tki::launch_short_k512(p, bf16, dev, info->sm_count, stream);
+  if (k <= 1024) return tki::launch_short_k1024(p, bf16, dev, info->sm_count, stream);
+  return tki::launch_short_k2048(p, bf16, dev, info->sm_count, stream);
 }
 
 topk_status select_impl(const void* scores, bool bf16, int64_t stride, const int32_t* lengths,

@@ -67,7 +67,18 @@ topk_status launch_cluster(const Params& p, int G, int dev, cudaStream_t stream)
 
 // Short-row kernel variant (E scores per thread).
 template <int E, int KMAX, bool PAGED, typename T>
-topk_status launch_short_variant(const ShortParams& p, cudaStream_t stream) {
+topk_status launch_short_variant(const ShortParams& p_in, int dev, int sm_count, cudaStream_t stream) {
+  // CTAs resident at once on this device (per device, found once).
+  static std::atomic<int> resident[64];
+  int per_sm = resident[dev].load(std::memory_order_relaxed);
+  if (per_sm == 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_short_kernel<E, KMAX, PAGED, T>,
+                                                      kThreads, 0) != cudaSuccess)
+      return TOPK_ECUDA;
+    resident[dev].store(per_sm, std::memory_order_relaxed);
+  }
+  ShortParams p = p_in;
+  p.ahead = per_sm * sm_count;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.B), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -80,27 +91,27 @@ topk_status launch_short_variant(const ShortParams& p, cudaStream_t stream) {
 
 // Rows of at most 8192 scores take E = 32, longer ones (up to 16384) E = 64.
 template <int KMAX>
-topk_status launch_short_bucket(const ShortParams& p, bool bf16, cudaStream_t stream) {
+topk_status launch_short_bucket(const ShortParams& p, bool bf16, int dev, int sms, cudaStream_t stream) {
   const bool paged = p.page_table != nullptr;
   const bool narrow = p.stride <= 32 * kThreads;
   if (bf16) {
     if (narrow)
-      return paged ? launch_short_variant<32, KMAX, true, uint16_t>(p, stream)
-                   : launch_short_variant<32, KMAX, false, uint16_t>(p, stream);
-    return paged ? launch_short_variant<64, KMAX, true, uint16_t>(p, stream)
-                 : launch_short_variant<64, KMAX, false, uint16_t>(p, stream);
+      return paged ? launch_short_variant<32, KMAX, true, uint16_t>(p, dev, sms, stream)
+                   : launch_short_variant<32, KMAX, false, uint16_t>(p, dev, sms, stream);
+    return paged ? launch_short_variant<64, KMAX, true, uint16_t>(p, dev, sms, stream)
+                 : launch_short_variant<64, KMAX, false, uint16_t>(p, dev, sms, stream);
   }
   if (narrow)
-    return paged ? launch_short_variant<32, KMAX, true, float>(p, stream)
-                 : launch_short_variant<32, KMAX, false, float>(p, stream);
-  return paged ? launch_short_variant<64, KMAX, true, float>(p, stream)
-               : launch_short_variant<64, KMAX, false, float>(p, stream);
+    return paged ? launch_short_variant<32, KMAX, true, float>(p, dev, sms, stream)
+                 : launch_short_variant<32, KMAX, false, float>(p, dev, sms, stream);
+  return paged ? launch_short_variant<64, KMAX, true, float>(p, dev, sms, stream)
+               : launch_short_variant<64, KMAX, false, float>(p, dev, sms, stream);
 }
 
 // Defined in topk_short_k{512,1024,2048}.cu.
-topk_status launch_short_k512(const ShortParams& p, bool bf16, cudaStream_t stream);
-topk_status launch_short_k1024(const ShortParams& p, bool bf16, cudaStream_t stream);
-topk_status launch_short_k2048(const ShortParams& p, bool bf16, cudaStream_t stream);
+topk_status launch_short_k512(const ShortParams& p, bool bf16, int dev, int sms, cudaStream_t stream);
+topk_status launch_short_k1024(const ShortParams& p, bool bf16, int dev, int sms, cudaStream_t stream);
+topk_status launch_short_k2048(const ShortParams& p, bool bf16, int dev, int sms, cudaStream_t stream);
 
 // Defined in topk_k{512,1024,2048}_{ragged,paged}.cu, one translation unit
 // each so that they compile in parallel.

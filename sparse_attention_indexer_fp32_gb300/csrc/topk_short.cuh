@@ -71,6 +71,7 @@ struct ShortParams {
   int32_t sample_mode;  // 0 automatic, 1 never (exact register path), 2 whenever possible
   float sample_z;
   uint32_t* counters;
+  int32_t ahead;  // CTAs resident at once: the block that will take this CTA's slot next
 };
 
 template <typename T>
@@ -134,6 +135,19 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? 3 : 2) topk_short_kernel(c
 
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
   const int row = static_cast<int>(blockIdx.x);
+  // Start bringing the row of the block that will most likely take this
+  // CTA's slot next into L2, so that its loads do not wait on HBM.
+  if (t == 0 && p.ahead > 0 && row + p.ahead < p.B) {
+    const int nr = row + p.ahead;
+    const int64_t ln = p.lengths[nr];
+    const int len = static_cast<int>(ln < 0 ? 0 : (ln > p.stride ? p.stride : ln));
+    const char* base = reinterpret_cast<const char*>(static_cast<const T*>(p.scores) +
+                                                     static_cast<int64_t>(nr) * p.stride);
+    const uintptr_t a0 = (reinterpret_cast<uintptr_t>(base) + 15u) & ~static_cast<uintptr_t>(15u);
+    const uintptr_t a1 = (reinterpret_cast<uintptr_t>(base) + static_cast<uintptr_t>(len) * sizeof(T)) &
+                         ~static_cast<uintptr_t>(15u);
+    if (a1 > a0) bulk_prefetch_l2(reinterpret_cast<const void*>(a0), static_cast<uint32_t>(a1 - a0));
+  }
   const int64_t len_raw = p.lengths[row];
   const int n = static_cast<int>(len_raw < 0 ? 0 : (len_raw > p.stride ? p.stride : len_raw));
   int32_t* out_row = p.out + static_cast<int64_t>(row) * p.k;

@@ -2,7 +2,7 @@
 #include "topk_launch.cuh"
 
 namespace tki {
-topk_status launch_short_k2048(const ShortParams& p, bool bf16, cudaStream_t stream) {
-  return launch_short_bucket<2048>(p, bf16, stream);
+topk_status launch_short_k2048(const ShortParams& p, bool bf16, int dev, int sms, cudaStream_t stream) {
+  return launch_short_bucket<2048>(p, bf16, dev, sms, stream);
 }
 }  // namespace tki
