@@ -237,7 +237,8 @@ int32_t topk_abi_version(void);
  *                   kernel unless cluster_size, stash_capacity, probe_stage or
  *                   split_rows > 0 is given); -1 never; 1 always (width <= 16384
  *                   and none of those options). In the short-row kernel
- *                   sample_mode 1 selects its exact register path.
+ *                   sample_mode 1 selects its register path for every row
+ *                   (no stash) and sample_z has no effect.
  */
 typedef enum topk_counter {
   TOPK_CNT_ROWS = 0,          /* rows handled */
@@ -249,7 +250,7 @@ typedef enum topk_counter {
   TOPK_CNT_CLUSTER_ROWS = 6,  /* rows split over a cluster of CTAs */
   TOPK_CNT_SPLIT_ROWS = 7,    /* rows streamed by two independent CTAs and merged */
   TOPK_CNT_SHORT_ROWS = 8,    /* rows taken by the short-row kernel */
-  TOPK_CNT_SHORT_EXACT = 9,   /* of them, rows that took its exact register path */
+  TOPK_CNT_SHORT_EXACT = 9,   /* of them, rows selected from registers (no stash) */
   TOPK_NUM_COUNTERS = 16
 } topk_counter;
 

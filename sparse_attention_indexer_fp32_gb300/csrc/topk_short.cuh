@@ -11,20 +11,24 @@
 // shared-memory stash. The design follows the bf16 small-row top-k of the
 // sglang PR 39648 report (实现拆解 2: one CTA per row, the row resident in
 // registers, radix passes to the exact k-th value, page-table transform on
-// output), with the sampled cutoff of vLLM PR 56346 (实现拆解 1) in front:
+// output):
 //
-//  1. Sampled cutoff: E / 16 scores per thread (every 16th score of the row)
-//     go through two 11-bit radix passes to the sample's rank
-//     mu + z*sqrt(mu) + 1, mu = k * samples / n: a cutoff below the row's
-//     k-th largest score with overwhelming probability.
-//  2. Filter: the scores whose key clears the cutoff go to the stash as
-//     (key, index), in index order (per-thread counts, one block prefix).
-//  3. Exact cutoff over the stash and emission in stash (= index) order, with
-//     the streaming kernel's select_stash / emit_rounds.
-//  4. Exact register path: if the cutoff kept fewer than k scores or more
-//     than the stash holds (ties, adversarial rows), or sampling is off, the
-//     radix passes run over the registers themselves and the census writes
-//     the selection straight from them.
+//  1. Coarse pass over the whole row (it is in registers, so this costs no
+//     memory traffic): the 11-bit bin b1 of the k-th largest key, with the
+//     counts above it and in it. If the whole bin is selected, the census
+//     (4) follows at once.
+//  2. Filter: the scores in or above bin b1 go to the stash as (key, index),
+//     in index order (per-thread counts, one block prefix).
+//  3. The finer passes (11, then 10 bits) over the stash entries of bin b1
+//     only, and emission in stash (= index) order with the streaming
+//     kernel's emit_rounds.
+//  4. Exact register path: when bin b1 and above hold more entries than the
+//     stash (ties, narrow rows), the finer passes run over the registers and
+//     a census writes the selection straight from them.
+//
+// A sampled cutoff (the streaming kernel's) was tried here first and was
+// slower: with the row already in registers, its two sample passes cost more
+// than the exact coarse pass they replace.
 #pragma once
 
 #include <cstdint>
@@ -210,114 +214,88 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? 3 : 2) topk_short_kernel(c
     total = __reduce_add_sync(0xffffffffu, e);
   };
 
-  // ---- 1. sampled cutoff ------------------------------------------------------
-  bool fast = false;
-  uint32_t thr = 0;
-  if (p.sample_mode != 1) {
-    // Samples: scores 16 s (s < E / 16) of every thread that has them.
-    const int a = (n + 15) / 16;  // scores at positions that are multiples of 16
-    const float mu = static_cast<float>(kk) * static_cast<float>(a) * __frcp_rn(static_cast<float>(n));
-    float rf = ceilf(mu + p.sample_z * sqrtf(mu)) + 1.0f;
-    rf = fmaxf(rf, 1.0f);
-    if (rf < static_cast<float>(a)) {
-      fast = true;
-      const uint32_t target = static_cast<uint32_t>(rf);
-      uint32_t above, inbin;
+  // ---- 1. the coarse bin of the k-th largest score, over the whole row -------
+  uint32_t above, inbin;
 #pragma unroll
-      for (int s = 0; s < kSamples; ++s)
-        hist_add(S.hist, 16 * s < nv ? (key[16 * s] >> 21) : 0xffffffffu);
-      const uint32_t b1 = merged_find<1, 8>(S, target, &above, &inbin);
-      const uint32_t rem = target - above;
-      if (rem == inbin) {
-        thr = b1 << 21;
-      } else {
-#pragma unroll
-        for (int s = 0; s < kSamples; ++s) {
-          const bool ok = 16 * s < nv && (key[16 * s] >> 21) == b1;
-          hist_add(S.hist, ok ? ((key[16 * s] >> 10) & 0x7ffu) : 0xffffffffu);
-        }
-        const uint32_t b2 = merged_find<1, 8>(S, rem, &above, &inbin);
-        thr = (b1 << 21) | (b2 << 10);
-      }
-    }
-  }
-
-  // ---- 2. filter into the stash, 3. exact cutoff and emission ----------------
-  if (fast) {
+  for (int j = 0; j < E; ++j) hist_add(S.hist, ((valid[j / 32] >> (j % 32)) & 1u) ? (key[j] >> 21) : 0xffffffffu);
+  const uint32_t b1 = merged_find<1, 8>(S, kk, &above, &inbin);
+  uint32_t rem = kk - above;
+  Cut cut;
+  if (rem == inbin) {
+    cut = Cut{21, b1, rem, true};  // the whole bin is selected: straight to the census
+  } else if (p.sample_mode != 1 && above + inbin <= static_cast<uint32_t>(C)) {
+    // ---- 2. the scores in or above that bin go to the stash, in index order --
     uint32_t hit[E / 32];
     uint32_t cnt = 0;
 #pragma unroll
     for (int q = 0; q < E / 32; ++q) {
       uint32_t m = 0;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) m |= static_cast<uint32_t>(key[32 * q + j] >= thr) << j;
+      for (int j = 0; j < 32; ++j) m |= static_cast<uint32_t>((key[32 * q + j] >> 21) >= b1) << j;
       hit[q] = m & valid[q];
       cnt += __popc(hit[q]);
     }
     uint32_t before, total;
-    block_prefix(cnt, before, total);
-    if (total >= kk && total <= static_cast<uint32_t>(C)) {  // uniform
-      uint32_t pos = before;
+    block_prefix(cnt, before, total);  // total == above + inbin
+    uint32_t pos = before;
 #pragma unroll
-      for (int q = 0; q < E / 32; ++q) {
+    for (int q = 0; q < E / 32; ++q) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          if ((hit[q] >> j) & 1u) {
-            S.skey[pos] = key[32 * q + j];
-            S.sidx[pos] = static_cast<uint32_t>(first + 32 * q + j);
-            ++pos;
-          }
+      for (int j = 0; j < 32; ++j) {
+        if ((hit[q] >> j) & 1u) {
+          S.skey[pos] = key[32 * q + j];
+          S.sidx[pos] = static_cast<uint32_t>(first + 32 * q + j);
+          ++pos;
         }
       }
-      if (PAGED) {  // the emission reads the row's page-table entries
-        const int p1 = (n + p.page_size - 1) / p.page_size;
-        for (int q = 32 * t; q < p1; q += 32 * kThreads) prefetch_l2(pt_row + q);
-      }
-      const Cut cut = select_stash<1>(S, static_cast<int>(total), kk);
-      emit_rounds(S, static_cast<int>(total), cut, 0u, 0u, [&](uint32_t pos, uint32_t, uint32_t idx) {
-        if (pos < kk) out_row[pos] = map_index(idx);
-      });
-      if (p.counters != nullptr && t == 0) atomicAdd(&p.counters[kCntSampled], 1u);
-      return;
     }
-    // too few or too many candidates: the exact path below
-  }
-
-  // ---- 4. exact register path --------------------------------------------------
-  if (p.counters != nullptr && t == 0) atomicAdd(&p.counters[kCntShortExact], 1u);
-  Cut cut;
-  {
-    uint32_t above, inbin;
-#pragma unroll
-    for (int j = 0; j < E; ++j) hist_add(S.hist, ((valid[j / 32] >> (j % 32)) & 1u) ? (key[j] >> 21) : 0xffffffffu);
-    const uint32_t b1 = merged_find<1, 8>(S, kk, &above, &inbin);
-    uint32_t rem = kk - above;
+    if (PAGED) {  // the emission reads the row's page-table entries
+      const int p1 = (n + p.page_size - 1) / p.page_size;
+      for (int q = 32 * t; q < p1; q += 32 * kThreads) prefetch_l2(pt_row + q);
+    }
+    // ---- 3. the exact cutoff inside bin b1 (its entries only), emission -------
+    __syncthreads();  // the stash is complete
+    stash_hist(S, static_cast<int>(total), true, 21, b1, 10, 0x7ff);
+    const uint32_t b2 = merged_find<1, 8>(S, rem, &above, &inbin);
+    const uint32_t p2 = (b1 << 11) | b2;
+    rem -= above;
     if (rem == inbin) {
-      cut = Cut{21, b1, rem, true};
+      cut = Cut{10, p2, rem, true};
+    } else {
+      stash_hist(S, static_cast<int>(total), true, 10, p2, 0, 0x3ff);
+      const uint32_t b3 = merged_find<1, 4>(S, rem, &above, &inbin);
+      rem -= above;
+      cut = Cut{0, (p2 << 10) | b3, rem, rem == inbin};
+    }
+    emit_rounds(S, static_cast<int>(total), cut, 0u, 0u, [&](uint32_t pos, uint32_t, uint32_t idx) {
+      if (pos < kk) out_row[pos] = map_index(idx);
+    });
+    return;
+  } else {
+    // ---- 4. exact register path: the finer passes over the registers --------
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+      const bool ok = ((valid[j / 32] >> (j % 32)) & 1u) && (key[j] >> 21) == b1;
+      hist_add(S.hist, ok ? ((key[j] >> 10) & 0x7ffu) : 0xffffffffu);
+    }
+    const uint32_t b2 = merged_find<1, 8>(S, rem, &above, &inbin);
+    const uint32_t p2 = (b1 << 11) | b2;
+    rem -= above;
+    if (rem == inbin) {
+      cut = Cut{10, p2, rem, true};
     } else {
 #pragma unroll
       for (int j = 0; j < E; ++j) {
-        const bool ok = ((valid[j / 32] >> (j % 32)) & 1u) && (key[j] >> 21) == b1;
-        hist_add(S.hist, ok ? ((key[j] >> 10) & 0x7ffu) : 0xffffffffu);
+        const bool ok = ((valid[j / 32] >> (j % 32)) & 1u) && (key[j] >> 10) == p2;
+        hist_add(S.hist, ok ? (key[j] & 0x3ffu) : 0xffffffffu);
       }
-      const uint32_t b2 = merged_find<1, 8>(S, rem, &above, &inbin);
-      const uint32_t p2 = (b1 << 11) | b2;
+      const uint32_t b3 = merged_find<1, 4>(S, rem, &above, &inbin);
       rem -= above;
-      if (rem == inbin) {
-        cut = Cut{10, p2, rem, true};
-      } else {
-#pragma unroll
-        for (int j = 0; j < E; ++j) {
-          const bool ok = ((valid[j / 32] >> (j % 32)) & 1u) && (key[j] >> 10) == p2;
-          hist_add(S.hist, ok ? (key[j] & 0x3ffu) : 0xffffffffu);
-        }
-        const uint32_t b3 = merged_find<1, 4>(S, rem, &above, &inbin);
-        rem -= above;
-        cut = Cut{0, (p2 << 10) | b3, rem, rem == inbin};
-      }
+      cut = Cut{0, (p2 << 10) | b3, rem, rem == inbin};
     }
   }
   // Census: scores above the cut and the first r tied ones (index order).
+  if (p.counters != nullptr && t == 0) atomicAdd(&p.counters[kCntShortExact], 1u);
   uint32_t gtm[E / 32], eqm[E / 32];
   uint32_t c = 0;
 #pragma unroll
