@@ -253,6 +253,88 @@ def bench_workload(config: int, steps: int, warmup: int, world: int, local: int,
     return res
 
 
+def bench_prefill(config: int, local: int, steps: int, warmup: int, world: int, bf16: bool = False):
+    """Prefill-shaped batch (many rows of at most 16384 scores): the
+    short-row kernel, FP32 scores or the same scores rounded to BF16."""
+    import torch
+
+    import sparse_attention_indexer_fp32_gb300 as tk
+    from synth import make_workload, to_bf16_bits
+
+    dev = torch.device("cuda", local)
+    w = make_workload(config)
+    if bf16:
+        s = torch.from_numpy(to_bf16_bits(w.scores).view(np.int16)).to(dev).view(torch.bfloat16)
+    else:
+        s = torch.from_numpy(w.scores).to(dev)
+    l = torch.from_numpy(w.lengths).to(dev)
+    out = torch.empty((w.B, w.k), dtype=torch.int32, device=dev)
+    if bf16:
+        fn = lambda: tk.topk_select_bf16(s, l, w.k, out=out)  # noqa: E731
+    else:
+        fn = lambda: tk.topk_ragged(s, l, w.k, out=out)  # noqa: E731
+    ms = max_over_ranks(time_device(fn, steps, warmup, world), world, dev)
+    us = 1000.0 * ms / steps
+    n = np.clip(w.lengths.astype(np.int64), 0, w.stride)
+    algo = int(n.sum() * (2 if bf16 else 4) + w.B * w.k * 4)
+    peak, peak_kind = measured_peak()
+    achieved = algo / (us * 1e-6) / 1e9
+    del s, l, out
+    torch.cuda.empty_cache()
+    return {"workload": w.name + ("_bf16" if bf16 else ""), "kind": "prefill", "us_per_call": us,
+            "rows_per_s": w.B / (us * 1e-6), "steps": steps,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_kind": f"{peak_kind} hbm_gbs (burst copy)",
+                         "traffic": None, "algorithmic_bytes_per_launch": algo},
+            "config": {"workload": w.name, "B": w.B, "stride": w.stride, "k": w.k,
+                       "dtype": "bf16" if bf16 else "f32",
+                       "lengths": "uniform integer in [ceil(0.8*stride), stride]",
+                       "l2": "inputs larger than L2 (no flush needed)"}}
+
+
+def bench_latency(config: int, local: int, steps: int = 200):
+    """Per-call latency of a small decode batch: eager calls through the
+    Python API, and replays of one call captured in a CUDA graph (the
+    launch path a decode loop uses; lengths may change between replays)."""
+    import torch
+
+    import sparse_attention_indexer_fp32_gb300 as tk
+    from synth import make_workload
+
+    dev = torch.device("cuda", local)
+    w = make_workload(config)
+    s = torch.from_numpy(w.scores).to(dev)
+    l = torch.from_numpy(w.lengths).to(dev)
+    out = torch.empty((w.B, w.k), dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        for _ in range(10):
+            tk.topk_ragged(s, l, w.k, out=out)
+        stream.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(steps):
+            tk.topk_ragged(s, l, w.k, out=out)
+        b.record()
+        b.synchronize()
+        eager = 1000.0 * a.elapsed_time(b) / steps
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            tk.topk_ragged(s, l, w.k, out=out)
+        for _ in range(10):
+            graph.replay()
+        stream.synchronize()
+        a.record()
+        for _ in range(steps):
+            graph.replay()
+        b.record()
+        b.synchronize()
+        replay = 1000.0 * a.elapsed_time(b) / steps
+    return {"workload": w.name, "kind": "latency", "eager_us_per_call": eager,
+            "graph_replay_us_per_call": replay, "steps": steps,
+            "note": "back-to-back calls on one stream; the graph holds one captured call"}
+
+
 def bench_e2e(w, dev, steps: int, world: int):
     """Same call through the public API with host buffers: every step copies the
     inputs from pinned host memory to the device and reads the result back."""
@@ -318,10 +400,15 @@ def run_gpu_arm(args):
     secondary = 3 if primary == 4 else 4
     res = bench_workload(primary, args.steps, args.warmup, world, local, with_e2e=not args.quick,
                          e2e_steps=args.e2e_steps, clocks=not args.quick, rows=args.rows)
-    also = None
+    also = latency = prefill = None
     if not args.quick:
         also = bench_workload(secondary, max(args.steps // 2, 1), args.warmup, world, local,
                               with_e2e=False, e2e_steps=0, clocks=False, rows=args.rows)
+        # every rank runs these (their timing takes the maximum over ranks)
+        latency = bench_latency(1, local)
+        prefill = [bench_prefill(6, local, 200, args.warmup, world),
+                   bench_prefill(7, local, 200, args.warmup, world),
+                   bench_prefill(6, local, 200, args.warmup, world, bf16=True)]
     if rank != 0:
         return
     if args.quick:  # profiling runs: timing of the primary workload only
@@ -356,6 +443,8 @@ def run_gpu_arm(args):
                   "roofline": also["roofline"], "config": also["config"],
                   "steps": max(args.steps // 2, 1),
                   "page_b300_us": PAGE_LATENCY_US.get(secondary)}],
+        "latency": latency,
+        "prefill": prefill,
         "page_b300_us": PAGE_LATENCY_US.get(primary),
         "kernel_source_hash": kernel_source_hash(),
     }
