@@ -2,8 +2,8 @@
 
 Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
 leg may import this package. It compiles ``topk_oracle.cpp`` with the host C++
-compiler on first use (or via :func:`build`) and exposes the two selections on
-numpy arrays. The library it loads is unrelated to the CUDA library of the
+compiler on first use (or via :func:`build`) and exposes the two selections
+and the two-level indexer's block helpers on numpy arrays. The library it loads is unrelated to the CUDA library of the
 product package; they share no source.
 """
 
@@ -64,6 +64,13 @@ class Oracle:
                                           ctypes.c_int32, i32p, ctypes.c_int64, ctypes.c_int32,
                                           i32p]
         lib.oracle_topk_paged.restype = ctypes.c_int
+        lib.oracle_amax8_varlen.argtypes = [f32p, ctypes.c_int64, i32p, ctypes.c_int32,
+                                            ctypes.c_int32, f32p, ctypes.c_int64]
+        lib.oracle_amax8_varlen.restype = ctypes.c_int
+        lib.oracle_sort_candidate_blocks.argtypes = [i32p, ctypes.c_int32, ctypes.c_int32, i32p,
+                                                     ctypes.c_int64, i32p, ctypes.c_int64,
+                                                     ctypes.c_int32, i32p]
+        lib.oracle_sort_candidate_blocks.restype = ctypes.c_int
         lib.oracle_abi_version.restype = ctypes.c_int
         self._lib = lib
         self.path = path
@@ -105,6 +112,38 @@ class Oracle:
         return out
 
 
+    def amax8_varlen(self, scores: np.ndarray, lengths: np.ndarray, topk: int,
+                     out: np.ndarray) -> np.ndarray:
+        """Level-one block keys written into ``out`` (float32 ``[B, >= ceil(stride/8)]``,
+        pre-filled by the caller: slots the definition does not write keep
+        their value)."""
+        scores = np.ascontiguousarray(scores, dtype=np.float32)
+        lengths = np.ascontiguousarray(lengths, dtype=np.int32)
+        out = np.ascontiguousarray(out, dtype=np.float32).copy()
+        B, stride = scores.shape
+        rc = self._lib.oracle_amax8_varlen(self._f32(scores), stride, self._i32(lengths), B, topk,
+                                           self._f32(out), out.shape[1])
+        if rc != ORACLE_OK:
+            raise OracleError(rc)
+        return out
+
+    def sort_candidate_blocks(self, blocks: np.ndarray, lengths: np.ndarray, stride: int,
+                              page_table: np.ndarray, page_size: int):
+        """(ascending block table, pool slots), both int32 ``[B, k]``."""
+        blocks = np.ascontiguousarray(blocks, dtype=np.int32).copy()
+        lengths = np.ascontiguousarray(lengths, dtype=np.int32)
+        page_table = np.ascontiguousarray(page_table, dtype=np.int32)
+        B, k = blocks.shape
+        pages = np.empty_like(blocks)
+        rc = self._lib.oracle_sort_candidate_blocks(self._i32(blocks), B, k, self._i32(lengths),
+                                                    stride, self._i32(page_table),
+                                                    page_table.shape[1], page_size,
+                                                    self._i32(pages))
+        if rc != ORACLE_OK:
+            raise OracleError(rc)
+        return blocks, pages
+
+
 def load(rebuild_if_stale: bool = True) -> Oracle:
     """The oracle built from this directory's source (compiled if missing)."""
     global _lib
@@ -121,6 +160,14 @@ def topk_ragged(scores, lengths, k):
 
 def topk_paged(scores, lengths, k, page_table, page_size):
     return load().topk_paged(scores, lengths, k, page_table, page_size)
+
+
+def amax8_varlen(scores, lengths, topk, out):
+    return load().amax8_varlen(scores, lengths, topk, out)
+
+
+def sort_candidate_blocks(blocks, lengths, stride, page_table, page_size):
+    return load().sort_candidate_blocks(blocks, lengths, stride, page_table, page_size)
 
 
 def source_path() -> str:

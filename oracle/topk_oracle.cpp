@@ -93,7 +93,7 @@ int page_map(int32_t idx, const int32_t* pt_row, int64_t pt_stride, int32_t page
 
 extern "C" {
 
-int oracle_abi_version(void) { return 1; }
+int oracle_abi_version(void) { return 2; }
 
 int oracle_topk_ragged(const float* scores, int64_t stride, const int32_t* lengths, int32_t B,
                        int32_t k, int32_t* out) {
@@ -122,6 +122,96 @@ int oracle_topk_paged(const float* scores, int64_t stride, const int32_t* length
       if (out_row[j] < 0) continue;
       const int prc = page_map(out_row[j], pt_row, pt_stride, page_size, &out_row[j]);
       if (prc != ORACLE_OK) return prc;
+    }
+  }
+  return ORACLE_OK;
+}
+
+// ---------------------------------------------------------------------------
+// The two-level indexer's helpers on either side of the selection (sglang PR
+// 39648 report, 实现拆解 2 table, and the `amax8_varlen` /
+// `sort_candidate_blocks` docstrings of candidate_table.py).
+
+// Level-one keys. For row b: n = clamp(lengths[b], 0, stride) scores,
+// nb = ceil(n / 8) blocks of 8 consecutive scores. If topk > 0 and
+// nb <= topk the row is left untouched (every block is selected anyway).
+// Otherwise out[b, i] = the largest of scores[b, 8i .. 8i + 8) for i < nb - 1,
+// and out[b, nb - 1] = +inf (the newest block is always selected); slots from
+// nb on are not written. out rows are out_stride >= ceil(stride / 8) floats.
+int oracle_amax8_varlen(const float* scores, int64_t stride, const int32_t* lengths, int32_t B,
+                        int32_t topk, float* out, int64_t out_stride) {
+  if (B < 0 || stride < 1 || topk < 0 || out_stride < (stride + 7) / 8) return ORACLE_EARG;
+  if (B > 0 && (scores == nullptr || lengths == nullptr || out == nullptr)) return ORACLE_EARG;
+  for (int32_t b = 0; b < B; ++b) {
+    const int64_t n = valid_length(lengths[b], stride);
+    const int64_t nb = (n + 7) / 8;
+    if (nb == 0 || (topk > 0 && nb <= topk)) continue;
+    const float* row = scores + static_cast<int64_t>(b) * stride;
+    float* out_row = out + static_cast<int64_t>(b) * out_stride;
+    for (int64_t i = 0; i < nb - 1; ++i) {
+      float m = row[8 * i];
+      for (int64_t j = 8 * i; j < 8 * i + 8; ++j) {
+        if (std::isnan(row[j])) return ORACLE_ENAN;
+        if (row[j] > m) m = row[j];
+      }
+      out_row[i] = m;
+    }
+    out_row[nb - 1] = INFINITY;
+  }
+  return ORACLE_OK;
+}
+
+// Block table. For row b: nb = ceil(clamp(lengths[b], 0, stride) / 8) and
+// m = min(k, nb). If nb <= k the table is the identity: blocks[b, j] = j for
+// j < nb, whatever the input. Otherwise the input row holds m distinct block
+// ids in [0, nb) in any order, -1 padded, and they are rewritten in
+// ascending order. Slots from m on hold INT32_MAX. out_pages[b, j] is the
+// pool slot of block blocks[b, j], page_table[b, id / bpp] * bpp + id % bpp
+// with bpp = page_size / 8 (page_size a power of two >= 8), and INT32_MAX in
+// the padded slots. A malformed input row (duplicate or out-of-range ids,
+// a wrong count) is an argument error.
+int oracle_sort_candidate_blocks(int32_t* blocks, int32_t B, int32_t k, const int32_t* lengths,
+                                 int64_t stride, const int32_t* page_table, int64_t pt_stride,
+                                 int32_t page_size, int32_t* out_pages) {
+  if (B < 0 || k < 1 || stride < 1 || page_size < 8 || (page_size & (page_size - 1)) != 0)
+    return ORACLE_EARG;
+  if (B > 0 && (blocks == nullptr || lengths == nullptr || page_table == nullptr ||
+                out_pages == nullptr))
+    return ORACLE_EARG;
+  const int64_t bpp = page_size / 8;
+  for (int32_t b = 0; b < B; ++b) {
+    const int64_t nb = (valid_length(lengths[b], stride) + 7) / 8;
+    const int64_t m = std::min<int64_t>(k, nb);
+    int32_t* row = blocks + static_cast<int64_t>(b) * k;
+    std::vector<int32_t> ids;
+    if (nb <= k) {
+      for (int64_t j = 0; j < nb; ++j) ids.push_back(static_cast<int32_t>(j));
+    } else {
+      for (int32_t j = 0; j < k; ++j) {
+        if (row[j] < 0) continue;
+        if (row[j] >= nb) return ORACLE_EARG;
+        ids.push_back(row[j]);
+      }
+      std::sort(ids.begin(), ids.end());
+      if (static_cast<int64_t>(ids.size()) != m) return ORACLE_EARG;
+      for (size_t j = 1; j < ids.size(); ++j)
+        if (ids[j] == ids[j - 1]) return ORACLE_EARG;
+    }
+    const int32_t* pt_row = page_table + static_cast<int64_t>(b) * pt_stride;
+    int32_t* pages = out_pages + static_cast<int64_t>(b) * k;
+    for (int32_t j = 0; j < k; ++j) {
+      if (j < m) {
+        const int64_t id = ids[static_cast<size_t>(j)];
+        const int64_t page = id / bpp;
+        if (page >= pt_stride) return ORACLE_EPAGE;
+        const int64_t slot = static_cast<int64_t>(pt_row[page]) * bpp + id % bpp;
+        if (slot < INT32_MIN || slot > INT32_MAX) return ORACLE_EPAGE;
+        row[j] = static_cast<int32_t>(id);
+        pages[j] = static_cast<int32_t>(slot);
+      } else {
+        row[j] = INT32_MAX;
+        pages[j] = INT32_MAX;
+      }
     }
   }
   return ORACLE_OK;

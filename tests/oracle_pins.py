@@ -320,6 +320,100 @@ def small_inputs(seed: int = 99):
     return scores, lengths
 
 
+# ------------------------------------------------ two-level indexer helpers
+
+INT32_MAX = np.iinfo(np.int32).max
+SENTINEL = np.float32(-12345.5)
+
+
+def amax8_reference(scores, lengths, topk, width):
+    """Block keys by numpy: pad each row to whole blocks of 8 with -inf and
+    take the maximum over axis 1 of the [blocks, 8] view."""
+    B, stride = scores.shape
+    out = np.full((B, width), SENTINEL, dtype=np.float32)
+    for b in range(B):
+        n = valid_len(lengths[b], stride)
+        nb = -(-n // 8)
+        if nb == 0 or (topk > 0 and nb <= topk):
+            continue
+        padded = np.full(nb * 8, -np.inf, dtype=np.float32)
+        padded[:n] = scores[b, :n]
+        out[b, :nb] = padded.reshape(nb, 8).max(axis=1)
+        out[b, nb - 1] = np.inf
+    return out
+
+
+def pin_amax8(orc) -> None:
+    rng = np.random.default_rng(81)
+    stride = 203
+    scores = rng.standard_normal((40, stride)).astype(np.float32)
+    scores[3] = np.arange(stride, dtype=np.float32)  # ascending: block i's max is 8i + 7
+    scores[4] = -np.inf
+    lengths = np.array([0, 1, 7, 8, 9, 16, 17, 203, 204, -5] + list(rng.integers(0, 260, 30)),
+                       dtype=np.int32)
+    lengths[3] = 203
+    width = -(-stride // 8)
+    for topk in (0, 1, 2, 3, 25, 26):
+        init = np.full((40, width), SENTINEL, dtype=np.float32)
+        got = orc.amax8_varlen(scores, lengths, topk, init)
+        want = amax8_reference(scores, lengths, topk, width)
+        assert np.array_equal(got, want), f"block keys differ (topk={topk})"
+    got = orc.amax8_varlen(scores[3:4], lengths[3:4], 0, np.full((1, width), SENTINEL, np.float32))
+    nb = -(-203 // 8)
+    assert np.array_equal(got[0, : nb - 1], np.arange(nb - 1, dtype=np.float32) * 8 + 7)
+    assert got[0, nb - 1] == np.inf
+
+
+def blocks_reference(blocks, lengths, stride, page_table, page_size):
+    """Block table by numpy: np.sort of the valid ids (identity when a row has
+    at most k blocks), INT32_MAX padding, slots by the pool formula."""
+    B, k = blocks.shape
+    bpp = page_size // 8
+    ids_out = np.full((B, k), INT32_MAX, dtype=np.int64)
+    pages = np.full((B, k), INT32_MAX, dtype=np.int64)
+    for b in range(B):
+        nb = -(-valid_len(lengths[b], stride) // 8)
+        ids = np.arange(nb) if nb <= k else np.sort(blocks[b][blocks[b] >= 0])
+        ids_out[b, : len(ids)] = ids
+        pages[b, : len(ids)] = page_table[b, ids // bpp].astype(np.int64) * bpp + ids % bpp
+    return ids_out.astype(np.int32), pages.astype(np.int32)
+
+
+def pin_sort_candidate_blocks(orc) -> None:
+    rng = np.random.default_rng(82)
+    B, k, stride = 24, 16, 800  # up to 100 blocks per row
+    lengths = np.array([0, 1, 8, 128, 129, 136, 800, 900, -3] + list(rng.integers(0, 800, 15)),
+                       dtype=np.int32)
+    blocks = np.full((B, k), -7, dtype=np.int32)  # rows with <= k blocks: input ignored
+    for b in range(B):
+        nb = -(-valid_len(lengths[b], stride) // 8)
+        if nb > k:
+            sel = rng.choice(nb, k, replace=False).astype(np.int32)
+            blocks[b] = sel  # any order
+    for page_size in (8, 16, 64):
+        bpp = page_size // 8
+        pt = rng.permutation(B * (100 // bpp + 1)).astype(np.int32).reshape(B, -1)
+        got_ids, got_pages = orc.sort_candidate_blocks(blocks, lengths, stride, pt, page_size)
+        want_ids, want_pages = blocks_reference(blocks, lengths, stride, pt, page_size)
+        assert np.array_equal(got_ids, want_ids), f"block ids differ (page {page_size})"
+        assert np.array_equal(got_pages, want_pages), f"pool slots differ (page {page_size})"
+    # a row with exactly k blocks is the identity; a padded (-1) entry in a row
+    # that needs k ids, or a duplicate, is refused
+    one = np.full((1, k), -1, dtype=np.int32)
+    ids, _ = orc.sort_candidate_blocks(one, np.array([8 * k], np.int32), stride,
+                                       np.zeros((1, 100), np.int32), 8)
+    assert np.array_equal(ids[0], np.arange(k))
+    bad = np.arange(k, dtype=np.int32)[None, :].copy()
+    bad[0, 3] = -1
+    for b_ in (bad, np.where(np.arange(k) == 5, 4, np.arange(k)).astype(np.int32)[None, :]):
+        try:
+            orc.sort_candidate_blocks(b_, np.array([8 * k + 8], np.int32), stride,
+                                      np.zeros((1, 100), np.int32), 8)
+        except RuntimeError:
+            continue
+        raise AssertionError("a malformed block row was accepted")
+
+
 def run_all_pins(orc, quick: bool = False) -> None:
     pin_golden(orc)
     pin_closed_forms(orc)
@@ -333,3 +427,5 @@ def run_all_pins(orc, quick: bool = False) -> None:
     rng = np.random.default_rng(5)
     pt = rng.permutation(scores.shape[0] * 48).astype(np.int32).reshape(scores.shape[0], 48)
     pin_paged_formula(orc, scores, lengths, 64, pt, 64)
+    pin_amax8(orc)
+    pin_sort_candidate_blocks(orc)

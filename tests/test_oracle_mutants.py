@@ -37,6 +37,25 @@ MUTANTS = {
                                 "return std::min<int64_t>(len, stride - 1);"),
     # NaN inside the valid prefix accepted silently
     "nan_accepted": ("if (std::isnan(row[i])) return ORACLE_ENAN;", "(void)row;"),
+    # block key misses the last score of each block
+    "amax_block_short": ("for (int64_t j = 8 * i; j < 8 * i + 8; ++j) {",
+                         "for (int64_t j = 8 * i; j < 8 * i + 7; ++j) {"),
+    # newest block not forced to +inf
+    "amax_no_inf": ("out_row[nb - 1] = INFINITY;", "out_row[nb - 1] = row[8 * (nb - 1)];"),
+    # rows with exactly topk blocks not skipped
+    "amax_skip_strict": ("if (nb == 0 || (topk > 0 && nb <= topk)) continue;",
+                         "if (nb == 0 || (topk > 0 && nb < topk)) continue;"),
+    # block table sorted descending
+    "blocks_descending": ("std::sort(ids.begin(), ids.end());",
+                          "std::sort(ids.begin(), ids.end(), [](int32_t a, int32_t b) { return a > b; });"),
+    # a row with exactly k blocks not treated as the identity
+    "blocks_identity_strict": ("    if (nb <= k) {\n      for (int64_t j = 0; j < nb; ++j)",
+                               "    if (nb < k) {\n      for (int64_t j = 0; j < nb; ++j)"),
+    # blocks per page taken as the page size itself
+    "blocks_bpp_page_size": ("const int64_t bpp = page_size / 8;", "const int64_t bpp = page_size;"),
+    # padding written as -1 instead of INT32_MAX
+    "blocks_pad_minus_one": ("        row[j] = INT32_MAX;\n        pages[j] = INT32_MAX;",
+                             "        row[j] = -1;\n        pages[j] = -1;"),
 }
 
 
