@@ -168,6 +168,50 @@ topk_status topk_select_bf16(const uint16_t* scores, int64_t stride, const int32
                              int32_t page_size, int32_t* out, topk_stream_t stream);
 
 /*
+ * The two-level indexer's helpers on either side of the selection (sglang PR
+ * 39648 report, 实现拆解 2 table, and the `amax8_varlen` /
+ * `sort_candidate_blocks` docstrings of its candidate_table.py). With n_b =
+ * clamp(lengths[b], 0, stride) scores, row b has nb_b = ceil(n_b / 8) blocks.
+ *
+ * topk_amax8_varlen - level-one keys: out[b * out_stride + i] = the largest
+ * of scores[b, 8i .. 8i + 8) for i < nb_b - 1, and +inf for i = nb_b - 1 (the
+ * newest block is always selected). Slots from nb_b on are not written. If
+ * topk > 0, rows with nb_b <= topk are skipped entirely (every block would be
+ * selected); topk = 0 never skips.
+ *   scores      [B, stride] float32 (4-byte aligned; rows that start on 32
+ *               bytes, i.e. a 32-byte aligned base and stride % 8 == 0, are
+ *               read with vector loads); no NaN in a row's valid prefix
+ *   out         float32 rows of out_stride >= ceil(stride / 8) entries
+ * Errors: TOPK_EINVAL (B < 0, topk < 0, out_stride too small, null or
+ * misaligned pointers), TOPK_ECUDA, TOPK_EDEVICE.
+ */
+topk_status topk_amax8_varlen(const float* scores, int64_t stride, const int32_t* lengths,
+                              int32_t B, int32_t topk, float* out, int64_t out_stride,
+                              topk_stream_t stream);
+
+/*
+ * topk_sort_candidate_blocks - the block table, in place: blocks [B, k]
+ * int32 holds row b's selected block ids in any order, -1 padded (for
+ * instance the output of topk_ragged over the level-one keys, with lengths
+ * nb_b). They are rewritten in ascending order, INT32_MAX past the last.
+ * out_pages [B, k] receives each id's pool slot,
+ *   page_table[b * pt_stride + id / bpp] * bpp + id % bpp,  bpp = page_size / 8,
+ * and INT32_MAX in the padded slots. A row with nb_b <= k gets the identity
+ * table (0 .. nb_b - 1) and its input is not read.
+ *   page_size   a power of two >= 8
+ *   pt_stride   >= ceil(ceil(stride / 8) / bpp)
+ *   stride      <= 1,048,576 (at most 131072 blocks per row)
+ * Precondition (not checked on the device): a row with nb_b > k holds
+ * min(k, nb_b) distinct ids in [0, nb_b); ids outside that range are ignored,
+ * duplicates collapse. Errors as above.
+ */
+topk_status topk_sort_candidate_blocks(int32_t* blocks, int32_t B, int32_t k,
+                                       const int32_t* lengths, int64_t stride,
+                                       const int32_t* page_table, int64_t pt_stride,
+                                       int32_t page_size, int32_t* out_pages,
+                                       topk_stream_t stream);
+
+/*
  * topk_select_noalloc - the same operation as topk_ragged (page_table NULL)
  * or topk_paged, for callers that cannot allocate device memory: for
  * instance a serving engine that reserves nearly all of HBM for its KV cache

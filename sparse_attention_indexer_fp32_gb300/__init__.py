@@ -18,8 +18,10 @@ from ._binding import (  # noqa: F401
     Counter,
     Status,
     TopkError,
+    amax8_varlen,
     load_library,
     raw_library,
+    sort_candidate_blocks,
     topk_paged,
     topk_ragged,
     topk_select_bf16,
@@ -28,7 +30,7 @@ from ._binding import (  # noqa: F401
 )
 
 __all__ = ["topk_ragged", "topk_paged", "topk_select_ex", "topk_select_bf16", "workspace_bytes",
-           "TopkError",
+           "amax8_varlen", "sort_candidate_blocks", "TopkError",
            "Status", "Counter",
            "load_library", "raw_library", "LIB_PATH", "TOPK_MAX_K", "NUM_COUNTERS",
            "DEVICE_ERROR_INDEX"]

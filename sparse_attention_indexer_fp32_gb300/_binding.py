@@ -100,6 +100,10 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.topk_select_noalloc.restype = ctypes.c_int
         lib.topk_select_bf16.argtypes = [vp, i64, vp, i32, i32, vp, i64, i32, vp, vp]
         lib.topk_select_bf16.restype = ctypes.c_int
+        lib.topk_amax8_varlen.argtypes = [vp, i64, vp, i32, i32, vp, i64, vp]
+        lib.topk_amax8_varlen.restype = ctypes.c_int
+        lib.topk_sort_candidate_blocks.argtypes = [vp, i32, i32, vp, i64, vp, i64, i32, vp, vp]
+        lib.topk_sort_candidate_blocks.restype = ctypes.c_int
         lib.topk_status_string.argtypes = [ctypes.c_int]
         lib.topk_status_string.restype = ctypes.c_char_p
         lib.topk_abi_version.restype = ctypes.c_int32
@@ -276,6 +280,56 @@ def topk_select_bf16(scores: torch.Tensor, lengths: torch.Tensor, k: int,
                                     pt_stride, page_size, out.data_ptr(),
                                     _stream_handle(scores.device, stream)))
     return out
+
+
+def amax8_varlen(scores: torch.Tensor, lengths: torch.Tensor, topk: int = 0,
+                 out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Level-one block keys of the two-level indexer (max of every 8 scores,
+    the newest block +inf, rows with at most ``topk`` blocks skipped). ``out``
+    float32 ``[B, >= ceil(stride / 8)]``; allocated (uninitialised) when not
+    given."""
+    lib = load_library()
+    if not isinstance(scores, torch.Tensor) or scores.dim() != 2 or scores.dtype != torch.float32 \
+            or not scores.is_cuda or not scores.is_contiguous():
+        raise ValueError("scores must be a contiguous float32 CUDA tensor [B, stride]")
+    B, stride = scores.shape
+    if lengths.dtype != torch.int32 or lengths.device != scores.device or lengths.numel() != B:
+        raise ValueError("lengths must be an int32 tensor [B] on the scores' device")
+    if out is None:
+        out = torch.empty((B, (stride + 7) // 8), dtype=torch.float32, device=scores.device)
+    elif out.dtype != torch.float32 or out.device != scores.device or out.dim() != 2 \
+            or out.shape[0] != B or out.stride(1) != 1:
+        raise ValueError("out must be a float32 tensor [B, width] with unit inner stride")
+    with torch.cuda.device(scores.device):
+        _check(lib.topk_amax8_varlen(scores.data_ptr(), stride, lengths.data_ptr(), B, int(topk),
+                                     out.data_ptr(), out.stride(0),
+                                     _stream_handle(scores.device, stream)))
+    return out
+
+
+def sort_candidate_blocks(blocks: torch.Tensor, lengths: torch.Tensor, stride: int,
+                          page_table: torch.Tensor, page_size: int,
+                          out_pages: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Rewrites ``blocks`` (int32 ``[B, k]``, selected block ids in any order,
+    -1 padded) in ascending order with ``INT32_MAX`` padding, and returns the
+    ids' pool slots ``page_table[b, id // bpp] * bpp + id % bpp`` (``bpp =
+    page_size // 8``) in ``out_pages``."""
+    lib = load_library()
+    if blocks.dtype != torch.int32 or not blocks.is_cuda or blocks.dim() != 2 \
+            or not blocks.is_contiguous():
+        raise ValueError("blocks must be a contiguous int32 CUDA tensor [B, k]")
+    B, k = blocks.shape
+    if out_pages is None:
+        out_pages = torch.empty_like(blocks)
+    if page_table.dtype != torch.int32 or not page_table.is_contiguous() or page_table.dim() != 2:
+        raise ValueError("page_table must be a contiguous int32 tensor [B, pages]")
+    with torch.cuda.device(blocks.device):
+        _check(lib.topk_sort_candidate_blocks(blocks.data_ptr(), B, k, lengths.data_ptr(),
+                                              int(stride), page_table.data_ptr(),
+                                              page_table.shape[1], int(page_size),
+                                              out_pages.data_ptr(),
+                                              _stream_handle(blocks.device, stream)))
+    return out_pages
 
 
 def raw_library() -> ctypes.CDLL:

@@ -20,7 +20,7 @@ BUILD = os.path.join(HERE, "_build")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(BUILD, "libtopk_indexer.so")
 SOURCES = (["topk_abi.cu"] + [f"topk_k{k}_{o}.cu" for k in (512, 1024, 2048) for o in ("ragged", "paged")]
-           + [f"topk_short_k{k}.cu" for k in (512, 1024, 2048)])
+           + [f"topk_short_k{k}.cu" for k in (512, 1024, 2048)] + ["topk_blocks.cu"])
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

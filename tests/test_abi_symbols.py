@@ -85,6 +85,21 @@ def test_bf16_checks_need_no_gpu(lib):
     assert lib.topk_select_bf16(some, 64, some, 0, 8, None, 0, 0, some, None) == tk.Status.OK
 
 
+def test_block_helper_checks_need_no_gpu(lib):
+    some = ctypes.c_void_p(0x1000)
+    # out rows narrower than ceil(stride / 8), negative topk, B = 0
+    assert lib.topk_amax8_varlen(some, 64, some, 2, 0, some, 7, None) == tk.Status.EINVAL
+    assert lib.topk_amax8_varlen(some, 64, some, 2, -1, some, 8, None) == tk.Status.EINVAL
+    assert lib.topk_amax8_varlen(some, 64, some, 0, 0, some, 8, None) == tk.Status.OK
+    # page size not a power of two >= 8, page table too narrow, rows too wide
+    assert lib.topk_sort_candidate_blocks(some, 2, 8, some, 64, some, 8, 12, some, None) == tk.Status.EINVAL
+    assert lib.topk_sort_candidate_blocks(some, 2, 8, some, 64, some, 8, 4, some, None) == tk.Status.EINVAL
+    assert lib.topk_sort_candidate_blocks(some, 2, 8, some, 640, some, 9, 64, some, None) == tk.Status.EINVAL
+    assert lib.topk_sort_candidate_blocks(some, 2, 8, some, (1 << 20) + 8, some, 1 << 17, 8, some,
+                                          None) == tk.Status.EINVAL
+    assert lib.topk_sort_candidate_blocks(some, 0, 8, some, 64, some, 8, 8, some, None) == tk.Status.OK
+
+
 def test_workspace_bytes(lib):
     out = ctypes.c_size_t(0)
     # 12 KiB of counters, then per split row and half k keys and k indices
