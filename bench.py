@@ -292,6 +292,55 @@ def bench_prefill(config: int, local: int, steps: int, warmup: int, world: int, 
                        "l2": "inputs larger than L2 (no flush needed)"}}
 
 
+def bench_two_level(local: int, steps: int, warmup: int, world: int):
+    """The two-level indexer's chain on the paged workload's rows: block-max
+    keys (one pass over the scores), top-k over the keys (k = 512 blocks), the
+    sorted block table with pool slots (64-token pages). Each stage timed on
+    its own, and the keys stage against the HBM roofline."""
+    import torch
+
+    import sparse_attention_indexer_fp32_gb300 as tk
+    from synth import make_workload
+
+    dev = torch.device("cuda", local)
+    w = make_workload(4)
+    k_blocks, page_size = 512, 64
+    s = torch.from_numpy(w.scores).to(dev)
+    l = torch.from_numpy(w.lengths).to(dev)
+    n = np.clip(w.lengths.astype(np.int64), 0, w.stride)
+    nb = -(-n // 8)
+    blen = torch.from_numpy(nb.astype(np.int32)).to(dev)
+    pt = torch.from_numpy(np.ascontiguousarray(w.page_table)).to(dev)
+    keys = torch.empty((w.B, -(-w.stride // 8)), dtype=torch.float32, device=dev)
+    sel = torch.empty((w.B, k_blocks), dtype=torch.int32, device=dev)
+    table = torch.empty_like(sel)
+    pages = torch.empty_like(sel)
+    stages = {
+        "amax8_varlen": lambda: tk.amax8_varlen(s, l, k_blocks, out=keys),
+        "topk_over_keys": lambda: tk.topk_ragged(keys, blen, k_blocks, out=sel),
+        "sort_candidate_blocks": lambda: (table.copy_(sel),
+                                          tk.sort_candidate_blocks(table, l, w.stride, pt, page_size,
+                                                                   out_pages=pages)),
+    }
+    res = {}
+    for name, fn in stages.items():
+        ms = max_over_ranks(time_device(fn, steps, warmup, world), world, dev)
+        res[name] = {"us_per_call": 1000.0 * ms / steps}
+    res["sort_candidate_blocks"]["note"] = "includes a device copy of the [B, k] selection (in-place API)"
+    peak, peak_kind = measured_peak()
+    algo = int((nb - 1).clip(min=0).sum() * 32 + nb.sum() * 4)  # scores read + keys written
+    us = res["amax8_varlen"]["us_per_call"]
+    achieved = algo / (us * 1e-6) / 1e9
+    res["amax8_varlen"]["roofline"] = {"bound": "hbm", "achieved": achieved, "peak": peak,
+                                       "unit": "GB/s", "frac": achieved / peak,
+                                       "peak_kind": f"{peak_kind} hbm_gbs (burst copy)",
+                                       "algorithmic_bytes_per_launch": algo}
+    del s, l, blen, pt, keys, sel, table, pages
+    torch.cuda.empty_cache()
+    return {"workload": w.name, "kind": "two_level", "k_blocks": k_blocks, "page_size": page_size,
+            "steps": steps, "stages": res}
+
+
 def bench_latency(config: int, local: int, steps: int = 200):
     """Per-call latency of a small decode batch: eager calls through the
     Python API, and replays of one call captured in a CUDA graph (the
@@ -400,12 +449,13 @@ def run_gpu_arm(args):
     secondary = 3 if primary == 4 else 4
     res = bench_workload(primary, args.steps, args.warmup, world, local, with_e2e=not args.quick,
                          e2e_steps=args.e2e_steps, clocks=not args.quick, rows=args.rows)
-    also = latency = prefill = None
+    also = latency = prefill = two_level = None
     if not args.quick:
         also = bench_workload(secondary, max(args.steps // 2, 1), args.warmup, world, local,
                               with_e2e=False, e2e_steps=0, clocks=False, rows=args.rows)
         # every rank runs these (their timing takes the maximum over ranks)
         latency = bench_latency(1, local)
+        two_level = bench_two_level(local, 200, args.warmup, world)
         prefill = [bench_prefill(6, local, 200, args.warmup, world),
                    bench_prefill(7, local, 200, args.warmup, world),
                    bench_prefill(6, local, 200, args.warmup, world, bf16=True)]
@@ -445,6 +495,7 @@ def run_gpu_arm(args):
                   "page_b300_us": PAGE_LATENCY_US.get(secondary)}],
         "latency": latency,
         "prefill": prefill,
+        "two_level": two_level,
         "page_b300_us": PAGE_LATENCY_US.get(primary),
         "kernel_source_hash": kernel_source_hash(),
     }
