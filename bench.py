@@ -37,7 +37,9 @@ FALLBACK_HBM_GBS = 6800.0
 # The pages' own B300 (GB300 GPU) warm latencies for the same B=1024 ragged
 # workloads (vLLM PR 56346, 执行摘要), context only.
 PAGE_LATENCY_US = {3: 207.06, 4: 301.72}
-WORKLOADS = {"w262144_k512_paged": 4, "w131072_k2048_ragged": 3}
+WORKLOADS = {"w262144_k512_paged": 4, "w131072_k2048_ragged": 3,
+             # prefill shapes (short-row kernel), for profiling runs with --quick
+             "w8192_k512_prefill": 6, "w16384_k2048_prefill": 7}
 
 
 # The files that make up the kernel's device code and launch shape; DRAM
