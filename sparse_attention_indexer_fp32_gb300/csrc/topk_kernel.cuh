@@ -689,8 +689,8 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
   // CTA. Returns this lane's inclusive packed count in the warp, and the
   // packed counts of the lower warps (base) and of all warps (total).
   auto publish = [&](uint32_t cnt, bool err, uint32_t& incl, uint32_t& base, uint32_t& total) {
+    const uint32_t wtot = __reduce_add_sync(0xffffffffu, cnt);  // off the scan's critical path
     incl = warp_incl_scan(cnt);
-    const uint32_t wtot = __shfl_sync(0xffffffffu, incl, 31);
     const bool werr = __any_sync(0xffffffffu, err);
     const int par = static_cast<int>(grp & 1u);
     ++grp;
@@ -797,12 +797,13 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
 
   // Takes stage j from the ring: waits for it (bounded) and returns this
   // thread's 16 scores in it, with the mask of those present.
+  const bool probing = p.probe_stage >= 0;  // test only
   auto take_stage = [&](int j, bool& err, uint32_t& valid, uint32_t& slot) -> const float* {
     slot = consumed % kStages;
     const uint32_t parity = (consumed / kStages) & 1u;
     ++consumed;
     if (!abort) {
-      if (j - s0 == p.probe_stage) {
+      if (probing && j - s0 == p.probe_stage) {
         err |= !mbar_wait_bounded(&S.never, 0u, 1000ull * p.probe_wait_us);  // runs out
       } else if (mbar_wait_bounded(&S.full[slot], parity, kWaitLimitNs)) {
         ++t0_seen;  // in order: stages [t0_seen, issued) are unobserved
