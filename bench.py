@@ -445,6 +445,48 @@ def cpu_baseline(config: int, budget_s: float = 12.0, min_rows: int = 8):
                       f"{elapsed:.1f} s, scaled to the whole batch"}
 
 
+def _oracle_chunk(config: int, rows):
+    """One worker of the parallel CPU baseline: the oracle on these rows
+    (drawn before the clock starts); returns (rows, seconds)."""
+    import oracle
+    from synth import make_rows
+
+    orc = oracle.load(rebuild_if_stale=False)
+    wk = make_rows(config, rows)
+    t0 = time.perf_counter()
+    if wk.page_table is None:
+        orc.topk_ragged(wk.scores, wk.lengths, wk.k)
+    else:
+        orc.topk_paged(wk.scores, wk.lengths, wk.k, wk.page_table, wk.page_size)
+    return len(rows), time.perf_counter() - t0
+
+
+def cpu_baseline_parallel(config: int, rows_per_core: int = 8):
+    """The same oracle over all host cores: one process per core (spawned, so
+    no CUDA state is inherited), each on its own rows; the whole batch's time
+    is scaled from the slowest worker."""
+    import multiprocessing as mp
+
+    import oracle
+    from synth import CONFIGS
+
+    oracle.load()  # compiled once, before the workers start
+    spec = CONFIGS[config]
+    cores = os.cpu_count() or 1
+    order = np.random.default_rng(1).permutation(spec.B)
+    chunks = [order[i * rows_per_core: (i + 1) * rows_per_core].tolist() for i in range(cores)]
+    chunks = [c for c in chunks if c]
+    with mp.get_context("spawn").Pool(len(chunks)) as pool:
+        res = pool.starmap(_oracle_chunk, [(config, c) for c in chunks])
+    rows = sum(r for r, _ in res)
+    slowest = max(t for _, t in res)
+    us = 1e6 * slowest / rows_per_core * spec.B / len(chunks)
+    return {"value": us, "unit": UNIT, "cores": len(chunks), "kind": "oracle",
+            "sample": f"{rows} random rows, {rows_per_core} per process on {len(chunks)} "
+                      f"processes (single-threaded full sort per row); the batch's time "
+                      f"scaled from the slowest process ({slowest:.2f} s)"}
+
+
 def run_gpu_arm(args):
     rank, local, world = dist_setup(args.gpus)
     primary = WORKLOADS[args.workload]
@@ -503,6 +545,7 @@ def run_gpu_arm(args):
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(primary)
+        line["cpu_baseline_all_cores"] = cpu_baseline_parallel(primary)
     print(json.dumps(line), flush=True)
 
 
