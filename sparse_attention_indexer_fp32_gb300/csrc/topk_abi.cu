@@ -90,6 +90,14 @@ int auto_cluster_size(int32_t B, int64_t stride, int sm_count) {
 
 bool aligned4(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 3u) == 0; }
 
+// log2 of a power-of-two page size, else -1 (the kernels then divide).
+int32_t page_shift_of(int32_t page_size) {
+  if (page_size < 1 || (page_size & (page_size - 1)) != 0) return -1;
+  int32_t s = 0;
+  while ((1 << s) < page_size) ++s;
+  return s;
+}
+
 // Launches the short-row kernel (rows of at most tki::kShortMaxRow scores,
 // FP32 or BF16), one CTA per row.
 topk_status launch_short(const void* scores, bool bf16, int64_t stride, const int32_t* lengths,
@@ -106,6 +114,7 @@ topk_status launch_short(const void* scores, bool bf16, int64_t stride, const in
   p.page_table = page_table;
   p.pt_stride = page_table != nullptr ? pt_stride : 0;
   p.page_size = page_table != nullptr ? page_size : 1;
+  p.page_shift = page_shift_of(p.page_size);
   p.sample_mode = opts != nullptr ? opts->sample_mode : 0;
   p.sample_z = (opts != nullptr && opts->sample_z != 0.0f) ? opts->sample_z : kDefaultSampleZ;
   p.counters = opts != nullptr ? opts->counters : nullptr;
@@ -149,6 +158,7 @@ topk_status select_impl(const void* scores, bool bf16, int64_t stride, const int
   p.page_table = page_table;
   p.pt_stride = page_table != nullptr ? pt_stride : 0;
   p.page_size = page_table != nullptr ? page_size : 1;
+  p.page_shift = page_shift_of(p.page_size);
   p.cap = cap_max;
   p.sample_mode = 0;
   p.sample_min_n = kDefaultSampleMinN;

@@ -124,6 +124,7 @@ struct Params {
   const int32_t* page_table;
   int64_t pt_stride;
   int32_t page_size;
+  int32_t page_shift;    // log2(page_size) when it is a power of two, else -1
   int32_t cap;           // stash capacity in use, in [k + kStageFloats, C]
   int32_t sample_mode;   // 0 automatic, 1 never, 2 whenever the row is long enough
   int32_t sample_min_n;  // automatic sampling gate on the row length
@@ -332,9 +333,12 @@ __device__ Cut select_stash(SM& S, int n, uint32_t target) {
   return Cut{0, (p2 << 10) | b3, rem, rem == inbin};
 }
 
-// Walks stash entries [0, n) in order and calls sink(pos, key, idx) for each
-// selected one, pos = (#above-cut before it) + min(#tied before it, r), with
+// Walks stash entries [0, n) in order and calls sink(sel, pos, key, idx) for
+// every one (entries past n as key 0, index 0): sel tells whether it is
+// selected, and then pos = (#above-cut before it) + min(#tied before it, r),
 // the counts starting at gt0 / eq0 (entries of lower-ranked cluster CTAs).
+// The sink may compute from idx unconditionally and store only when sel, so
+// that its loads (a page-table lookup) can all be in flight together.
 // Safe for in-place compaction: pos never exceeds the entry's own position
 // and a round's entries are all read before any of them is written.
 template <class SM, class Sink>
@@ -366,7 +370,9 @@ __device__ void emit_rounds(SM& S, int n, Cut cut, uint32_t gt0, uint32_t eq0, S
       uint32_t pos = run + __reduce_add_sync(0xffffffffu, lane < w ? e : 0u) + psel;
 #pragma unroll
       for (int c = 0; c < kRoundPerThread; ++c) {
-        if ((selm >> c) & 1u) sink(pos++, kv[c], iv[c]);
+        const bool sel = (selm >> c) & 1u;
+        sink(sel, pos, kv[c], base + c < n ? iv[c] : 0u);  // no stale index reaches the sink
+        pos += sel;
       }
       run += __reduce_add_sync(0xffffffffu, e);
     }
@@ -405,7 +411,7 @@ __device__ void emit_rounds(SM& S, int n, Cut cut, uint32_t gt0, uint32_t eq0, S
 #pragma unroll
     for (int c = 0; c < kRoundPerThread; ++c) {
       const bool gt = (gtm >> c) & 1u, eq = (eqm >> c) & 1u;
-      if (gt || (eq && eb < cut.r)) sink(gb + min(eb, cut.r), kv[c], iv[c]);
+      sink(gt || (eq && eb < cut.r), gb + min(eb, cut.r), kv[c], base + c < n ? iv[c] : 0u);
       gb += gt;
       eb += eq;
     }
@@ -447,11 +453,14 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
   const int32_t* pt_row = PAGED ? p.page_table + static_cast<int64_t>(row) * p.pt_stride : nullptr;
   const bool leader = (t == 0 && part == 0);
 
+  // Read-only loads (the table is never written during the call), so the
+  // emission's lookups need not wait for its earlier output stores; a
+  // power-of-two page size maps with a shift and a mask.
   auto map_index = [&](uint32_t i) -> int32_t {
     if constexpr (!PAGED) return static_cast<int32_t>(i);
     const uint32_t ps = static_cast<uint32_t>(p.page_size);
-    const uint32_t page = i / ps;
-    return static_cast<int32_t>(static_cast<int64_t>(pt_row[page]) * ps + (i - page * ps));
+    const uint32_t page = p.page_shift >= 0 ? (i >> p.page_shift) : i / ps;
+    return static_cast<int32_t>(static_cast<int64_t>(__ldg(pt_row + page)) * ps + (i - page * ps));
   };
 
   if (p.counters != nullptr && leader) {
@@ -622,8 +631,8 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
 
   auto compact = [&]() {
     const Cut cut = select_stash<1>(S, static_cast<int>(n_st), kk);
-    emit_rounds(S, static_cast<int>(n_st), cut, 0u, 0u, [&](uint32_t pos, uint32_t key, uint32_t idx) {
-      if (pos < kk) {  // exactly kk entries are selected; the guard only bounds a corrupted cut
+    emit_rounds(S, static_cast<int>(n_st), cut, 0u, 0u, [&](bool sel, uint32_t pos, uint32_t key, uint32_t idx) {
+      if (sel && pos < kk) {  // exactly kk entries are selected; the guard only bounds a corrupted cut
         S.skey[pos] = key;
         S.sidx[pos] = idx;
       }
@@ -884,8 +893,8 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
     if (!abort) {
       if (n_st > need) {
         const Cut c = select_stash<1>(S, static_cast<int>(n_st), need);
-        emit_rounds(S, static_cast<int>(n_st), c, 0u, 0u, [&](uint32_t pos, uint32_t key, uint32_t idx) {
-          if (pos < need) {
+        emit_rounds(S, static_cast<int>(n_st), c, 0u, 0u, [&](bool sel, uint32_t pos, uint32_t key, uint32_t idx) {
+          if (sel && pos < need) {
             p.ws_key[off + pos] = key;
             p.ws_idx[off + pos] = idx;
           }
@@ -933,8 +942,9 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
       S.sidx[e] = __ldcg(&p.ws_idx[src]);
     }
     const Cut c = select_stash<1>(S, static_cast<int>(c0 + c1), kk);
-    emit_rounds(S, static_cast<int>(c0 + c1), c, 0u, 0u, [&](uint32_t pos, uint32_t, uint32_t idx) {
-      if (pos < kk) out_row[pos] = map_index(idx);
+    emit_rounds(S, static_cast<int>(c0 + c1), c, 0u, 0u, [&](bool sel, uint32_t pos, uint32_t, uint32_t idx) {
+      const int32_t v = map_index(idx);
+      if (sel && pos < kk) out_row[pos] = v;
     });
     if (p.counters != nullptr && t == 0) atomicAdd(&p.counters[kCntSplitRows], 1u);
     return;
@@ -981,8 +991,9 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
     }
   }
   emit_rounds(S, static_cast<int>(n_st), cut, gt0, eq0,
-              [&](uint32_t pos, uint32_t, uint32_t idx) {
-                if (pos < kk) out_row[pos] = map_index(idx);
+              [&](bool sel, uint32_t pos, uint32_t, uint32_t idx) {
+                const int32_t v = map_index(idx);
+                if (sel && pos < kk) out_row[pos] = v;
               });
 
   if constexpr (G > 1) cluster_sync();  // no CTA leaves while others may read its shared memory

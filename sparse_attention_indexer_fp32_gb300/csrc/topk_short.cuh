@@ -72,6 +72,7 @@ struct ShortParams {
   const int32_t* page_table;
   int64_t pt_stride;
   int32_t page_size;
+  int32_t page_shift;   // log2(page_size) when it is a power of two, else -1
   int32_t sample_mode;  // 0 automatic, 1 never (exact register path), 2 whenever possible
   float sample_z;
   uint32_t* counters;
@@ -156,11 +157,11 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? 4 : 2) topk_short_kernel(c
   const int n = static_cast<int>(len_raw < 0 ? 0 : (len_raw > p.stride ? p.stride : len_raw));
   int32_t* out_row = p.out + static_cast<int64_t>(row) * p.k;
   const int32_t* pt_row = PAGED ? p.page_table + static_cast<int64_t>(row) * p.pt_stride : nullptr;
-  auto map_index = [&](uint32_t i) -> int32_t {
+  auto map_index = [&](uint32_t i) -> int32_t {  // read-only table loads
     if constexpr (!PAGED) return static_cast<int32_t>(i);
     const uint32_t ps = static_cast<uint32_t>(p.page_size);
-    const uint32_t page = i / ps;
-    return static_cast<int32_t>(static_cast<int64_t>(pt_row[page]) * ps + (i - page * ps));
+    const uint32_t page = p.page_shift >= 0 ? (i >> p.page_shift) : i / ps;
+    return static_cast<int32_t>(static_cast<int64_t>(__ldg(pt_row + page)) * ps + (i - page * ps));
   };
   if (p.counters != nullptr && t == 0) {
     atomicAdd(&p.counters[kCntRows], 1u);
@@ -267,8 +268,9 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? 4 : 2) topk_short_kernel(c
       rem -= above;
       cut = Cut{0, (p2 << 10) | b3, rem, rem == inbin};
     }
-    emit_rounds(S, static_cast<int>(total), cut, 0u, 0u, [&](uint32_t pos, uint32_t, uint32_t idx) {
-      if (pos < kk) out_row[pos] = map_index(idx);
+    emit_rounds(S, static_cast<int>(total), cut, 0u, 0u, [&](bool sel, uint32_t pos, uint32_t, uint32_t idx) {
+      const int32_t v = map_index(idx);
+      if (sel && pos < kk) out_row[pos] = v;
     });
     return;
   } else {
