@@ -47,12 +47,23 @@ WORKLOADS = {"w262144_k512_paged": 4, "w131072_k2048_ragged": 3,
 KERNEL_SOURCES = ("ptx.cuh", "topk_kernel.cuh", "topk_launch.cuh")
 
 
+def _code_only(text: str) -> str:
+    """The source without // comments and blank lines: the hash follows the
+    code, so an edited comment does not mark the counters stale."""
+    lines = []
+    for line in text.splitlines():
+        code = line.split("//", 1)[0].rstrip()
+        if code.strip():
+            lines.append(code)
+    return "\n".join(lines)
+
+
 def kernel_source_hash() -> str:
     csrc = os.path.join(ROOT, "sparse_attention_indexer_fp32_gb300", "csrc")
     h = hashlib.sha256()
     for name in KERNEL_SOURCES:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + b"\0" + f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(name.encode() + b"\0" + _code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
