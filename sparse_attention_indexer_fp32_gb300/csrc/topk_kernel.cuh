@@ -13,10 +13,11 @@
 //     cutoff sits below the row's k-th largest score with overwhelming
 //     probability while keeping a few thousand candidates.
 //  3. Streaming filter. The row body is brought into shared memory by a ring
-//     of 1-D bulk copies (TMA engine, cp.async.bulk + mbarrier); every score
-//     whose key clears the running threshold is appended, in index order, to
-//     a shared-memory stash of (key, index) pairs. Slots come from warp
-//     ballots and a per-stage block prefix (deterministic, no atomics).
+//     of four 16 KiB 1-D bulk copies (TMA engine, cp.async.bulk + mbarrier),
+//     consumed two stages at a time; every score whose key clears the running
+//     threshold is appended, in index order, to a shared-memory stash of
+//     (key, index) pairs. Slots come from per-lane hit counts, a warp scan and
+//     one block prefix per pair of stages (deterministic, no atomics).
 //  4. Compaction instead of truncation. When the stash would overflow, the
 //     exact top-k of the stash is found (below) and kept in place, and the
 //     threshold rises to just above the new cutoff. Nothing a later step
@@ -39,6 +40,11 @@
 // with their own stash; histograms are merged over distributed shared memory
 // so every CTA derives the same cutoffs, and per-CTA counts give each CTA its
 // output offsets.
+//
+// Split rows (this library's own device, for the last partial wave of a large
+// batch): two independent CTAs stream the halves of a row, each leaves its
+// exact top-k in a caller workspace, and the one that finishes second merges
+// them; no CTA waits for another.
 #pragma once
 
 #include <cstdint>
