@@ -42,9 +42,13 @@ WORKLOADS = {"w262144_k512_paged": 4, "w131072_k2048_ragged": 3,
              "w8192_k512_prefill": 6, "w16384_k2048_prefill": 7}
 
 
-# The files that make up the kernel's device code and launch shape; DRAM
-# counters taken on other sources are not reported as this kernel's traffic.
-KERNEL_SOURCES = ("ptx.cuh", "topk_kernel.cuh", "topk_launch.cuh")
+# The files that make up the kernels' device code and launch shapes (every
+# CUDA source of the library: the decode and short-row kernels, the block
+# helpers and the dispatch in the C ABI); DRAM counters taken on other sources
+# are not reported as a kernel's traffic.
+def kernel_sources():
+    csrc = os.path.join(ROOT, "sparse_attention_indexer_fp32_gb300", "csrc")
+    return sorted(n for n in os.listdir(csrc) if n.endswith((".cu", ".cuh")))
 
 
 def _code_only(text: str) -> str:
@@ -61,7 +65,7 @@ def _code_only(text: str) -> str:
 def kernel_source_hash() -> str:
     csrc = os.path.join(ROOT, "sparse_attention_indexer_fp32_gb300", "csrc")
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in kernel_sources():
         with open(os.path.join(csrc, name), encoding="utf-8") as f:
             h.update(name.encode() + b"\0" + _code_only(f.read()).encode())
     return h.hexdigest()[:16]
