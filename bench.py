@@ -42,13 +42,17 @@ WORKLOADS = {"w262144_k512_paged": 4, "w131072_k2048_ragged": 3,
              "w8192_k512_prefill": 6, "w16384_k2048_prefill": 7}
 
 
-# The files that make up the kernels' device code and launch shapes (every
-# CUDA source of the library: the decode and short-row kernels, the block
-# helpers and the dispatch in the C ABI); DRAM counters taken on other sources
-# are not reported as a kernel's traffic.
-def kernel_sources():
-    csrc = os.path.join(ROOT, "sparse_attention_indexer_fp32_gb300", "csrc")
-    return sorted(n for n in os.listdir(csrc) if n.endswith((".cu", ".cuh")))
+# The files that make up each kernel's device code and launch shape. DRAM
+# counters are reported as a kernel's traffic only while the code-only hash of
+# these files equals the one recorded beside the counters.
+_LAUNCH_FILES = ("ptx.cuh", "topk_kernel.cuh", "topk_launch.cuh", "topk_abi.cu")
+KERNEL_SOURCES = {
+    "topk_rows_kernel": _LAUNCH_FILES + tuple(f"topk_k{k}_{o}.cu" for k in (512, 1024, 2048)
+                                              for o in ("ragged", "paged")),
+    "topk_short_kernel": _LAUNCH_FILES + ("topk_short.cuh",) + tuple(f"topk_short_k{k}.cu"
+                                                                   for k in (512, 1024, 2048)),
+    "amax8_kernel": ("ptx.cuh", "topk_kernel.cuh", "topk_blocks.cu"),
+}
 
 
 def _code_only(text: str) -> str:
@@ -62,10 +66,10 @@ def _code_only(text: str) -> str:
     return "\n".join(lines)
 
 
-def kernel_source_hash() -> str:
-    csrc = os.path.join(ROOT, "sparse_attention_indexer_fp32_gb300", "csrc")
+def kernel_source_hash(kernel: str = "topk_rows_kernel", csrc: str = "") -> str:
+    csrc = csrc or os.path.join(ROOT, "sparse_attention_indexer_fp32_gb300", "csrc")
     h = hashlib.sha256()
-    for name in kernel_sources():
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(csrc, name), encoding="utf-8") as f:
             h.update(name.encode() + b"\0" + _code_only(f.read()).encode())
     return h.hexdigest()[:16]
@@ -90,7 +94,9 @@ def profiled_traffic(workload: str):
     except (OSError, ValueError):
         return None
     entry = doc.get("workloads", {}).get(workload)
-    if not entry or doc.get("kernel_source_hash") != kernel_source_hash():
+    if not entry or entry.get("kernel") not in KERNEL_SOURCES:
+        return None
+    if entry.get("kernel_source_hash") != kernel_source_hash(entry["kernel"]):
         return None
     return entry.get("dram_bytes_per_launch")
 
@@ -302,7 +308,8 @@ def bench_prefill(config: int, local: int, steps: int, warmup: int, world: int, 
             "rows_per_s": w.B / (us * 1e-6), "steps": steps,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": f"{peak_kind} hbm_gbs (burst copy)",
-                         "traffic": None, "algorithmic_bytes_per_launch": algo},
+                         "traffic": None if bf16 else profiled_traffic(w.name),
+                         "algorithmic_bytes_per_launch": algo},
             "config": {"workload": w.name, "B": w.B, "stride": w.stride, "k": w.k,
                        "dtype": "bf16" if bf16 else "f32",
                        "lengths": "uniform integer in [ceil(0.8*stride), stride]",
@@ -351,6 +358,7 @@ def bench_two_level(local: int, steps: int, warmup: int, world: int):
     res["amax8_varlen"]["roofline"] = {"bound": "hbm", "achieved": achieved, "peak": peak,
                                        "unit": "GB/s", "frac": achieved / peak,
                                        "peak_kind": f"{peak_kind} hbm_gbs (burst copy)",
+                                       "traffic": profiled_traffic("amax8_varlen_" + w.name.split("_k")[0]),
                                        "algorithmic_bytes_per_launch": algo}
     del s, l, blen, pt, keys, sel, table, pages
     torch.cuda.empty_cache()
@@ -556,7 +564,7 @@ def run_gpu_arm(args):
         "prefill": prefill,
         "two_level": two_level,
         "page_b300_us": PAGE_LATENCY_US.get(primary),
-        "kernel_source_hash": kernel_source_hash(),
+        "kernel_source_hash": {k: kernel_source_hash(k) for k in KERNEL_SOURCES},
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(primary)

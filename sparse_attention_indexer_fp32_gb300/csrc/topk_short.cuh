@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? 4 : 2) topk_short_kernel(c
     const int m = min(max(nv - 32 * q, 0), 32);
     valid[q] = m >= 32 ? 0xffffffffu : ((1u << m) - 1u);
   }
-  for (int i = t; i < kBins; i += kThreads) S.hist[i] = 0;
+  for (int i = t; i < kBins / 4; i += kThreads) reinterpret_cast<uint4*>(S.hist)[i] = make_uint4(0, 0, 0, 0);
   __syncthreads();
 
   int grp = 0;
@@ -217,8 +217,13 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? 4 : 2) topk_short_kernel(c
 
   // ---- 1. the coarse bin of the k-th largest score, over the whole row -------
   uint32_t above, inbin;
+  if (nv == E) {  // every score of this thread exists (all threads but the row's last)
 #pragma unroll
-  for (int j = 0; j < E; ++j) hist_add(S.hist, ((valid[j / 32] >> (j % 32)) & 1u) ? (key[j] >> 21) : 0xffffffffu);
+    for (int j = 0; j < E; ++j) atomicAdd(&S.hist[key[j] >> 21], 1u);
+  } else {
+#pragma unroll
+    for (int j = 0; j < E; ++j) hist_add(S.hist, ((valid[j / 32] >> (j % 32)) & 1u) ? (key[j] >> 21) : 0xffffffffu);
+  }
   const uint32_t b1 = merged_find<1, 8>(S, kk, &above, &inbin);
   uint32_t rem = kk - above;
   Cut cut;
@@ -228,11 +233,12 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? 4 : 2) topk_short_kernel(c
     // ---- 2. the scores in or above that bin go to the stash, in index order --
     uint32_t hit[E / 32];
     uint32_t cnt = 0;
+    const uint32_t lo1 = b1 << 21;  // the lowest key of bin b1
 #pragma unroll
     for (int q = 0; q < E / 32; ++q) {
       uint32_t m = 0;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) m |= static_cast<uint32_t>((key[32 * q + j] >> 21) >= b1) << j;
+      for (int j = 0; j < 32; ++j) m |= static_cast<uint32_t>(key[32 * q + j] >= lo1) << j;
       hit[q] = m & valid[q];
       cnt += __popc(hit[q]);
     }
