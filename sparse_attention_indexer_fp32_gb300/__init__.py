@@ -1,11 +1,16 @@
 """GB300 (sm_103a) batched, ragged, exact per-row top-k over FP32 indexer scores.
 
-Two calls, both enqueued on a CUDA stream and computed entirely by the
-library's CUDA kernels (``_build/libtopk_indexer.so``):
+Every call is enqueued on a CUDA stream and computed entirely by the library's
+CUDA kernels (``_build/libtopk_indexer.so``):
 
 * :func:`topk_ragged` - indices of each row's k largest scores, ``-1`` past
   the row's length;
-* :func:`topk_paged` - the same indices mapped through a page table.
+* :func:`topk_paged` - the same indices mapped through a page table;
+* :func:`topk_select_bf16` - the same selection over bfloat16 scores (rows of
+  at most 16384);
+* :func:`amax8_varlen`, :func:`sort_candidate_blocks` - the two-level
+  indexer's block-max keys and sorted candidate block table;
+* :func:`topk_select_ex` - diagnostics: a forced internal path, path counters.
 
 PyTorch only provides device memory and streams.
 """

@@ -117,10 +117,13 @@ def _check(status: int) -> None:
         raise TopkError(status, f"top-k call failed: {msg}")
 
 
+def _stream(device: torch.device, stream):
+    """The torch stream a call is enqueued on (default: the current one)."""
+    return torch.cuda.current_stream(device) if stream is None else stream
+
+
 def _stream_handle(device: torch.device, stream) -> int:
-    if stream is None:
-        stream = torch.cuda.current_stream(device)
-    return int(stream.cuda_stream)
+    return int(_stream(device, stream).cuda_stream)
 
 
 def workspace_bytes(k: int = TOPK_MAX_K, max_split_rows: int = 0) -> int:
@@ -136,14 +139,25 @@ def workspace_bytes(k: int = TOPK_MAX_K, max_split_rows: int = 0) -> int:
 # one after another, so they can share it; the library leaves its counters
 # zero after every call.
 _workspaces = {}
+_ws_lock = threading.Lock()
 
 
-def _workspace(device: torch.device, stream_handle: int) -> torch.Tensor:
-    key = (device.index, stream_handle)
-    ws = _workspaces.get(key)
-    if ws is None:
-        ws = torch.zeros(workspace_bytes(TOPK_MAX_K), dtype=torch.uint8, device=device)
-        _workspaces[key] = ws
+def _workspace(device: torch.device, stream) -> Optional[torch.Tensor]:
+    """The cached workspace of this device and stream, created (and zeroed on
+    that stream, so that the first call is ordered after the zeroing) on first
+    use. None while the stream captures a CUDA graph and has no workspace yet:
+    zeroing it inside the capture would run only at replay, so the call takes
+    the unsplit path instead (same results)."""
+    stream = _stream(device, stream)
+    key = (device.index, int(stream.cuda_stream))
+    with _ws_lock:
+        ws = _workspaces.get(key)
+        if ws is None:
+            with torch.cuda.stream(stream):
+                if torch.cuda.is_current_stream_capturing():
+                    return None
+                ws = torch.zeros(workspace_bytes(TOPK_MAX_K), dtype=torch.uint8, device=device)
+            _workspaces[key] = ws
     return ws
 
 
@@ -175,13 +189,14 @@ def topk_ragged(scores: torch.Tensor, lengths: torch.Tensor, k: int,
     the current stream). With ``split`` (the default) the call goes through
     ``topk_ragged_ws`` with a workspace cached per device and stream, so that
     the last rows of a large batch may be split over two CTAs; the result is
-    the same either way."""
+    the same either way. A stream's workspace is created by its first call
+    outside a CUDA graph capture: a call captured before that runs unsplit."""
     lib = load_library()
     B, stride, out = _prepare(scores, lengths, k, out)
     with torch.cuda.device(scores.device):
         sh = _stream_handle(scores.device, stream)
-        if split:
-            ws = _workspace(scores.device, sh)
+        ws = _workspace(scores.device, stream) if split else None
+        if ws is not None:
             _check(lib.topk_ragged_ws(scores.data_ptr(), stride, lengths.data_ptr(), B, k,
                                       out.data_ptr(), ws.data_ptr(), ws.numel(), sh))
         else:
@@ -202,8 +217,8 @@ def topk_paged(scores: torch.Tensor, lengths: torch.Tensor, k: int, page_table: 
         raise ValueError("page_table must be a contiguous int32 tensor [B, pages] on the scores' device")
     with torch.cuda.device(scores.device):
         sh = _stream_handle(scores.device, stream)
-        if split:
-            ws = _workspace(scores.device, sh)
+        ws = _workspace(scores.device, stream) if split else None
+        if ws is not None:
             _check(lib.topk_paged_ws(scores.data_ptr(), stride, lengths.data_ptr(), B, k,
                                      page_table.data_ptr(), page_table.shape[1], page_size,
                                      out.data_ptr(), ws.data_ptr(), ws.numel(), sh))

@@ -358,6 +358,39 @@ def test_wait_limit_reports_device_error(cluster):
     check_against_oracle(w.scores, w.lengths, w.k, cluster_size=cluster)
 
 
+def test_capture_before_the_streams_first_call_runs_unsplit():
+    """A stream that captures a graph before any call on it has no workspace
+    yet; zeroing one inside the capture would happen only at replay, so the
+    binding's default call runs unsplit there. The replays match the oracle,
+    and a later eager call on the same stream creates the workspace, splits
+    the last rows, and gives the same indices."""
+    from sparse_attention_indexer_fp32_gb300 import _binding
+
+    w = make_workload(4, B=160)  # 262144-wide rows: the last 144 are split when a workspace is given
+    s, l = to_dev(w.scores), to_dev(w.lengths)
+    tk.topk_ragged(s, l, w.k)  # the library's one-time set-up, on the current stream
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream()
+    key = (0, int(stream.cuda_stream))
+    _binding._workspaces.pop(key, None)  # streams come from a pool: forget an earlier test's
+    out = torch.empty((w.B, w.k), dtype=torch.int32, device="cuda:0")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        tk.topk_ragged(s, l, w.k, out=out)
+    assert key not in _binding._workspaces
+    graph.replay()
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    rows = np.arange(w.B - 24, w.B)
+    assert_parity(w.scores[rows], w.lengths[rows], w.k, got[rows],
+                  run_oracle(w.scores[rows], w.lengths[rows], w.k), rows=rows)
+    with torch.cuda.stream(stream):
+        eager = tk.topk_ragged(s, l, w.k)
+    stream.synchronize()
+    assert key in _binding._workspaces
+    assert np.array_equal(eager.cpu().numpy(), got)
+
+
 @pytest.mark.parametrize("paged,split", [(False, False), (True, False), (False, True)])
 def test_cuda_graph_replay_with_mutated_lengths(paged, split):
     """One captured call replayed with the row lengths (and once the scores)
