@@ -119,3 +119,63 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(_binding, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         _binding.load_library(str(tmp_path / "missing.so"))
+
+
+def _opts(**kw):
+    from sparse_attention_indexer_fp32_gb300._binding import _DebugOpts
+
+    o = _DebugOpts()
+    for name, value in kw.items():
+        setattr(o, name, value)
+    return o
+
+
+def test_debug_option_checks_need_no_gpu(lib):
+    """Every option outside its documented range is refused before anything
+    is enqueued (rows of 65536 scores at k = 512: the streaming kernel's
+    options apply)."""
+    some = ctypes.c_void_p(0x1000)
+
+    def call(B=2, stride=65536, k=512, **kw):
+        return lib.topk_select_ex(some, stride, some, B, k, None, 0, 0, some,
+                                  ctypes.byref(_opts(**kw)), None)
+
+    bad = [
+        dict(sample_mode=-1), dict(sample_mode=3),
+        dict(stash_capacity=512 + 2047), dict(stash_capacity=512 + 4096 + 1),  # [k + 2048, default]
+        dict(cluster_size=3), dict(cluster_size=16), dict(cluster_size=-1),
+        dict(counters=0x1002),  # misaligned
+        dict(probe_stage=-1), dict(probe_stage=1, probe_wait_us=0),
+        dict(probe_stage=1, probe_wait_us=5000001),
+        dict(split_rows=-2), dict(split_rows=3),  # more than B
+        dict(split_rows=1),  # no workspace
+        dict(split_rows=1, workspace=0x100000, workspace_bytes=1 << 20, cluster_size=2),
+        dict(split_rows=1, workspace=0x100008, workspace_bytes=1 << 20),  # misaligned
+        dict(split_rows=1, workspace=0x100000, workspace_bytes=12287),  # below the counters
+        dict(short_rows=2), dict(short_rows=-2),
+    ]
+    for kw in bad:
+        assert call(**kw) == tk.Status.EINVAL, kw
+    # the short-row kernel: rows of at most 16384 scores, no streaming-kernel option
+    assert call(stride=16385, short_rows=1) == tk.Status.EINVAL
+    assert call(stride=8192, short_rows=1, cluster_size=2) == tk.Status.EINVAL
+    assert call(stride=8192, short_rows=1, stash_capacity=4000) == tk.Status.EINVAL
+    # k is checked first; B = 0 is a no-op whatever the options
+    assert call(k=2049, sample_mode=3) == tk.Status.EUNSUPPORTED_K
+    assert call(B=0, cluster_size=3) == tk.Status.OK
+
+
+def test_noalloc_checks_need_no_gpu(lib):
+    """B <= 0 and k out of range are decided before the call looks at the
+    device (the other argument checks follow its device query)."""
+    some = ctypes.c_void_p(0x1000)
+    assert lib.topk_select_noalloc(some, 64, some, 0, 512, None, 0, 0, some, None) == tk.Status.OK
+    assert lib.topk_select_noalloc(some, 64, some, 2, 0, None, 0, 0, some, None) == \
+        tk.Status.EUNSUPPORTED_K
+    assert lib.topk_select_noalloc(some, 64, some, 2, 2049, None, 0, 0, some, None) == \
+        tk.Status.EUNSUPPORTED_K
+    assert lib.topk_select_noalloc(some, 64, some, -1, 512, None, 0, 0, some, None) == \
+        tk.Status.EINVAL
+    assert lib.topk_select_noalloc(some, 0, some, 2, 512, None, 0, 0, some, None) == \
+        tk.Status.EINVAL
+    assert b"scratch" in lib.topk_status_string(tk.Status.ESCRATCH)
