@@ -106,6 +106,16 @@ def algorithmic_bytes(lengths: np.ndarray, stride: int, B: int, k: int) -> int:
     return int(n.sum() * 4 + B * k * 4)
 
 
+def hbm_roofline(algo: int, us: float, traffic=None) -> dict:
+    """The roofline object of a launch that moves `algo` algorithmic bytes in
+    `us` microseconds, against the measured HBM peak."""
+    peak, peak_kind = measured_peak()
+    achieved = algo / (us * 1e-6) / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "peak_kind": f"{peak_kind} hbm_gbs (burst copy)",
+            "traffic": traffic, "algorithmic_bytes_per_launch": int(algo)}
+
+
 # ----------------------------------------------------------------- clocks
 
 
@@ -350,16 +360,20 @@ def bench_two_level(local: int, steps: int, warmup: int, world: int):
     for name, fn in stages.items():
         ms = max_over_ranks(time_device(fn, steps, warmup, world), world, dev)
         res[name] = {"us_per_call": 1000.0 * ms / steps}
-    res["sort_candidate_blocks"]["note"] = "includes a device copy of the [B, k] selection (in-place API)"
-    peak, peak_kind = measured_peak()
-    algo = int((nb - 1).clip(min=0).sum() * 32 + nb.sum() * 4)  # scores read + keys written
-    us = res["amax8_varlen"]["us_per_call"]
-    achieved = algo / (us * 1e-6) / 1e9
-    res["amax8_varlen"]["roofline"] = {"bound": "hbm", "achieved": achieved, "peak": peak,
-                                       "unit": "GB/s", "frac": achieved / peak,
-                                       "peak_kind": f"{peak_kind} hbm_gbs (burst copy)",
-                                       "traffic": profiled_traffic("amax8_varlen_" + w.name.split("_k")[0]),
-                                       "algorithmic_bytes_per_launch": algo}
+    res["sort_candidate_blocks"]["note"] = ("includes a device copy of the [B, k] selection (in-place "
+                                            "API); algorithmic bytes: ids read and written, one "
+                                            "page-table entry read and one pool slot written per id")
+    # keys: the scores read (the newest block is +inf, not read) and the keys written
+    algo_keys = int((nb - 1).clip(min=0).sum() * 32 + nb.sum() * 4)
+    res["amax8_varlen"]["roofline"] = hbm_roofline(
+        algo_keys, res["amax8_varlen"]["us_per_call"],
+        profiled_traffic("amax8_varlen_" + w.name.split("_k")[0]))
+    # top-k over the keys: the keys read and the block ids written
+    algo_sel = algorithmic_bytes(nb, keys.shape[1], w.B, k_blocks)
+    res["topk_over_keys"]["roofline"] = hbm_roofline(algo_sel, res["topk_over_keys"]["us_per_call"])
+    algo_table = 4 * w.B * k_blocks * 4
+    res["sort_candidate_blocks"]["roofline"] = hbm_roofline(
+        algo_table, res["sort_candidate_blocks"]["us_per_call"])
     del s, l, blen, pt, keys, sel, table, pages
     torch.cuda.empty_cache()
     return {"workload": w.name, "kind": "two_level", "k_blocks": k_blocks, "page_size": page_size,
