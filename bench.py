@@ -326,6 +326,26 @@ def bench_prefill(config: int, local: int, steps: int, warmup: int, world: int, 
                        "l2": "inputs larger than L2 (no flush needed)"}}
 
 
+def two_level_rooflines(res: dict, nb: np.ndarray, keys_stride: int, B: int, k_blocks: int,
+                        workload: str) -> None:
+    """Adds the roofline of each two-level stage to `res` (stage -> {"us_per_call"}),
+    from the rows' block counts `nb`."""
+    res["sort_candidate_blocks"]["note"] = ("includes a device copy of the [B, k] selection (in-place "
+                                            "API); algorithmic bytes: ids read and written, one "
+                                            "page-table entry read and one pool slot written per id")
+    # keys: the scores read (the newest block is +inf, not read) and the keys written
+    algo_keys = int((nb - 1).clip(min=0).sum() * 32 + nb.sum() * 4)
+    res["amax8_varlen"]["roofline"] = hbm_roofline(
+        algo_keys, res["amax8_varlen"]["us_per_call"],
+        profiled_traffic("amax8_varlen_" + workload.split("_k")[0]))
+    # top-k over the keys: the keys read and the block ids written
+    algo_sel = algorithmic_bytes(nb, keys_stride, B, k_blocks)
+    res["topk_over_keys"]["roofline"] = hbm_roofline(algo_sel, res["topk_over_keys"]["us_per_call"])
+    algo_table = 4 * B * k_blocks * 4
+    res["sort_candidate_blocks"]["roofline"] = hbm_roofline(
+        algo_table, res["sort_candidate_blocks"]["us_per_call"])
+
+
 def bench_two_level(local: int, steps: int, warmup: int, world: int):
     """The two-level indexer's chain on the paged workload's rows: block-max
     keys (one pass over the scores), top-k over the keys (k = 512 blocks), the
@@ -360,20 +380,7 @@ def bench_two_level(local: int, steps: int, warmup: int, world: int):
     for name, fn in stages.items():
         ms = max_over_ranks(time_device(fn, steps, warmup, world), world, dev)
         res[name] = {"us_per_call": 1000.0 * ms / steps}
-    res["sort_candidate_blocks"]["note"] = ("includes a device copy of the [B, k] selection (in-place "
-                                            "API); algorithmic bytes: ids read and written, one "
-                                            "page-table entry read and one pool slot written per id")
-    # keys: the scores read (the newest block is +inf, not read) and the keys written
-    algo_keys = int((nb - 1).clip(min=0).sum() * 32 + nb.sum() * 4)
-    res["amax8_varlen"]["roofline"] = hbm_roofline(
-        algo_keys, res["amax8_varlen"]["us_per_call"],
-        profiled_traffic("amax8_varlen_" + w.name.split("_k")[0]))
-    # top-k over the keys: the keys read and the block ids written
-    algo_sel = algorithmic_bytes(nb, keys.shape[1], w.B, k_blocks)
-    res["topk_over_keys"]["roofline"] = hbm_roofline(algo_sel, res["topk_over_keys"]["us_per_call"])
-    algo_table = 4 * w.B * k_blocks * 4
-    res["sort_candidate_blocks"]["roofline"] = hbm_roofline(
-        algo_table, res["sort_candidate_blocks"]["us_per_call"])
+    two_level_rooflines(res, nb, int(keys.shape[1]), w.B, k_blocks, w.name)
     del s, l, blen, pt, keys, sel, table, pages
     torch.cuda.empty_cache()
     return {"workload": w.name, "kind": "two_level", "k_blocks": k_blocks, "page_size": page_size,
