@@ -134,7 +134,6 @@ struct ScoreIn<uint16_t> {
 template <int E, int KMAX, bool PAGED, typename T>
 __global__ void __launch_bounds__(kThreads, E <= 32 ? 4 : 2) topk_short_kernel(const ShortParams p) {
   constexpr int C = ShortCap<KMAX>::value;
-  constexpr int kSamples = E / 16;  // per thread
   static_assert(E % 32 == 0 && E * kThreads <= kShortMaxRow, "a row must fit the CTA's registers");
   __shared__ __align__(16) ShortSmem<C> S;
 
