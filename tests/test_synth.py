@@ -80,3 +80,28 @@ def test_bf16_rounding_is_nearest_even():
     assert np.all((b[tie] & 1) == 0)
     assert np.array_equal(bf16_bits_to_float(b[-6:-1]),
                           np.array([1.0, 1.015625, -2.0, 0.0, -0.0], dtype=np.float32))
+
+
+def test_config3_offsets_config4_spikes_and_prefill_rows():
+    """The value recipes: N(0,1) plus one offset per row in [-4, 4] (workload
+    3); N(0,1) with about 1 % of positions raised by U(3, 6) (workload 4);
+    N(0,1) rows of 80-100 % length for the prefill shapes (workloads 6, 7)."""
+    w = make_rows(3, range(16))
+    means = np.array([w.scores[b, : w.lengths[b]].mean() for b in range(16)])
+    stds = np.array([w.scores[b, : w.lengths[b]].std() for b in range(16)])
+    assert np.all(np.abs(means) < 4.02) and np.ptp(means) > 1.0  # offsets differ per row
+    assert np.all(np.abs(stds - 1.0) < 0.02)
+    w = make_rows(4, [0, 1])
+    for b in range(2):
+        x = w.scores[b, : w.lengths[b]].astype(np.float64)
+        # spikes: x > 2.5 is N(0,1)'s 0.6 % tail plus ~1 % raised by at least 3
+        frac = float(np.mean(x > 2.5))
+        assert 0.013 < frac < 0.019, frac
+        assert x.max() < 6.0 + 6.0  # U(3, 6) over N(0,1)
+    for cfg in (6, 7):
+        spec = CONFIGS[cfg]
+        w = make_rows(cfg, [0, spec.B // 2, spec.B - 1])
+        assert w.scores.shape == (3, spec.stride)
+        assert w.lengths.min() >= int(np.ceil(0.8 * spec.stride)) and w.lengths.max() <= spec.stride
+        x = w.scores[0, : w.lengths[0]]
+        assert abs(float(x.mean())) < 0.05 and abs(float(x.std()) - 1.0) < 0.05
