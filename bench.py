@@ -34,6 +34,7 @@ if ROOT not in sys.path:
 METRIC = "µs/call and scores-read GB/s (% of HBM peak) at B=1024, 80–100% ragged, k=512/2048"
 UNIT = "µs/call"
 FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 2 ** 20  # GB300
 # The pages' own B300 (GB300 GPU) warm latencies for the same B=1024 ragged
 # workloads (vLLM PR 56346, 执行摘要), context only.
 PAGE_LATENCY_US = {3: 207.06, 4: 301.72}
@@ -99,6 +100,16 @@ def profiled_traffic(workload: str):
     if entry.get("kernel_source_hash") != kernel_source_hash(entry["kernel"]):
         return None
     return entry.get("dram_bytes_per_launch")
+
+
+def workload_config(spec) -> dict:
+    """The `config` object of a bench line for a workload (both arms print it)."""
+    return {"workload": spec.name, "B": spec.B, "stride": spec.stride, "k": spec.k,
+            "lengths": "uniform integer in [ceil(0.8*stride), stride]",
+            "paged": bool(spec.page_size), "page_size": spec.page_size or None,
+            "scores": "f32", "keys": "u32 order-preserving keys of the f32 scores (exact ranking)",
+            "scores_bytes": int(spec.B) * int(spec.stride) * 4,
+            "l2": "inputs larger than L2 (no flush needed)"}
 
 
 def algorithmic_bytes(lengths: np.ndarray, stride: int, B: int, k: int) -> int:
@@ -236,7 +247,7 @@ def bench_workload(config: int, steps: int, warmup: int, world: int, local: int,
     import torch
 
     import sparse_attention_indexer_fp32_gb300 as tk
-    from synth import make_workload
+    from synth import CONFIGS, make_workload
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
@@ -271,11 +282,7 @@ def bench_workload(config: int, steps: int, warmup: int, world: int, local: int,
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} hbm_gbs (burst copy)",
                      "traffic": profiled_traffic(w.name),
                      "algorithmic_bytes_per_launch": algo},
-        "config": {"workload": w.name, "B": w.B, "stride": w.stride, "k": w.k,
-                   "lengths": "uniform integer in [ceil(0.8*stride), stride]",
-                   "paged": pt is not None, "page_size": w.page_size or None,
-                   "scores_bytes": int(w.scores.nbytes),
-                   "l2": "inputs larger than L2 (no flush needed)"},
+        "config": dict(workload_config(CONFIGS[config]), B=w.B, scores_bytes=int(w.scores.nbytes)),
         "gpu_launches": steps,
         "sampler": sampler.summary() if sampler else None,
     }
@@ -330,9 +337,10 @@ def two_level_rooflines(res: dict, nb: np.ndarray, keys_stride: int, B: int, k_b
                         workload: str) -> None:
     """Adds the roofline of each two-level stage to `res` (stage -> {"us_per_call"}),
     from the rows' block counts `nb`."""
-    res["sort_candidate_blocks"]["note"] = ("includes a device copy of the [B, k] selection (in-place "
-                                            "API); algorithmic bytes: ids read and written, one "
-                                            "page-table entry read and one pool slot written per id")
+    res["sort_candidate_blocks"]["note"] = ("the kernel alone (the table is sorted in place; repeated "
+                                            "calls redo the same counting sort); algorithmic bytes: "
+                                            "ids read and written, one page-table entry read and one "
+                                            "pool slot written per id")
     # keys: the scores read (the newest block is +inf, not read) and the keys written
     algo_keys = int((nb - 1).clip(min=0).sum() * 32 + nb.sum() * 4)
     res["amax8_varlen"]["roofline"] = hbm_roofline(
@@ -372,12 +380,17 @@ def bench_two_level(local: int, steps: int, warmup: int, world: int):
     stages = {
         "amax8_varlen": lambda: tk.amax8_varlen(s, l, k_blocks, out=keys),
         "topk_over_keys": lambda: tk.topk_ragged(keys, blen, k_blocks, out=sel),
-        "sort_candidate_blocks": lambda: (table.copy_(sel),
-                                          tk.sort_candidate_blocks(table, l, w.stride, pt, page_size,
-                                                                   out_pages=pages)),
+        # in place: after the first call the table is already ascending, and a
+        # repeated call redoes the same counting sort (its cost does not depend
+        # on the order of the ids)
+        "sort_candidate_blocks": lambda: tk.sort_candidate_blocks(table, l, w.stride, pt, page_size,
+                                                                  out_pages=pages),
     }
     res = {}
     for name, fn in stages.items():
+        if name == "sort_candidate_blocks":  # the selection, once, outside the timed region
+            stages["topk_over_keys"]()
+            table.copy_(sel)
         ms = max_over_ranks(time_device(fn, steps, warmup, world), world, dev)
         res[name] = {"us_per_call": 1000.0 * ms / steps}
     two_level_rooflines(res, nb, int(keys.shape[1]), w.B, k_blocks, w.name)
@@ -387,7 +400,7 @@ def bench_two_level(local: int, steps: int, warmup: int, world: int):
             "steps": steps, "stages": res}
 
 
-def bench_latency(config: int, local: int, steps: int = 200):
+def bench_latency(config: int, local: int, steps: int = 200, cold_steps: int = 50):
     """Per-call latency of a small decode batch: eager calls through the
     Python API, and replays of one call captured in a CUDA graph (the
     launch path a decode loop uses; lengths may change between replays)."""
@@ -425,9 +438,29 @@ def bench_latency(config: int, local: int, steps: int = 200):
         b.record()
         b.synchronize()
         replay = 1000.0 * a.elapsed_time(b) / steps
+
+        # Cold L2: before every call a buffer twice the L2's size is written
+        # (outside the timed events), so the call finds none of its inputs there.
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
+        cold = {}
+        for mode, fn in (("eager", lambda: tk.topk_ragged(s, l, w.k, out=out)),
+                         ("graph_replay", graph.replay)):
+            times = []
+            for i in range(cold_steps):
+                flush.fill_(i)
+                a.record()
+                fn()
+                b.record()
+                b.synchronize()
+                times.append(1000.0 * a.elapsed_time(b))
+            cold[mode] = statistics.median(times)
+        del flush
     return {"workload": w.name, "kind": "latency", "eager_us_per_call": eager,
             "graph_replay_us_per_call": replay, "steps": steps,
-            "note": "back-to-back calls on one stream; the graph holds one captured call"}
+            "cold_l2_eager_us_per_call": cold["eager"],
+            "cold_l2_graph_replay_us_per_call": cold["graph_replay"], "cold_steps": cold_steps,
+            "note": "warm: back-to-back calls on one stream; cold: median of single calls, each "
+                    "after writing a buffer of twice the L2 size; the graph holds one captured call"}
 
 
 def bench_e2e(w, dev, steps: int, world: int):
@@ -531,6 +564,180 @@ def cpu_baseline_parallel(config: int, rows_per_core: int = 8):
                       f"scaled from the slowest process ({slowest:.2f} s)"}
 
 
+# ------------------------------------------------------------- dispatch sweep
+
+SWEEP_WIDTHS = (4096, 8192, 16384, 32768, 65536, 131072, 196608, 262144)
+SWEEP_BATCHES = (1, 4, 16, 64, 256, 1024, 2048)
+SWEEP_KS = (512, 1024, 2048)
+SWEEP_MAX_ELEMS = 2048 * 262144  # 2 GiB of scores at most
+
+
+def _sweep_split_rows(B: int, sm_count: int) -> int:
+    """The split-row count of the automatic policy without its width gate."""
+    slots = 2 * sm_count
+    r = B % slots if B >= slots else B
+    return min(r, slots - r)
+
+
+def sweep_paths(width: int, B: int, sm_count: int):
+    """(name, options) of every path worth timing on rows of this width."""
+    paths = [("auto", {})]
+    if width <= 16384:
+        paths += [("short", dict(short_rows=1)), ("short_regs", dict(short_rows=1, sample_mode=1))]
+    for G in (1, 2, 4, 8, 16):
+        if width // G < 4096:  # a CTA would stream less than one stage
+            continue
+        for sm in (1, 2):
+            paths.append((f"G{G}_{'sampled' if sm == 2 else 'full'}",
+                          dict(short_rows=-1, cluster_size=G, sample_mode=sm)))
+    m = _sweep_split_rows(B, sm_count)
+    if width >= 32768 and 0 < m <= 1024:
+        paths.append((f"G1_split{m}", dict(short_rows=-1, cluster_size=1, split_rows=m)))
+    if width >= 32768 and B <= 512 and B != m:
+        paths.append(("G1_split_all", dict(short_rows=-1, cluster_size=1, split_rows=B)))
+    return paths
+
+
+def run_sweep(args):
+    """Times every path of the library on N(0,1) rows over batch x width x k,
+    with full and 80-100 % ragged lengths; writes the measurements (JSON) and
+    a summary table (markdown) under the output folder."""
+    import torch
+
+    import sparse_attention_indexer_fp32_gb300 as tk
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0x5EED0100)
+    big = torch.randn(SWEEP_MAX_ELEMS, generator=gen, device=dev, dtype=torch.float32)
+    ws = torch.zeros(tk.workspace_bytes(2048, 1024), dtype=torch.uint8, device=dev)
+    cnt = torch.zeros(tk.NUM_COUNTERS, dtype=torch.int32, device=dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    results = []
+    t0 = time.time()
+    for width in SWEEP_WIDTHS:
+        for B in SWEEP_BATCHES:
+            if B * width > SWEEP_MAX_ELEMS:
+                continue
+            scores = big[: B * width].view(B, width)
+            for lmode in ("full", "ragged"):
+                if lmode == "full":
+                    lengths = torch.full((B,), width, dtype=torch.int32, device=dev)
+                else:
+                    lengths = torch.randint(-(-width * 4 // 5), width + 1, (B,), generator=gen,
+                                            device=dev, dtype=torch.int32)
+                n = int(lengths.clamp(0, width).sum().item())
+                for k in SWEEP_KS:
+                    out = torch.empty((B, k), dtype=torch.int32, device=dev)
+                    rec = {"width": width, "B": B, "lengths": lmode, "k": k, "paths": {}}
+                    for name, opts in sweep_paths(width, B, sms):
+                        if name == "auto":
+                            fn = lambda: tk.topk_ragged(scores, lengths, k, out=out)  # noqa: E731
+                        else:
+                            o = dict(opts)
+                            if "split_rows" in o:
+                                o["workspace"] = ws
+                            fn = lambda o=o: tk.topk_select_ex(scores, lengths, k, out=out, **o)  # noqa: E731
+                        for _ in range(3):
+                            fn()
+                        reps = 20
+                        start.record()
+                        for _ in range(reps):
+                            fn()
+                        end.record()
+                        end.synchronize()
+                        rec["paths"][name] = 1000.0 * start.elapsed_time(end) / reps
+                    # what the automatic policy did, from the device counters
+                    cnt.zero_()
+                    tk.topk_select_ex(scores, lengths, k, out=out, counters=cnt,
+                                      workspace=ws if width > 16384 else None)
+                    c = cnt.cpu().tolist()
+                    rec["auto_counters"] = {"short": c[tk.Counter.SHORT_ROWS],
+                                            "cluster": c[tk.Counter.CLUSTER_ROWS],
+                                            "split": c[tk.Counter.SPLIT_ROWS],
+                                            "sampled": c[tk.Counter.SAMPLED]}
+                    rec["algorithmic_bytes"] = n * 4 + B * k * 4
+                    results.append(rec)
+    doc = {"sm_count": sms, "gpu": torch.cuda.get_device_name(dev), "seconds": time.time() - t0,
+           "reps": 20, "warmup": 3, "command": "python bench.py --sweep --sweep-out DIR",
+           "results": results}
+    os.makedirs(args.sweep_out, exist_ok=True)
+    with open(os.path.join(args.sweep_out, "dispatch_sweep.json"), "w") as f:
+        json.dump(doc, f)
+    with open(os.path.join(args.sweep_out, "dispatch_sweep.md"), "w") as f:
+        f.write(sweep_markdown(doc))
+    print(json.dumps({"sweep": len(results), "seconds": doc["seconds"]}), flush=True)
+
+
+def sweep_markdown(doc: dict) -> str:
+    """Summary tables of a sweep: per shape the automatic path against the
+    best forced one, and the comparisons each dispatch gate rests on."""
+    peak, _ = measured_peak()
+    res = doc["results"]
+    lines = [f"# Dispatch sweep: every path of the library over batch x width x k",
+             "",
+             f"GPU: {doc['gpu']} ({doc['sm_count']} SMs). Command: `{doc['command']}`. N(0,1) rows "
+             f"(seeded torch generator on the device), lengths full or uniform in [0.8w, w]; each "
+             f"path {doc['warmup']} warm-up calls then {doc['reps']} timed back-to-back (CUDA "
+             f"events; small shapes stay in L2). Times in us per call. `frac` = algorithmic bytes / "
+             f"time / {peak:.0f} GB/s.",
+             ""]
+    lines += ["## Automatic policy against the best forced path (ragged lengths)", "",
+              "| k | width | B | auto us | frac | best path | best us | auto/best |",
+              "|---|---|---|---|---|---|---|---|"]
+    for r in res:
+        if r["lengths"] != "ragged":
+            continue
+        p = r["paths"]
+        best = min((v, n) for n, v in p.items() if n != "auto")
+        frac = r["algorithmic_bytes"] / (p["auto"] * 1e-6) / 1e9 / peak
+        lines.append(f"| {r['k']} | {r['width']} | {r['B']} | {p['auto']:.1f} | {frac:.2f} | "
+                     f"{best[1]} | {best[0]:.1f} | {p['auto'] / best[0]:.2f} |")
+    lines += ["", "## Gate: short-row kernel against the streaming kernel (width <= 16384)", "",
+              "| k | width | B | lengths | short us | short_regs us | best streaming | us |",
+              "|---|---|---|---|---|---|---|---|"]
+    for r in res:
+        if r["width"] > 16384:
+            continue
+        p = r["paths"]
+        st = min((v, n) for n, v in p.items() if n.startswith("G"))
+        lines.append(f"| {r['k']} | {r['width']} | {r['B']} | {r['lengths']} | {p['short']:.1f} | "
+                     f"{p['short_regs']:.1f} | {st[1]} | {st[0]:.1f} |")
+    lines += ["", "## Gate: sampled cutoff against the full stream (one CTA per row, ragged)", "",
+              "| k | width | B | full us | sampled us | sampled/full |", "|---|---|---|---|---|---|"]
+    for r in res:
+        if r["lengths"] != "ragged" or "G1_full" not in r["paths"]:
+            continue
+        p = r["paths"]
+        lines.append(f"| {r['k']} | {r['width']} | {r['B']} | {p['G1_full']:.1f} | "
+                     f"{p['G1_sampled']:.1f} | {p['G1_sampled'] / p['G1_full']:.2f} |")
+    lines += ["", "## Gate: split rows of the last wave (one CTA per row, sampled, ragged)", "",
+              "| k | width | B | unsplit us | split path | split us | split/unsplit |",
+              "|---|---|---|---|---|---|---|"]
+    for r in res:
+        if r["lengths"] != "ragged":
+            continue
+        p = r["paths"]
+        for n, v in p.items():
+            if n.startswith("G1_split") and "G1_sampled" in p:
+                lines.append(f"| {r['k']} | {r['width']} | {r['B']} | {p['G1_sampled']:.1f} | {n} | "
+                             f"{v:.1f} | {v / p['G1_sampled']:.2f} |")
+    lines += ["", "## Gate: cluster size (sampled, ragged): time per G", "",
+              "| k | width | B | G1 | G2 | G4 | G8 | G16 | best |", "|---|---|---|---|---|---|---|---|---|"]
+    for r in res:
+        if r["lengths"] != "ragged" or r["width"] <= 16384:
+            continue
+        p = r["paths"]
+        cells = [p.get(f"G{g}_sampled") for g in (1, 2, 4, 8, 16)]
+        vals = [(v, g) for v, g in zip(cells, (1, 2, 4, 8, 16)) if v is not None]
+        best = min(vals)[1]
+        lines.append(f"| {r['k']} | {r['width']} | {r['B']} | " +
+                     " | ".join("-" if v is None else f"{v:.1f}" for v in cells) + f" | G{best} |")
+    return "\n".join(lines) + "\n"
+
+
 def run_gpu_arm(args):
     rank, local, world = dist_setup(args.gpus)
     primary = WORKLOADS[args.workload]
@@ -556,6 +763,10 @@ def run_gpu_arm(args):
         return
     clocks = res.pop("sampler")
     also.pop("sampler")
+    also_line = {"workload": also["workload"], "us_per_call": also["us_per_call"],
+                 "rows_per_s": also["rows_per_s"], "scores_read_gbs": also["scores_read_gbs"],
+                 "roofline": also["roofline"], "config": also["config"],
+                 "steps": max(args.steps // 2, 1), "page_b300_us": PAGE_LATENCY_US.get(secondary)}
     line = {
         "metric": METRIC,
         "value": res["us_per_call"],
@@ -567,7 +778,7 @@ def run_gpu_arm(args):
         "higher_is_better": False,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "u32",
+        "dtype": "f32",
         "data": "synthetic (seeded Philox rows shaped like the decode-step indexer workload)",
         "config": dict(res["config"], parallelism=f"replicas x{world}"),
         "rows_per_s": res["rows_per_s"] * world,
@@ -576,11 +787,6 @@ def run_gpu_arm(args):
         "clocks": clocks,
         "e2e": res["e2e"],
         "gpu_launches": res["gpu_launches"],
-        "also": [{"workload": also["workload"], "us_per_call": also["us_per_call"],
-                  "rows_per_s": also["rows_per_s"], "scores_read_gbs": also["scores_read_gbs"],
-                  "roofline": also["roofline"], "config": also["config"],
-                  "steps": max(args.steps // 2, 1),
-                  "page_b300_us": PAGE_LATENCY_US.get(secondary)}],
         "latency": latency,
         "prefill": prefill,
         "two_level": two_level,
@@ -590,7 +796,35 @@ def run_gpu_arm(args):
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(primary)
         line["cpu_baseline_all_cores"] = cpu_baseline_parallel(primary)
+    # The other metric workload, then a compact summary of every line: last,
+    # so that a reader keeping only the end of the line still has them.
+    line["also"] = [also_line]
+    line["summary"] = summary_of(line)
     print(json.dumps(line), flush=True)
+
+
+def summary_of(line: dict) -> list:
+    """One short entry per timed workload: time per call, roofline fraction
+    of the measured peak, DRAM traffic per launch (null when not captured on
+    the current kernel source)."""
+    def entry(name, us, roof):
+        return {"w": name, "us": round(us, 2), "frac": round(roof["frac"], 3),
+                "traffic": roof.get("traffic"), "algo": roof["algorithmic_bytes_per_launch"]}
+
+    out = [entry(line["config"]["workload"], line["value"], line["roofline"])]
+    out += [entry(a["workload"], a["us_per_call"], a["roofline"]) for a in line.get("also") or []]
+    out += [entry(p["workload"], p["us_per_call"], p["roofline"]) for p in line.get("prefill") or []]
+    tl = line.get("two_level")
+    if tl:
+        out += [entry(f"{name}_{tl['workload']}", st["us_per_call"], st["roofline"])
+                for name, st in tl["stages"].items()]
+    lat = line.get("latency")
+    if lat:
+        out.append({"w": lat["workload"], "eager_us": round(lat["eager_us_per_call"], 2),
+                    "graph_us": round(lat["graph_replay_us_per_call"], 2),
+                    "cold_eager_us": round(lat["cold_l2_eager_us_per_call"], 2),
+                    "cold_graph_us": round(lat["cold_l2_graph_replay_us_per_call"], 2)})
+    return out
 
 
 def run_reference_arm(args):
@@ -631,14 +865,13 @@ def run_reference_arm(args):
         "impl": "reference",
         "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1000.0 * elapsed / args.steps,
-        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "u32",
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded Philox rows shaped like the decode-step indexer workload)",
-        "config": {"workload": spec.name, "B": spec.B, "stride": spec.stride, "k": spec.k,
-                   "paged": bool(spec.page_size), "page_size": spec.page_size or None,
-                   "parallelism": "none (host oracle)"},
+        "config": dict(workload_config(spec), parallelism="replicas x1"),
         "cpu_baseline": {"value": us, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": f"{args.steps} steps of {rows_per_step} row each, cycling over "
-                                   f"{pool.B} random rows; scaled to the {spec.B}-row batch"},
+                                   f"{pool.B} random rows; scaled to the {spec.B}-row batch "
+                                   "(the host oracle, one thread: no GPU and no replicas)"},
         "e2e": {"value": us, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
@@ -658,10 +891,16 @@ def main(argv=None):
                     help="use only the first ROWS rows of the workload (profiling runs)")
     ap.add_argument("--quick", action="store_true",
                     help="primary workload only, no e2e / clocks / CPU baseline (profiling runs)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time every path over batch x width x k instead (dispatch sweep)")
+    ap.add_argument("--sweep-out", default="gpurun_out",
+                    help="folder for the sweep's JSON and markdown summary")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    if args.impl == "reference":
+    if args.sweep:
+        run_sweep(args)
+    elif args.impl == "reference":
         run_reference_arm(args)
     else:
         run_gpu_arm(args)

@@ -175,7 +175,9 @@ topk_status topk_select_bf16(const uint16_t* scores, int64_t stride, const int32
  *
  * topk_amax8_varlen - level-one keys: out[b * out_stride + i] = the largest
  * of scores[b, 8i .. 8i + 8) for i < nb_b - 1, and +inf for i = nb_b - 1 (the
- * newest block is always selected). Slots from nb_b on are not written. If
+ * newest block is always selected). "Largest" is in the selection's order,
+ * +0 above -0, so a block whose maximum is a zero gets +0 if it holds one,
+ * whatever the order of its scores (the page's fmaxf leaves that sign open). Slots from nb_b on are not written. If
  * topk > 0, rows with nb_b <= topk are skipped entirely (every block would be
  * selected); topk = 0 never skips.
  *   scores      [B, stride] float32 (4-byte aligned; rows that start on 32
@@ -227,12 +229,15 @@ topk_status topk_sort_candidate_blocks(int32_t* blocks, int32_t B, int32_t k,
  * A call that would split more rows than that returns TOPK_ESCRATCH before
  * anything is enqueued.
  *
- * The first call on a device looks up the array's device address and clears
- * its counters (a synchronous cudaMemset); make that first call before any
- * stream capture. Every call shares the one array: calls that may run at the
- * same time on the GPU (other streams, other host threads) race on it, so
- * serialise them. The caller still passes inputs and outputs as for
- * topk_ragged / topk_paged, with the same contract.
+ * The first call on a device looks up the array's device address and
+ * enqueues a clear of its counters on that call's stream, ahead of its
+ * kernel (the array is also zero when the library's module loads); make that
+ * first call before any stream capture. Every call shares the one array:
+ * calls that may run at the same time on the GPU (other streams, other host
+ * threads) race on it, so serialise them. The caller still passes inputs and
+ * outputs as for topk_ragged / topk_paged, with the same contract; invalid
+ * arguments return TOPK_EINVAL / TOPK_EUNSUPPORTED_K exactly as there, before
+ * the scratch is sized.
  */
 topk_status topk_select_noalloc(const float* scores, int64_t stride, const int32_t* lengths,
                                 int32_t B, int32_t k, const int32_t* page_table,
@@ -253,8 +258,9 @@ int32_t topk_abi_version(void);
  *
  *   sample_mode     0 automatic, 1 never use the sampled cutoff,
  *                   2 use it on every row long enough to sample
- *   cluster_size    0 automatic, 1 one CTA per row, or 2 / 4 / 8 CTAs of a
- *                   thread-block cluster per row
+ *   cluster_size    0 automatic, 1 one CTA per row, or 2 / 4 / 8 / 16 CTAs
+ *                   of a thread-block cluster per row (16 is a non-portable
+ *                   cluster size; the automatic policy uses at most 8)
  *   stash_capacity  0 = default; otherwise the candidate-buffer size to use,
  *                   in [k + 2048, default]: small values force the in-buffer
  *                   compaction path on ordinary inputs. The default is

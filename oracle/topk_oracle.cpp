@@ -138,6 +138,9 @@ int oracle_topk_paged(const float* scores, int64_t stride, const int32_t* length
 // Otherwise out[b, i] = the largest of scores[b, 8i .. 8i + 8) for i < nb - 1,
 // and out[b, nb - 1] = +inf (the newest block is always selected); slots from
 // nb on are not written. out rows are out_stride >= ceil(stride / 8) floats.
+// "Largest" is taken in the same total order as the selection (+0 above -0):
+// the page names fmaxf, which leaves the sign of a zero maximum open, and this
+// reading makes the key independent of the order of the block's scores.
 int oracle_amax8_varlen(const float* scores, int64_t stride, const int32_t* lengths, int32_t B,
                         int32_t topk, float* out, int64_t out_stride) {
   if (B < 0 || stride < 1 || topk < 0 || out_stride < (stride + 7) / 8) return ORACLE_EARG;
@@ -152,7 +155,7 @@ int oracle_amax8_varlen(const float* scores, int64_t stride, const int32_t* leng
       float m = row[8 * i];
       for (int64_t j = 8 * i; j < 8 * i + 8; ++j) {
         if (std::isnan(row[j])) return ORACLE_ENAN;
-        if (row[j] > m) m = row[j];
+        if (ranks_above(row[j], m)) m = row[j];
       }
       out_row[i] = m;
     }

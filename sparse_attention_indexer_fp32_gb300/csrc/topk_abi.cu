@@ -81,14 +81,31 @@ topk_status device_info(int* dev, DeviceInfo** info) {
   return TOPK_OK;
 }
 
-// CTAs per row: enough to occupy the GPU when the batch is small, as long as
+// Resident clusters of G CTAs for the variant of this k bucket and output.
+int max_clusters(int kmax, bool paged, int G, int dev) {
+  switch (kmax) {
+    case 512: return paged ? tki::clusters_k512_paged(G, dev) : tki::clusters_k512_ragged(G, dev);
+    case 1024: return paged ? tki::clusters_k1024_paged(G, dev) : tki::clusters_k1024_ragged(G, dev);
+    default: return paged ? tki::clusters_k2048_paged(G, dev) : tki::clusters_k2048_ragged(G, dev);
+  }
+}
+
+// Largest cluster the automatic policy picks.
+constexpr int kAutoMaxCluster = 8;
+
+// CTAs per row: enough to occupy the GPU when the batch is small. G doubles
+// while the clusters of every row still fit on the GPU at once (the driver's
+// answer for clusters of that size, which must each sit in one GPC) and
 // every CTA still gets a long slice of the row.
-int auto_cluster_size(int32_t B, int64_t stride, int sm_count) {
-  const int64_t resident = 2LL * sm_count;  // two CTAs per SM
+int auto_cluster_size(int32_t B, int64_t stride, int kmax, bool paged, int dev) {
   int G = 1;
-  while (G < 8 && static_cast<int64_t>(B) * (2 * G) <= resident &&
-         stride / (2 * G) >= kMinClusterSlice)
-    G *= 2;
+  while (G < kAutoMaxCluster) {
+    const int G2 = 2 * G;
+    if (stride / G2 < kMinClusterSlice) break;
+    const int fit = max_clusters(kmax, paged, G2, dev);
+    if (fit <= 0 || B > fit) break;
+    G = G2;
+  }
   return G;
 }
 
@@ -131,10 +148,11 @@ topk_status launch_short(const void* scores, bool bf16, int64_t stride, const in
   return tki::launch_short_k2048(p, bf16, dev, info->sm_count, stream);
 }
 
-topk_status select_impl(const void* scores, bool bf16, int64_t stride, const int32_t* lengths,
-                        int32_t B, int32_t k, const int32_t* page_table, int64_t pt_stride,
-                        int32_t page_size, int32_t* out, void* workspace, size_t workspace_bytes,
-                        const topk_debug_opts* opts, cudaStream_t stream) {
+// Argument checks of every selection entry point; they read no device state,
+// and nothing is enqueued when one fails. TOPK_OK with B == 0 means a no-op.
+topk_status check_select_args(const void* scores, bool bf16, int64_t stride, const int32_t* lengths,
+                              int32_t B, int32_t k, const int32_t* page_table, int64_t pt_stride,
+                              int32_t page_size, const int32_t* out) {
   if (B < 0 || stride < 1 || stride > INT32_MAX) return TOPK_EINVAL;
   if (k < 1 || k > TOPK_MAX_K) return TOPK_EUNSUPPORTED_K;
   if (B == 0) return TOPK_OK;
@@ -146,6 +164,16 @@ topk_status select_impl(const void* scores, bool bf16, int64_t stride, const int
     if (page_size < 1 || pt_stride < 1 || !aligned4(page_table)) return TOPK_EINVAL;
     if (pt_stride < (stride + page_size - 1) / page_size) return TOPK_EINVAL;
   }
+  return TOPK_OK;
+}
+
+topk_status select_impl(const void* scores, bool bf16, int64_t stride, const int32_t* lengths,
+                        int32_t B, int32_t k, const int32_t* page_table, int64_t pt_stride,
+                        int32_t page_size, int32_t* out, void* workspace, size_t workspace_bytes,
+                        const topk_debug_opts* opts, cudaStream_t stream) {
+  const topk_status args =
+      check_select_args(scores, bf16, stride, lengths, B, k, page_table, pt_stride, page_size, out);
+  if (args != TOPK_OK || B == 0) return args;
 
   const int kmax = k <= 512 ? 512 : (k <= 1024 ? 1024 : 2048);
   const int cap_max = kmax == 512    ? tki::StashCap<512>::value
@@ -185,7 +213,7 @@ topk_status select_impl(const void* scores, bool bf16, int64_t stride, const int
     if (opts->sample_z != 0.0f) p.sample_z = opts->sample_z;
     if (opts->cluster_size != 0) {
       const int g = opts->cluster_size;
-      if (g != 1 && g != 2 && g != 4 && g != 8) return TOPK_EINVAL;
+      if (g != 1 && g != 2 && g != 4 && g != 8 && g != 16) return TOPK_EINVAL;
       G = g;
     }
     if (opts->counters != nullptr && !aligned4(opts->counters)) return TOPK_EINVAL;
@@ -235,7 +263,7 @@ topk_status select_impl(const void* scores, bool bf16, int64_t stride, const int
   const topk_status st = device_info(&dev, &info);
   if (st != TOPK_OK) return st;
   if (split_rows > 0) G = 1;
-  if (G == 0) G = auto_cluster_size(B, stride, info->sm_count);
+  if (G == 0) G = auto_cluster_size(B, stride, kmax, page_table != nullptr, dev);
   if (static_cast<int64_t>(B) * G > INT32_MAX) return TOPK_EINVAL;
 
   // Split rows: the last m rows each run as two independent CTAs.
@@ -289,13 +317,14 @@ StaticWs g_static_ws_state[kMaxDevices];
 
 // Device address of g_static_ws on device `dev` (current). In host code the
 // array's name only stands in for it, so the address is looked up once per
-// device; the arrival counters are cleared then, and every call that
-// completes leaves them clear again.
-topk_status static_workspace(int dev, void** ptr) {
+// device. The array is zero when the module loads; the first call also
+// enqueues a clear of the arrival counters on its own stream, ahead of its
+// kernel, and every call that completes leaves them clear again.
+topk_status static_workspace(int dev, cudaStream_t stream, void** ptr) {
   StaticWs& st = g_static_ws_state[dev];
   std::call_once(st.once, [&]() {
     st.err = cudaGetSymbolAddress(&st.ptr, g_static_ws);
-    if (st.err == cudaSuccess) st.err = cudaMemset(st.ptr, 0, kWsCounterBytes);
+    if (st.err == cudaSuccess) st.err = cudaMemsetAsync(st.ptr, 0, kWsCounterBytes, stream);
   });
   if (st.err != cudaSuccess) return TOPK_ECUDA;
   *ptr = st.ptr;
@@ -374,19 +403,25 @@ topk_status topk_select_noalloc(const float* scores, int64_t stride, const int32
                                 int64_t pt_stride, int32_t page_size, int32_t* out,
                                 topk_stream_t stream) {
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  if (B <= 0 || stride < 1 || k < 1 || k > TOPK_MAX_K)  // the plain checks decide these cases
-    return select_impl(scores, false, stride, lengths, B, k, page_table, pt_stride, page_size, out,
-                       nullptr, 0, nullptr, cs);
+  // Invalid arguments are reported as by topk_ragged / topk_paged, before the
+  // scratch is sized.
+  if (page_table != nullptr && (page_size < 1 || pt_stride < 1)) return TOPK_EINVAL;
+  const topk_status args =
+      check_select_args(scores, false, stride, lengths, B, k, page_table, pt_stride, page_size, out);
+  if (args != TOPK_OK || B == 0) return args;
   int dev = 0;
   DeviceInfo* info = nullptr;
   topk_status st = device_info(&dev, &info);
   if (st != TOPK_OK) return st;
   // The scratch this call would use, against the fixed array.
-  const int G = auto_cluster_size(B, stride, info->sm_count);
+  // (the same policy as the call it makes: rows of at most kShortMaxRow scores
+  // take the short-row kernel, which splits nothing)
+  const int kmax = k <= 512 ? 512 : (k <= 1024 ? 1024 : 2048);
+  const int G = stride <= tki::kShortMaxRow ? 0 : auto_cluster_size(B, stride, kmax, page_table != nullptr, dev);
   const int m = G == 1 ? auto_split_rows(B, stride, info->sm_count) : 0;
   if (ws_bytes_for(k, m) > kStaticWsBytes) return TOPK_ESCRATCH;
   void* ws = nullptr;
-  st = static_workspace(dev, &ws);
+  st = static_workspace(dev, cs, &ws);
   if (st != TOPK_OK) return st;
   return select_impl(scores, false, stride, lengths, B, k, page_table, pt_stride, page_size, out, ws,
                      kStaticWsBytes, nullptr, cs);

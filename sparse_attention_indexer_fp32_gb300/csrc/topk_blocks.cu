@@ -3,7 +3,7 @@
 // `sort_candidate_blocks` docstrings of candidate_table.py):
 //
 //  * topk_amax8_varlen: level-one keys, the maximum of every block of 8
-//    consecutive scores, the newest block forced to +inf. A pure stream:
+//    consecutive scores (+0 above -0), the newest block forced to +inf. A pure stream:
 //    each thread reads two blocks (2 x 32 bytes), consecutive threads
 //    consecutive blocks, and writes their maxima.
 //  * topk_sort_candidate_blocks: the selected block ids of a row rewritten
@@ -35,6 +35,18 @@ struct AmaxParams {
   int32_t chunks;  // CTAs per row
 };
 
+// Block keys are maxima in the selection's own total order (+0 above -0), so
+// the key of a block does not depend on the order of its scores; fmaxf,
+// which the page names, leaves the sign of a zero maximum open. The maximum
+// is taken over the order-preserving keys and turned back into the float.
+__device__ __forceinline__ float key_float(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key ^ 0x80000000u) : ~key);
+}
+
+__device__ __forceinline__ uint32_t max_key4(float4 a) {
+  return max(max(order_key(a.x), order_key(a.y)), max(order_key(a.z), order_key(a.w)));
+}
+
 __global__ void __launch_bounds__(kThreads) amax8_kernel(const AmaxParams p) {
   const int row = static_cast<int>(blockIdx.x / static_cast<unsigned>(p.chunks));
   const int chunk = static_cast<int>(blockIdx.x % static_cast<unsigned>(p.chunks));
@@ -55,11 +67,12 @@ __global__ void __launch_bounds__(kThreads) amax8_kernel(const AmaxParams p) {
     } else if (vec) {
       const float4 a = __ldcs(reinterpret_cast<const float4*>(rp + 8 * i));
       const float4 b = __ldcs(reinterpret_cast<const float4*>(rp + 8 * i) + 1);
-      m = fmaxf(fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w)), fmaxf(fmaxf(b.x, b.y), fmaxf(b.z, b.w)));
+      m = key_float(max(max_key4(a), max_key4(b)));
     } else {
-      m = __ldcs(rp + 8 * i);
+      uint32_t km = order_key(__ldcs(rp + 8 * i));
 #pragma unroll
-      for (int j = 1; j < 8; ++j) m = fmaxf(m, __ldcs(rp + 8 * i + j));
+      for (int j = 1; j < 8; ++j) km = max(km, order_key(__ldcs(rp + 8 * i + j)));
+      m = key_float(km);
     }
     op[i] = m;
   }

@@ -5,4 +5,5 @@ namespace tki {
 topk_status launch_k1024_paged(const Params& p, int G, int dev, cudaStream_t stream) {
   return launch_cluster<1024, true>(p, G, dev, stream);
 }
+int clusters_k1024_paged(int G, int dev) { return max_active_clusters<1024, true>(G, dev); }
 }  // namespace tki

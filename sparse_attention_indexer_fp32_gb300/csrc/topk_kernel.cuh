@@ -956,6 +956,14 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
     return;
   }
 
+  if constexpr (G == 1) {
+    if (abort) {  // uniform: nothing is selected from an incomplete stash, and
+      drain();    // the poison is the only store this CTA makes to its row
+      poison_row();
+      return;
+    }
+  }
+
   // ---- exact cutoff over the stash(es) and emission --------------------------
   if (PAGED && !abort) {
     // The emission maps every selected index through the page table: start
@@ -1008,8 +1016,8 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
     if (compactions) atomicAdd(&p.counters[kCntCompactions], compactions);
     if (rank == 0 && sampled) atomicAdd(&p.counters[kCntSampled], 1u);
   }
-  if (abort) {
-    drain();
+  if (abort) {  // a cluster CTA: the cluster barrier above orders every
+    drain();    // emission store of the cluster before the poison
     poison_row();
   }
 }

@@ -20,19 +20,65 @@ std::atomic<uint64_t>& attr_flags() {
   return flags;
 }
 
+// Sets the variant's kernel attributes on device `dev` (current), once:
+// its shared memory, and for clusters of 16 the non-portable cluster size.
+template <int KMAX, int G, bool PAGED>
+topk_status prepare_variant(int dev) {
+  constexpr int C = StashCap<KMAX>::value;
+  auto kernel = topk_rows_kernel<KMAX, G, PAGED>;
+  const uint64_t bit = 1ull << dev;
+  std::atomic<uint64_t>& flags = attr_flags<KMAX, G, PAGED>();
+  if ((flags.load(std::memory_order_acquire) & bit) == 0) {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(sizeof(Smem<C>))) != cudaSuccess)
+      return TOPK_ECUDA;
+    if (G > 8 && cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+                     cudaSuccess)
+      return TOPK_ECUDA;
+    flags.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  return TOPK_OK;
+}
+
+// Clusters of G CTAs of this variant that can be resident at once on device
+// `dev`, as the driver answers it (cudaOccupancyMaxActiveClusters): a
+// cluster's CTAs must share one GPC, so this can fall short of the SM count
+// times the CTAs per SM, divided by G. Found once per device; 0 when none fit
+// or the query fails.
+template <int KMAX, int G, bool PAGED>
+int max_active_clusters_variant(int dev) {
+  static std::atomic<int> known[64];  // answer + 1; 0 = not asked yet
+  const int seen = known[dev].load(std::memory_order_relaxed);
+  if (seen > 0) return seen - 1;
+  int n = 0;
+  if (prepare_variant<KMAX, G, PAGED>(dev) == TOPK_OK) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(G, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = sizeof(Smem<StashCap<KMAX>::value>);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = G;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, topk_rows_kernel<KMAX, G, PAGED>, &cfg) != cudaSuccess) {
+      (void)cudaGetLastError();  // the query's failure is not a launch error
+      n = 0;
+    }
+  }
+  known[dev].store(n + 1, std::memory_order_relaxed);
+  return n;
+}
+
 template <int KMAX, int G, bool PAGED>
 topk_status launch_variant(const Params& p, int dev, cudaStream_t stream) {
   constexpr int C = StashCap<KMAX>::value;
   auto kernel = topk_rows_kernel<KMAX, G, PAGED>;
   const size_t smem = sizeof(Smem<C>);
-  const uint64_t bit = 1ull << dev;
-  std::atomic<uint64_t>& flags = attr_flags<KMAX, G, PAGED>();
-  if ((flags.load(std::memory_order_acquire) & bit) == 0) {
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-      return TOPK_ECUDA;
-    flags.fetch_or(bit, std::memory_order_acq_rel);
-  }
+  const topk_status prep = prepare_variant<KMAX, G, PAGED>(dev);
+  if (prep != TOPK_OK) return prep;
   cudaLaunchConfig_t cfg = {};
   // G CTAs per row, or one per row plus one more per split row.
   const unsigned grid = G > 1 ? static_cast<unsigned>(p.B) * G
@@ -60,7 +106,19 @@ topk_status launch_cluster(const Params& p, int G, int dev, cudaStream_t stream)
     case 2: return launch_variant<KMAX, 2, PAGED>(p, dev, stream);
     case 4: return launch_variant<KMAX, 4, PAGED>(p, dev, stream);
     case 8: return launch_variant<KMAX, 8, PAGED>(p, dev, stream);
+    case 16: return launch_variant<KMAX, 16, PAGED>(p, dev, stream);
     default: return TOPK_EINVAL;
+  }
+}
+
+template <int KMAX, bool PAGED>
+int max_active_clusters(int G, int dev) {
+  switch (G) {
+    case 2: return max_active_clusters_variant<KMAX, 2, PAGED>(dev);
+    case 4: return max_active_clusters_variant<KMAX, 4, PAGED>(dev);
+    case 8: return max_active_clusters_variant<KMAX, 8, PAGED>(dev);
+    case 16: return max_active_clusters_variant<KMAX, 16, PAGED>(dev);
+    default: return 0;
   }
 }
 
@@ -121,5 +179,12 @@ topk_status launch_k1024_ragged(const Params& p, int G, int dev, cudaStream_t st
 topk_status launch_k1024_paged(const Params& p, int G, int dev, cudaStream_t stream);
 topk_status launch_k2048_ragged(const Params& p, int G, int dev, cudaStream_t stream);
 topk_status launch_k2048_paged(const Params& p, int G, int dev, cudaStream_t stream);
+// Resident clusters of G CTAs (see max_active_clusters_variant), same units.
+int clusters_k512_ragged(int G, int dev);
+int clusters_k512_paged(int G, int dev);
+int clusters_k1024_ragged(int G, int dev);
+int clusters_k1024_paged(int G, int dev);
+int clusters_k2048_ragged(int G, int dev);
+int clusters_k2048_paged(int G, int dev);
 
 }  // namespace tki

@@ -241,7 +241,9 @@ def golden_cases():
 
 def pin_golden(orc) -> None:
     for name, doc in golden_cases():
-        if "cases" in doc:
+        if "amax8_cases" in doc:
+            pin_golden_amax8(orc, name, doc["amax8_cases"])
+        elif "cases" in doc:
             for case in doc["cases"]:
                 got = _run(orc, case["scores"], case["lengths"], case["k"])
                 assert got.tolist() == case["expected"], (name, case, got.tolist())
@@ -251,6 +253,23 @@ def pin_golden(orc) -> None:
             assert got.tolist() == doc["expected_ragged"], (name, got.tolist())
             got = _run(orc, scores, doc["lengths"], doc["k"], doc["page_table"], doc["page_size"])
             assert got.tolist() == doc["expected_paged"], (name, got.tolist())
+
+
+def _golden_floats(rows, fill):
+    """JSON rows of numbers and the strings "inf", "-inf", "sentinel" as float32."""
+    conv = {"inf": np.inf, "-inf": -np.inf, "sentinel": fill}
+    return np.array([[conv.get(v, v) if isinstance(v, str) else v for v in r] for r in rows],
+                    dtype=np.float32)
+
+
+def pin_golden_amax8(orc, name, cases) -> None:
+    """Block keys compared bit for bit (a float compare would take -0 for +0)."""
+    for case in cases:
+        scores = _golden_floats(case["scores"], np.nan)
+        want = _golden_floats(case["expected"], SENTINEL)
+        init = np.full(want.shape, SENTINEL, dtype=np.float32)
+        got = orc.amax8_varlen(scores, np.array(case["lengths"], np.int32), case["topk"], init)
+        assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), (name, got.tolist())
 
 
 def page_map_reference(ragged_out, page_table, page_size):

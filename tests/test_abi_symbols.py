@@ -143,7 +143,7 @@ def test_debug_option_checks_need_no_gpu(lib):
     bad = [
         dict(sample_mode=-1), dict(sample_mode=3),
         dict(stash_capacity=512 + 2047), dict(stash_capacity=512 + 4096 + 1),  # [k + 2048, default]
-        dict(cluster_size=3), dict(cluster_size=16), dict(cluster_size=-1),
+        dict(cluster_size=3), dict(cluster_size=32), dict(cluster_size=-1),
         dict(counters=0x1002),  # misaligned
         dict(probe_stage=-1), dict(probe_stage=1, probe_wait_us=0),
         dict(probe_stage=1, probe_wait_us=5000001),
@@ -166,8 +166,9 @@ def test_debug_option_checks_need_no_gpu(lib):
 
 
 def test_noalloc_checks_need_no_gpu(lib):
-    """B <= 0 and k out of range are decided before the call looks at the
-    device (the other argument checks follow its device query)."""
+    """Every argument check of the allocation-free call runs before it looks
+    at the device or sizes its scratch: an invalid call gets the same code as
+    from topk_ragged / topk_paged, never TOPK_ESCRATCH."""
     some = ctypes.c_void_p(0x1000)
     assert lib.topk_select_noalloc(some, 64, some, 0, 512, None, 0, 0, some, None) == tk.Status.OK
     assert lib.topk_select_noalloc(some, 64, some, 2, 0, None, 0, 0, some, None) == \
@@ -178,4 +179,22 @@ def test_noalloc_checks_need_no_gpu(lib):
         tk.Status.EINVAL
     assert lib.topk_select_noalloc(some, 0, some, 2, 512, None, 0, 0, some, None) == \
         tk.Status.EINVAL
+    # a call big enough to need more scratch than the array holds (153 rows
+    # of 196608 at k = 2048), with one argument broken at a time
+    big = dict(scores=some, stride=196608, lengths=some, B=153, k=2048, pt=None, pt_stride=0,
+               page_size=0, out=some)
+
+    def noalloc(**kw):
+        a = dict(big, **kw)
+        return lib.topk_select_noalloc(a["scores"], a["stride"], a["lengths"], a["B"], a["k"],
+                                       a["pt"], a["pt_stride"], a["page_size"], a["out"], None)
+
+    assert noalloc(scores=None) == tk.Status.EINVAL
+    assert noalloc(lengths=None) == tk.Status.EINVAL
+    assert noalloc(out=None) == tk.Status.EINVAL
+    assert noalloc(scores=ctypes.c_void_p(0x1002)) == tk.Status.EINVAL  # misaligned
+    assert noalloc(stride=2 ** 31) == tk.Status.EINVAL
+    assert noalloc(pt=some, pt_stride=3071, page_size=64) == tk.Status.EINVAL  # table too narrow
+    assert noalloc(pt=some, pt_stride=3072, page_size=0) == tk.Status.EINVAL
+    assert noalloc(pt=ctypes.c_void_p(0x1001), pt_stride=3072, page_size=64) == tk.Status.EINVAL
     assert b"scratch" in lib.topk_status_string(tk.Status.ESCRATCH)

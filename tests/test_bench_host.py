@@ -39,7 +39,7 @@ def test_two_level_rooflines():
     for stage in res.values():
         r = stage["roofline"]
         assert r["achieved"] == pytest.approx(r["algorithmic_bytes_per_launch"] / 10e-6 / 1e9)
-    assert "copy" in res["sort_candidate_blocks"]["note"]
+    assert "kernel alone" in res["sort_candidate_blocks"]["note"]
 
 
 def test_dram_counters_follow_their_kernels_sources(tmp_path, monkeypatch):
@@ -72,3 +72,51 @@ def test_dram_counters_follow_their_kernels_sources(tmp_path, monkeypatch):
     assert bench.kernel_source_hash("topk_short_kernel") != h_short
     assert bench.kernel_source_hash("topk_rows_kernel") == h_rows  # not one of its sources
     assert bench.profiled_traffic("a") == 5.0
+
+
+def test_reference_arm_prints_the_gpu_arms_config(capsys):
+    """The reference arm (the host oracle) reports on the same workload
+    config, metric and unit as the GPU arm, with dtype f32."""
+    from synth import CONFIGS
+
+    bench.main(["--impl", "reference", "--steps", "3", "--warmup", "3"])
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["dtype"] == "f32"
+    assert line["metric"] == bench.METRIC and line["unit"] == bench.UNIT
+    want = dict(bench.workload_config(CONFIGS[bench.WORKLOADS["w262144_k512_paged"]]),
+                parallelism="replicas x1")
+    assert line["config"] == want
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_summary_lists_every_timed_workload_last():
+    roof = bench.hbm_roofline(10**9, 200.0)
+    line = {"config": {"workload": "A"}, "value": 200.0, "roofline": roof,
+            "also": [{"workload": "B", "us_per_call": 100.0, "roofline": roof}],
+            "prefill": [{"workload": "C", "us_per_call": 50.0, "roofline": roof}],
+            "two_level": {"workload": "A", "stages": {"amax8_varlen": {"us_per_call": 1.0,
+                                                                       "roofline": roof}}},
+            "latency": {"workload": "L", "eager_us_per_call": 9.0, "graph_replay_us_per_call": 8.0,
+                        "cold_l2_eager_us_per_call": 12.0,
+                        "cold_l2_graph_replay_us_per_call": 11.0}}
+    summ = bench.summary_of(line)
+    assert [e["w"] for e in summ] == ["A", "B", "C", "amax8_varlen_A", "L"]
+    assert summ[1]["us"] == 100.0 and summ[1]["frac"] == round(roof["frac"], 3)
+    assert len(json.dumps(summ)) < 1500
+
+
+def test_sweep_paths_and_summary_tables():
+    """The dispatch sweep's path list per shape, and its markdown summary on
+    a made-up measurement."""
+    names = [n for n, _ in bench.sweep_paths(8192, 64, 152)]
+    assert names[:3] == ["auto", "short", "short_regs"] and "G2_sampled" in names
+    assert "G4_full" not in names  # 8192 / 4 < one stage
+    names = [n for n, _ in bench.sweep_paths(262144, 1024, 152)]
+    assert "G16_sampled" in names and "G1_split112" in names and "G1_split_all" not in names
+    assert bench._sweep_split_rows(1024, 152) == 112
+    paths = {n: 10.0 + i for i, (n, _) in enumerate(bench.sweep_paths(262144, 4, 152))}
+    doc = {"gpu": "test", "sm_count": 152, "reps": 20, "warmup": 3, "command": "cmd",
+           "results": [{"width": 262144, "B": 4, "lengths": "ragged", "k": 512, "paths": paths,
+                        "algorithmic_bytes": 10 ** 6, "auto_counters": {}}]}
+    md = bench.sweep_markdown(doc)
+    assert "| 512 | 262144 | 4 | 10.0 |" in md and "G1_split4" in md

@@ -31,6 +31,10 @@ def test_amax8_matches_the_oracle(stride, topk):
     B = 24
     scores = rng.standard_normal((B, stride)).astype(np.float32)
     scores[2] = -np.inf
+    # blocks whose maximum is a zero of either sign, in either order
+    zeros = rng.choice([-0.0, 0.0, -1.0, -np.inf], size=(4, stride), p=[0.4, 0.1, 0.4, 0.1])
+    scores[10:14] = zeros.astype(np.float32)
+    scores[10, :16] = [-0.0, 0.0, -1, -1, -1, -1, -1, -1, 0.0, -0.0, -1, -1, -1, -1, -1, -1]
     lengths = np.array([0, 1, 7, 8, 9, 24, 25, stride, stride + 3, -1]
                        + list(rng.integers(0, stride, B - 10)), dtype=np.int32)
     width = -(-stride // 8)
@@ -39,7 +43,11 @@ def test_amax8_matches_the_oracle(stride, topk):
     tk.amax8_varlen(to_dev(scores), to_dev(lengths), topk, out=out)
     torch.cuda.synchronize()
     want = oracle.amax8_varlen(scores, lengths, topk, init)
-    assert np.array_equal(out.cpu().numpy(), want)
+    got = out.cpu().numpy()
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), "keys differ (bit for bit)"
+    if topk == 0:  # the case does hold zero maxima of both signs
+        z = want[10:14].view(np.uint32)
+        assert (z == 0).any() and (z == 0x80000000).any()
 
 
 @pytest.mark.parametrize("page_size", [8, 64])

@@ -69,14 +69,14 @@ def _mixed_rows():
 
 @pytest.mark.parametrize("k", [512, 1024, 2048])
 @pytest.mark.parametrize("sample_mode", [1, 2])
-@pytest.mark.parametrize("cluster", [1, 2, 4, 8])
+@pytest.mark.parametrize("cluster", [1, 2, 4, 8, 16])
 def test_forced_paths(k, sample_mode, cluster):
     scores, lengths = _mixed_rows()
     check_against_oracle(scores, lengths, k, sample_mode=sample_mode, cluster_size=cluster)
 
 
 @pytest.mark.parametrize("k", [512, 1024, 2048])
-@pytest.mark.parametrize("cluster", [1, 4])
+@pytest.mark.parametrize("cluster", [1, 4, 16])
 def test_compaction_path(k, cluster):
     """Smallest candidate buffer (k + 2048 entries): the in-buffer compaction
     runs many times, and on the ascending rows the hits of one group exceed
@@ -89,7 +89,7 @@ def test_compaction_path(k, cluster):
     assert int(cnt[tk.Counter.COMPACTIONS]) > 0
 
 
-@pytest.mark.parametrize("cluster", [1, 2, 8])
+@pytest.mark.parametrize("cluster", [1, 2, 8, 16])
 def test_underflow_rescan_path(cluster):
     """A sampled cutoff set far too high keeps fewer than k candidates: every
     sampled row must be rescanned and still come out exact."""
@@ -344,18 +344,25 @@ def test_deterministic_over_100_calls(config):
     torch.cuda.synchronize()
 
 
+@pytest.mark.parametrize("k", [512, 1024, 2048])
 @pytest.mark.parametrize("cluster", [1, 2])
-def test_wait_limit_reports_device_error(cluster):
+def test_wait_limit_reports_device_error(cluster, k):
     """A wait that runs out (on a barrier nothing completes) is reported: the
-    rows carry TOPK_DEVICE_ERROR_INDEX, the error is counted, the call
-    returns, and the context keeps working."""
+    rows carry TOPK_DEVICE_ERROR_INDEX in every slot, the error is counted,
+    the call returns, and the context keeps working. The output starts out
+    holding a third value, so a slot written by a selection after (or
+    instead of) the failure mark would show."""
     w = make_workload(3, B=4)
+    s, l = to_dev(w.scores), to_dev(w.lengths)
     cnt = counters_tensor()
-    out = run_gpu(w.scores, w.lengths, w.k, cluster_size=cluster, counters=cnt,
-                  probe_stage=2, probe_wait_us=2000)
-    assert np.all(out == tk.DEVICE_ERROR_INDEX)
+    out = torch.full((w.B, k), 0x1234567, dtype=torch.int32, device="cuda:0")
+    tk.topk_select_ex(s, l, k, out=out, cluster_size=cluster, counters=cnt,
+                      probe_stage=2, probe_wait_us=2000)
+    torch.cuda.synchronize()
+    assert torch.all(out == tk.DEVICE_ERROR_INDEX), "a slot of a failed row holds something else"
     assert int(cnt[tk.Counter.DEVICE_ERRORS]) == 4 * cluster
-    check_against_oracle(w.scores, w.lengths, w.k, cluster_size=cluster)
+    assert int(cnt[tk.Counter.SPLIT_ROWS]) == 0
+    check_against_oracle(w.scores, w.lengths, k, cluster_size=cluster)
 
 
 def test_capture_before_the_streams_first_call_runs_unsplit():

@@ -40,6 +40,8 @@ MUTANTS = {
     # block key misses the last score of each block
     "amax_block_short": ("for (int64_t j = 8 * i; j < 8 * i + 8; ++j) {",
                          "for (int64_t j = 8 * i; j < 8 * i + 7; ++j) {"),
+    # block key keeps the first of two equal-comparing scores (-0 / +0 order-dependent)
+    "amax_first_of_equals": ("if (ranks_above(row[j], m)) m = row[j];", "if (row[j] > m) m = row[j];"),
     # newest block not forced to +inf
     "amax_no_inf": ("out_row[nb - 1] = INFINITY;", "out_row[nb - 1] = row[8 * (nb - 1)];"),
     # rows with exactly topk blocks not skipped
