@@ -598,6 +598,34 @@ def sweep_paths(width: int, B: int, sm_count: int):
     return paths
 
 
+SWEEP_REPS = 20
+
+
+def _graph_time_us(fn, stream, start, end) -> float:
+    """Device time per call of `fn`: SWEEP_REPS calls captured in one CUDA
+    graph (so that the host's launch cost is not timed), replayed once to warm
+    up, then twice under CUDA events."""
+    import torch
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            fn()
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for _ in range(SWEEP_REPS):
+                fn()
+        graph.replay()
+        start.record()
+        graph.replay()
+        graph.replay()
+        end.record()
+        end.synchronize()
+    us = 1000.0 * start.elapsed_time(end) / (2 * SWEEP_REPS)
+    del graph
+    return us
+
+
 def run_sweep(args):
     """Times every path of the library on N(0,1) rows over batch x width x k,
     with full and 80-100 % ragged lengths; writes the measurements (JSON) and
@@ -615,6 +643,7 @@ def run_sweep(args):
     ws = torch.zeros(tk.workspace_bytes(2048, 1024), dtype=torch.uint8, device=dev)
     cnt = torch.zeros(tk.NUM_COUNTERS, dtype=torch.int32, device=dev)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    stream = torch.cuda.Stream(dev)
     results = []
     t0 = time.time()
     for width in SWEEP_WIDTHS:
@@ -633,22 +662,11 @@ def run_sweep(args):
                     out = torch.empty((B, k), dtype=torch.int32, device=dev)
                     rec = {"width": width, "B": B, "lengths": lmode, "k": k, "paths": {}}
                     for name, opts in sweep_paths(width, B, sms):
-                        if name == "auto":
-                            fn = lambda: tk.topk_ragged(scores, lengths, k, out=out)  # noqa: E731
-                        else:
-                            o = dict(opts)
-                            if "split_rows" in o:
-                                o["workspace"] = ws
-                            fn = lambda o=o: tk.topk_select_ex(scores, lengths, k, out=out, **o)  # noqa: E731
-                        for _ in range(3):
-                            fn()
-                        reps = 20
-                        start.record()
-                        for _ in range(reps):
-                            fn()
-                        end.record()
-                        end.synchronize()
-                        rec["paths"][name] = 1000.0 * start.elapsed_time(end) / reps
+                        o = dict(opts)
+                        if name == "auto" or "split_rows" in o:
+                            o["workspace"] = ws  # the automatic policy with a workspace
+                        fn = lambda o=o: tk.topk_select_ex(scores, lengths, k, out=out, **o)  # noqa: E731
+                        rec["paths"][name] = _graph_time_us(fn, stream, start, end)
                     # what the automatic policy did, from the device counters
                     cnt.zero_()
                     tk.topk_select_ex(scores, lengths, k, out=out, counters=cnt,
@@ -660,8 +678,11 @@ def run_sweep(args):
                                             "sampled": c[tk.Counter.SAMPLED]}
                     rec["algorithmic_bytes"] = n * 4 + B * k * 4
                     results.append(rec)
+    clusters = {f"k{k}_G{g}": tk.max_active_clusters(k, False, g) for k in SWEEP_KS
+                for g in (2, 4, 8, 16)}
     doc = {"sm_count": sms, "gpu": torch.cuda.get_device_name(dev), "seconds": time.time() - t0,
-           "reps": 20, "warmup": 3, "command": "python bench.py --sweep --sweep-out DIR",
+           "max_active_clusters": clusters,
+           "reps": SWEEP_REPS, "warmup": 3, "command": "python bench.py --sweep --sweep-out DIR",
            "results": results}
     os.makedirs(args.sweep_out, exist_ok=True)
     with open(os.path.join(args.sweep_out, "dispatch_sweep.json"), "w") as f:
@@ -680,9 +701,13 @@ def sweep_markdown(doc: dict) -> str:
              "",
              f"GPU: {doc['gpu']} ({doc['sm_count']} SMs). Command: `{doc['command']}`. N(0,1) rows "
              f"(seeded torch generator on the device), lengths full or uniform in [0.8w, w]; each "
-             f"path {doc['warmup']} warm-up calls then {doc['reps']} timed back-to-back (CUDA "
-             f"events; small shapes stay in L2). Times in us per call. `frac` = algorithmic bytes / "
-             f"time / {peak:.0f} GB/s.",
+             f"path: {doc['warmup']} warm-up calls, then {doc['reps']} calls captured in one CUDA "
+             f"graph, replayed once untimed and twice under CUDA events (device time, no host "
+             f"launch cost; small shapes stay in L2). Times in us per call. `frac` = algorithmic "
+             f"bytes / time / {peak:.0f} GB/s.",
+             "",
+             "Clusters resident at once (the driver's answer, ragged kernel): " +
+             ", ".join(f"{n} {v}" for n, v in doc.get("max_active_clusters", {}).items()) + ".",
              ""]
     lines += ["## Automatic policy against the best forced path (ragged lengths)", "",
               "| k | width | B | auto us | frac | best path | best us | auto/best |",

@@ -244,6 +244,21 @@ topk_status topk_select_noalloc(const float* scores, int64_t stride, const int32
                                 int64_t pt_stride, int32_t page_size, int32_t* out,
                                 topk_stream_t stream);
 
+/*
+ * topk_max_active_clusters - diagnostic: writes to *clusters how many
+ * thread-block clusters of cluster_size (2, 4, 8 or 16) CTAs of the streaming
+ * kernel for this k (ragged output when paged == 0, paged otherwise) can be
+ * resident at once on the current device, as the driver answers it
+ * (cudaOccupancyMaxActiveClusters; the CTAs of a cluster must share one GPC,
+ * so this can be less than the SM count times the CTAs per SM, divided by
+ * the cluster size). The automatic policy gives a row a cluster only while
+ * the clusters of every row fit at once. Errors: TOPK_EUNSUPPORTED_K,
+ * TOPK_EINVAL (clusters NULL or another cluster size), TOPK_ECUDA,
+ * TOPK_EDEVICE.
+ */
+topk_status topk_max_active_clusters(int32_t k, int32_t paged, int32_t cluster_size,
+                                     int32_t* clusters);
+
 /* Static, human-readable description of a status code. */
 const char* topk_status_string(topk_status status);
 

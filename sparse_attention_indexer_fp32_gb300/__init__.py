@@ -10,7 +10,8 @@ CUDA kernels (``_build/libtopk_indexer.so``):
   at most 16384);
 * :func:`amax8_varlen`, :func:`sort_candidate_blocks` - the two-level
   indexer's block-max keys and sorted candidate block table;
-* :func:`topk_select_ex` - diagnostics: a forced internal path, path counters.
+* :func:`topk_select_ex` - diagnostics: a forced internal path, path counters;
+  :func:`max_active_clusters` - the driver's cluster residency per size.
 
 PyTorch only provides device memory and streams.
 """
@@ -25,6 +26,7 @@ from ._binding import (  # noqa: F401
     TopkError,
     amax8_varlen,
     load_library,
+    max_active_clusters,
     raw_library,
     sort_candidate_blocks,
     topk_paged,
@@ -35,7 +37,7 @@ from ._binding import (  # noqa: F401
 )
 
 __all__ = ["topk_ragged", "topk_paged", "topk_select_ex", "topk_select_bf16", "workspace_bytes",
-           "amax8_varlen", "sort_candidate_blocks", "TopkError",
+           "amax8_varlen", "sort_candidate_blocks", "max_active_clusters", "TopkError",
            "Status", "Counter",
            "load_library", "raw_library", "LIB_PATH", "TOPK_MAX_K", "NUM_COUNTERS",
            "DEVICE_ERROR_INDEX"]

@@ -104,6 +104,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.topk_amax8_varlen.restype = ctypes.c_int
         lib.topk_sort_candidate_blocks.argtypes = [vp, i32, i32, vp, i64, vp, i64, i32, vp, vp]
         lib.topk_sort_candidate_blocks.restype = ctypes.c_int
+        lib.topk_max_active_clusters.argtypes = [i32, i32, i32, ctypes.POINTER(i32)]
+        lib.topk_max_active_clusters.restype = ctypes.c_int
         lib.topk_status_string.argtypes = [ctypes.c_int]
         lib.topk_status_string.restype = ctypes.c_char_p
         lib.topk_abi_version.restype = ctypes.c_int32
@@ -345,6 +347,16 @@ def sort_candidate_blocks(blocks: torch.Tensor, lengths: torch.Tensor, stride: i
                                               out_pages.data_ptr(),
                                               _stream_handle(blocks.device, stream)))
     return out_pages
+
+
+def max_active_clusters(k: int, paged: bool, cluster_size: int) -> int:
+    """Clusters of ``cluster_size`` CTAs of the streaming kernel (this k
+    bucket and output kind) resident at once on the current device, as the
+    driver answers it."""
+    out = ctypes.c_int32(0)
+    _check(load_library().topk_max_active_clusters(int(k), int(bool(paged)), int(cluster_size),
+                                                   ctypes.byref(out)))
+    return int(out.value)
 
 
 def raw_library() -> ctypes.CDLL:

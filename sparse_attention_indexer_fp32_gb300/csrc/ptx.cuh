@@ -147,6 +147,16 @@ __device__ __forceinline__ uint32_t ld_dsmem_u32(uint32_t addr) {
   return v;
 }
 
+__device__ __forceinline__ void st_dsmem_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Relaxed atomic add, no value returned, to a shared-memory word of a CTA of
+// this cluster (ordered for other CTAs by the next cluster barrier).
+__device__ __forceinline__ void red_dsmem_add(uint32_t addr, uint32_t v) {
+  asm volatile("red.relaxed.cluster.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ uint4 ld_dsmem_v4(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"

@@ -427,6 +427,21 @@ topk_status topk_select_noalloc(const float* scores, int64_t stride, const int32
                      kStaticWsBytes, nullptr, cs);
 }
 
+topk_status topk_max_active_clusters(int32_t k, int32_t paged, int32_t cluster_size,
+                                     int32_t* clusters) {
+  if (k < 1 || k > TOPK_MAX_K) return TOPK_EUNSUPPORTED_K;
+  if (clusters == nullptr) return TOPK_EINVAL;
+  if (cluster_size != 2 && cluster_size != 4 && cluster_size != 8 && cluster_size != 16)
+    return TOPK_EINVAL;
+  int dev = 0;
+  DeviceInfo* info = nullptr;
+  const topk_status st = device_info(&dev, &info);
+  if (st != TOPK_OK) return st;
+  const int kmax = k <= 512 ? 512 : (k <= 1024 ? 1024 : 2048);
+  *clusters = max_clusters(kmax, paged != 0, cluster_size, dev);
+  return TOPK_OK;
+}
+
 const char* topk_status_string(topk_status status) {
   switch (status) {
     case TOPK_OK: return "success";

@@ -37,9 +37,10 @@
 //
 // Cluster split (sglang PR 39648 report, 实现拆解 4): for batches too small to
 // fill the GPU, G CTAs of a cluster each stream a contiguous slice of the row
-// with their own stash; histograms are merged over distributed shared memory
-// so every CTA derives the same cutoffs, and per-CTA counts give each CTA its
-// output offsets.
+// with their own stash. Rank 0 owns the row's histograms: the other CTAs add
+// into it over distributed shared memory, rank 0 finds each cutoff bin and
+// sends it to the others (one cluster barrier before and one after), and
+// per-CTA counts give each CTA its output offsets.
 //
 // Split rows (this library's own device, for the last partial wave of a large
 // batch): two independent CTAs stream the halves of a row, each leaves its
@@ -118,6 +119,7 @@ struct __align__(128) Smem {
   uint32_t scan[kWarps];
   uint32_t res[4];
   uint32_t pub[4];                  // values the other CTAs of the cluster read
+  uint32_t off[2];                  // this CTA's emission offsets in a cluster
 };
 
 struct Params {
@@ -202,6 +204,26 @@ __device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t bin) {
   if (bin != 0xffffffffu) atomicAdd(&hist[bin], 1u);
 }
 
+// Where a CTA's histogram increments go. In a cluster (G > 1) rank 0 owns
+// the one histogram of the row: its own increments are local shared atomics,
+// the other CTAs add remotely into it (h0 = its address in the cluster's
+// shared window), and rank 0 alone searches it.
+template <int G>
+struct HistDst {
+  uint32_t h0;
+  bool local;
+};
+
+template <int G>
+__device__ __forceinline__ void hist_inc(uint32_t* hist, HistDst<G> d, uint32_t bin) {
+  if (bin == 0xffffffffu) return;
+  if (G == 1 || d.local) {
+    atomicAdd(&hist[bin], 1u);
+  } else {
+    red_dsmem_add(d.h0 + 4u * bin, 1u);
+  }
+}
+
 // Locates the bin holding the target-th largest element (1 <= target <= total).
 // Thread t owns BPT consecutive bins, given in DESCENDING bin order in c[].
 // Returns the bin; *above = elements in higher bins; *inbin = elements in it.
@@ -231,17 +253,18 @@ __device__ uint32_t find_bin(const uint32_t (&c)[BPT], uint32_t target, SM& S,
   return S.res[0];
 }
 
-// Reads this thread's BPT bins (descending), merged over the cluster when
-// G > 1, zeroes them, and finds the bin of the target-th largest element.
-// Must be called by every thread (of every CTA of the cluster) after the
-// histogram increments.
+// Reads this thread's BPT bins (descending), zeroes them, and finds the bin
+// of the target-th largest element. Must be called by every thread (of every
+// CTA of the cluster) after the histogram increments. In a cluster (G > 1)
+// the histogram is rank 0's (see HistDst): rank 0 searches it and sends the
+// result to the other CTAs, two cluster barriers in all.
 template <int G, int BPT, class SM>
-__device__ uint32_t merged_find(SM& S, uint32_t target, uint32_t* above, uint32_t* inbin) {
+__device__ uint32_t merged_find(SM& S, uint32_t target, uint32_t* above, uint32_t* inbin,
+                                bool rank0 = true) {
   const int lo = (BPT * kThreads) - BPT * (threadIdx.x + 1);  // lowest owned bin
-  uint32_t c[BPT];
-  if constexpr (G == 1) {
-    __syncthreads();
+  auto search_own = [&]() -> uint32_t {
     // Only this thread reads or writes its bins here.
+    uint32_t c[BPT];
     uint4* h4 = reinterpret_cast<uint4*>(&S.hist[lo]);
 #pragma unroll
     for (int q = 0; q < BPT; q += 4) {
@@ -253,29 +276,24 @@ __device__ uint32_t merged_find(SM& S, uint32_t target, uint32_t* above, uint32_
       c[BPT - 4 - q] = v.w;
     }
     return find_bin<BPT>(c, target, S, above, inbin);
+  };
+  if constexpr (G == 1) {
+    __syncthreads();
+    return search_own();
   } else {
-    cluster_sync();  // every CTA's histogram is complete
+    cluster_sync();  // every CTA's increments have reached rank 0's histogram
+    if (rank0) {
+      (void)search_own();  // leaves the result in S.res[0 .. 2]
+      if (threadIdx.x < G - 1) {
 #pragma unroll
-    for (int i = 0; i < BPT; ++i) c[i] = 0;
-    const uint32_t local = smem_addr(&S.hist[lo]);
-#pragma unroll 1
-    for (int r = 0; r < G; ++r) {
-      const uint32_t a = map_rank(local, r);
-#pragma unroll
-      for (int q = 0; q < BPT; q += 4) {
-        const uint4 v = ld_dsmem_v4(a + 4 * q);
-        c[BPT - 1 - q] += v.x;
-        c[BPT - 2 - q] += v.y;
-        c[BPT - 3 - q] += v.z;
-        c[BPT - 4 - q] += v.w;
+        for (int j = 0; j < 3; ++j)
+          st_dsmem_u32(map_rank(smem_addr(&S.res[j]), threadIdx.x + 1), S.res[j]);
       }
     }
-    const uint32_t bin = find_bin<BPT>(c, target, S, above, inbin);
-    cluster_sync();  // every CTA has read every histogram
-#pragma unroll
-    for (int i = 0; i < BPT; ++i) S.hist[lo + i] = 0;
-    __syncthreads();
-    return bin;
+    cluster_sync();  // the result has reached every CTA
+    *above = S.res[1];
+    *inbin = S.res[2];
+    return S.res[0];
   }
 }
 
@@ -297,9 +315,9 @@ __device__ __forceinline__ void load_round(const uint32_t* a, int base, int n,
 
 // Histogram of stash keys: entries e < n with (key >> fshift) == fval (all
 // entries when !filter) add one to bin (key >> dshift) & dmask.
-template <class SM>
+template <int G = 1, class SM>
 __device__ void stash_hist(SM& S, int n, bool filter, uint32_t fshift, uint32_t fval,
-                           uint32_t dshift, uint32_t dmask) {
+                           uint32_t dshift, uint32_t dmask, HistDst<G> dst = HistDst<G>{0u, true}) {
   for (int base0 = 0; base0 < n; base0 += kRoundEntries) {
     const int base = base0 + kRoundPerThread * threadIdx.x;
     uint32_t kv[kRoundPerThread];
@@ -308,7 +326,7 @@ __device__ void stash_hist(SM& S, int n, bool filter, uint32_t fshift, uint32_t 
     for (int c = 0; c < kRoundPerThread; ++c) {
       const uint32_t key = kv[c];
       const bool ok = (base + c < n) && (!filter || (key >> fshift) == fval);
-      hist_add(S.hist, ok ? ((key >> dshift) & dmask) : 0xffffffffu);
+      hist_inc<G>(S.hist, dst, ok ? ((key >> dshift) & dmask) : 0xffffffffu);
     }
   }
 }
@@ -321,20 +339,27 @@ __device__ void stash_hist(SM& S, int n, bool filter, uint32_t fshift, uint32_t 
 // share a few coarse bins, and their shared atomics would serialise in the
 // streaming loop.) The histogram is all zero on entry and on return.
 template <int G, class SM>
-__device__ Cut select_stash(SM& S, int n, uint32_t target) {
+__device__ Cut select_stash(SM& S, int n, uint32_t target, HistDst<G> dst = HistDst<G>{0u, true}) {
   uint32_t above, inbin;
-  __syncthreads();  // the last stash writes of every thread are visible
-  stash_hist(S, n, false, 0, 0, 21, 0x7ff);
-  const uint32_t b1 = merged_find<G, 8>(S, target, &above, &inbin);
+  // The last stash writes of every thread are visible; in a cluster, rank 0
+  // is also done with its histogram (its own compactions) before any CTA
+  // adds into it.
+  if constexpr (G > 1) {
+    cluster_sync();
+  } else {
+    __syncthreads();
+  }
+  stash_hist<G>(S, n, false, 0, 0, 21, 0x7ff, dst);
+  const uint32_t b1 = merged_find<G, 8>(S, target, &above, &inbin, dst.local);
   uint32_t rem = target - above;
   if (rem == inbin) return Cut{21, b1, rem, true};
-  stash_hist(S, n, true, 21, b1, 10, 0x7ff);
-  const uint32_t b2 = merged_find<G, 8>(S, rem, &above, &inbin);
+  stash_hist<G>(S, n, true, 21, b1, 10, 0x7ff, dst);
+  const uint32_t b2 = merged_find<G, 8>(S, rem, &above, &inbin, dst.local);
   const uint32_t p2 = (b1 << 11) | b2;
   rem -= above;
   if (rem == inbin) return Cut{10, p2, rem, true};
-  stash_hist(S, n, true, 10, p2, 0, 0x3ff);
-  const uint32_t b3 = merged_find<G, 4>(S, rem, &above, &inbin);
+  stash_hist<G>(S, n, true, 10, p2, 0, 0x3ff, dst);
+  const uint32_t b3 = merged_find<G, 4>(S, rem, &above, &inbin, dst.local);
   rem -= above;
   return Cut{0, (p2 << 10) | b3, rem, rem == inbin};
 }
@@ -600,6 +625,14 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
   prime();  // the first stages are in flight during the setup and the sample passes
   for (int i = t; i < kBins; i += kThreads) S.hist[i] = 0;
   __syncthreads();
+  // In a cluster, every CTA's histogram increments go to rank 0's histogram,
+  // which is zero before any CTA adds into it (and after every search).
+  HistDst<G> hdst{0u, true};
+  if constexpr (G > 1) {
+    hdst.h0 = map_rank(smem_addr(&S.hist[0]), 0);
+    hdst.local = rank == 0;
+    cluster_sync();
+  }
 
   // ---- sampled cutoff: two 11-bit radix passes over the sample ---------------
   if (sampled) {
@@ -613,8 +646,8 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
       sk[4 * v + 3] = order_key(sx[v].w);
     }
 #pragma unroll
-    for (int i = 0; i < 16; ++i) hist_add(S.hist, ((smask >> i) & 1u) ? (sk[i] >> 21) : 0xffffffffu);
-    const uint32_t b1 = merged_find<G, 8>(S, target, &above, &inbin);
+    for (int i = 0; i < 16; ++i) hist_inc<G>(S.hist, hdst, ((smask >> i) & 1u) ? (sk[i] >> 21) : 0xffffffffu);
+    const uint32_t b1 = merged_find<G, 8>(S, target, &above, &inbin, hdst.local);
     const uint32_t rem = target - above;
     if (rem == inbin) {
       thr = b1 << 21;
@@ -622,9 +655,9 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const bool ok = ((smask >> i) & 1u) && (sk[i] >> 21) == b1;
-        hist_add(S.hist, ok ? ((sk[i] >> 10) & 0x7ffu) : 0xffffffffu);
+        hist_inc<G>(S.hist, hdst, ok ? ((sk[i] >> 10) & 0x7ffu) : 0xffffffffu);
       }
-      const uint32_t b2 = merged_find<G, 8>(S, rem, &above, &inbin);
+      const uint32_t b2 = merged_find<G, 8>(S, rem, &above, &inbin, hdst.local);
       thr = (b1 << 21) | (b2 << 10);
     }
   }
@@ -861,17 +894,20 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
     if constexpr (G > 1) {
       if (t == 0) S.pub[0] = n_st;
       cluster_sync();
-      total = 0;
-      for (int r = 0; r < G; ++r) total += ld_dsmem_u32(map_rank(smem_addr(&S.pub[0]), r));
-      cluster_sync();
+      if (w == 0) {  // lane r reads rank r's count
+        uint32_t v = lane < G ? ld_dsmem_u32(map_rank(smem_addr(&S.pub[0]), lane)) : 0u;
+        v = __reduce_add_sync(0xffffffffu, v);
+        if (lane == 0) S.res[3] = v;
+      }
+      cluster_sync();  // every CTA has read every count; S.res[3] is visible
+      total = S.res[3];
     }
     if (total < need) {  // uniform over the cluster
       if (p.counters != nullptr && t == 0 && rank == 0) atomicAdd(&p.counters[kCntRescan], 1u);
       thr = 0;
       bound = float_bound(thr);
       n_st = 0;
-      for (int i = t; i < kBins; i += kThreads) S.hist[i] = 0;  // forget the first pass
-      __syncthreads();
+      __syncthreads();  // (the histogram is zero: every search leaves it so)
       prime();
       stream_pass();
     }
@@ -975,7 +1011,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
     for (int q = p0 + 32 * t; q < p1; q += 32 * kThreads) prefetch_l2(pt_row + q);
     if (t == 0 && p1 > p0) prefetch_l2(pt_row + p1 - 1);  // the last line, if no start fell in it
   }
-  const Cut cut = select_stash<G>(S, static_cast<int>(n_st), kk);
+  const Cut cut = select_stash<G>(S, static_cast<int>(n_st), kk, hdst);
   uint32_t gt0 = 0, eq0 = 0;
   if constexpr (G > 1) {
     // Entries above / at the cutoff in this CTA's stash; lower ranks come first.
@@ -999,10 +1035,22 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
       atomicAdd(&S.pub[2], le);
     }
     cluster_sync();
-    for (int r = 0; r < rank; ++r) {
-      gt0 += ld_dsmem_u32(map_rank(smem_addr(&S.pub[1]), r));
-      eq0 += ld_dsmem_u32(map_rank(smem_addr(&S.pub[2]), r));
+    if (w == 0) {  // lane r < rank reads rank r's counts
+      uint32_t g = 0, e = 0;
+      if (lane < rank) {
+        g = ld_dsmem_u32(map_rank(smem_addr(&S.pub[1]), lane));
+        e = ld_dsmem_u32(map_rank(smem_addr(&S.pub[2]), lane));
+      }
+      g = __reduce_add_sync(0xffffffffu, g);
+      e = __reduce_add_sync(0xffffffffu, e);
+      if (lane == 0) {
+        S.off[0] = g;
+        S.off[1] = e;
+      }
     }
+    __syncthreads();
+    gt0 = S.off[0];
+    eq0 = S.off[1];
   }
   emit_rounds(S, static_cast<int>(n_st), cut, gt0, eq0,
               [&](bool sel, uint32_t pos, uint32_t, uint32_t idx) {

@@ -198,3 +198,11 @@ def test_noalloc_checks_need_no_gpu(lib):
     assert noalloc(pt=some, pt_stride=3072, page_size=0) == tk.Status.EINVAL
     assert noalloc(pt=ctypes.c_void_p(0x1001), pt_stride=3072, page_size=64) == tk.Status.EINVAL
     assert b"scratch" in lib.topk_status_string(tk.Status.ESCRATCH)
+
+
+def test_cluster_residency_query_checks_need_no_gpu(lib):
+    out = ctypes.c_int32(0)
+    assert lib.topk_max_active_clusters(0, 0, 2, ctypes.byref(out)) == tk.Status.EUNSUPPORTED_K
+    assert lib.topk_max_active_clusters(512, 0, 2, None) == tk.Status.EINVAL
+    for g in (0, 1, 3, 32):
+        assert lib.topk_max_active_clusters(512, 0, g, ctypes.byref(out)) == tk.Status.EINVAL

@@ -441,3 +441,13 @@ def test_cuda_graph_replay_with_mutated_lengths(paged, split):
         want = run_oracle(scores, lengths, k, pt, ps if paged else 0)
         assert_parity(scores, lengths, k, out.cpu().numpy(), want, page_table=pt)
 
+
+
+def test_cluster_residency_answers():
+    """The driver's cluster residency answers that the automatic policy uses:
+    clusters of 2, 4 and 8 fit; larger clusters never fit more at once."""
+    for k in (512, 2048):
+        for paged in (False, True):
+            n = [tk.max_active_clusters(k, paged, g) for g in (2, 4, 8, 16)]
+            assert n[0] > 0 and n[1] > 0 and n[2] > 0, n
+            assert n[0] >= n[1] >= n[2] >= n[3] >= 0, n
