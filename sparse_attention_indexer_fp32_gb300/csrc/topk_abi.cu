@@ -13,16 +13,29 @@ namespace {
 using tki::Params;
 
 constexpr int kMaxDevices = 64;
-// Rows at least this long stream against a sampled cutoff by default.
-constexpr int kDefaultSampleMinN = 16384;
+// Rows at least this long stream against a sampled cutoff by default (the
+// dispatch sweep: from 8192-score rows up the sampled cutoff is faster than
+// the full stream, 8.1 against 14.7 us for one 16384-score row; shorter rows
+// have no room for the 4096-score sample).
+constexpr int kDefaultSampleMinN = 8192;
+// FP32 rows of at most this width take the short-row kernel by default. The
+// sweep measured the streaming kernel faster from width 16384 on (B = 1024
+// rows of 16384: 34 against 42 us), the short-row kernel faster at 8192 and
+// below (B = 1024 rows of 8192: 22 against 64 us).
+constexpr int64_t kShortAutoWidth = 8192;
 // Default margin of the sampled rank, in standard deviations. At 5 a row
 // whose sampled cutoff lands above its k-th largest score (and is streamed
 // again) is a ~3e-7 event for the B=1024 workloads; 4 was 1.4 % faster on
 // the 131072-wide rows but makes such a rescan (a latency spike) a few-percent
 // event per call, 6 keeps ~6 % more candidates.
 constexpr float kDefaultSampleZ = 5.0f;
-// A cluster slice should hold at least this many scores to be worth a CTA.
+// A cluster CTA's slice of the row should hold at least this many scores:
+// 16384 for batches of at most kSmallClusterBatch rows, 32768 for larger
+// ones (the sweep: 64 rows of 65536 took 19.2 us on clusters of 4 and 15.7
+// us on one CTA per row; 64 rows of 131072, 21.1 against 23.9 us).
 constexpr int64_t kMinClusterSlice = 16384;
+constexpr int64_t kMinClusterSliceWide = 32768;
+constexpr int32_t kSmallClusterBatch = 16;
 // Workspace layout: per split row one arrival counter (the first 4 KiB,
 // which persist between calls and are zero outside a call), two hand-over
 // counts (the next 8 KiB), then per split row and half k keys and k indices.
@@ -90,23 +103,20 @@ int max_clusters(int kmax, bool paged, int G, int dev) {
   }
 }
 
-// Largest cluster the automatic policy picks.
-constexpr int kAutoMaxCluster = 8;
-
-// CTAs per row: enough to occupy the GPU when the batch is small. G doubles
-// while the clusters of every row still fit on the GPU at once (the driver's
-// answer for clusters of that size, which must each sit in one GPC) and
-// every CTA still gets a long slice of the row.
+// CTAs per row when the batch is too small to occupy the GPU: the largest
+// cluster size G in {16, 8, 4} whose clusters for every row fit on the GPU at
+// once (the driver's answer for clusters of that size, which must each sit
+// in one GPC) while every CTA keeps a long slice of the row; else one CTA per
+// row. Clusters of 2 are never chosen: on the dispatch sweep they were never
+// faster than one CTA per row, two split halves, or clusters of 4.
 int auto_cluster_size(int32_t B, int64_t stride, int kmax, bool paged, int dev) {
-  int G = 1;
-  while (G < kAutoMaxCluster) {
-    const int G2 = 2 * G;
-    if (stride / G2 < kMinClusterSlice) break;
-    const int fit = max_clusters(kmax, paged, G2, dev);
-    if (fit <= 0 || B > fit) break;
-    G = G2;
+  const int64_t slice_min = B <= kSmallClusterBatch ? kMinClusterSlice : kMinClusterSliceWide;
+  for (int G = 16; G >= 4; G /= 2) {
+    if (stride / G < slice_min) continue;
+    const int fit = max_clusters(kmax, paged, G, dev);
+    if (fit > 0 && B <= fit) return G;
   }
-  return G;
+  return 1;
 }
 
 bool aligned4(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 3u) == 0; }
@@ -254,7 +264,7 @@ topk_status select_impl(const void* scores, bool bf16, int64_t stride, const int
     return launch_short(scores, bf16, stride, lengths, B, k, page_table, pt_stride, page_size, out,
                         opts, stream);
   }
-  if (short_rows == 0 && fits_short && !streaming_opts)
+  if (short_rows == 0 && stride <= kShortAutoWidth && !streaming_opts)
     return launch_short(scores, false, stride, lengths, B, k, page_table, pt_stride, page_size, out,
                         opts, stream);
 
@@ -417,7 +427,7 @@ topk_status topk_select_noalloc(const float* scores, int64_t stride, const int32
   // (the same policy as the call it makes: rows of at most kShortMaxRow scores
   // take the short-row kernel, which splits nothing)
   const int kmax = k <= 512 ? 512 : (k <= 1024 ? 1024 : 2048);
-  const int G = stride <= tki::kShortMaxRow ? 0 : auto_cluster_size(B, stride, kmax, page_table != nullptr, dev);
+  const int G = stride <= kShortAutoWidth ? 0 : auto_cluster_size(B, stride, kmax, page_table != nullptr, dev);
   const int m = G == 1 ? auto_split_rows(B, stride, info->sm_count) : 0;
   if (ws_bytes_for(k, m) > kStaticWsBytes) return TOPK_ESCRATCH;
   void* ws = nullptr;

@@ -5,20 +5,24 @@
 // The streaming kernel's per-row fixed costs (sample loads, ring set-up,
 // three radix passes, emission rounds) are paid for every row, and with two
 // rows in flight per SM they dominate rows this short. Here one CTA of 256
-// threads takes a row and keeps it in registers, E consecutive scores per
-// thread (E = 32: rows up to 8192; E = 64: up to 16384), so the row is read
-// from HBM exactly once and every later step works on registers and a small
-// shared-memory stash. The design follows the bf16 small-row top-k of the
-// sglang PR 39648 report (实现拆解 2: one CTA per row, the row resident in
-// registers, radix passes to the exact k-th value, page-table transform on
-// output):
+// threads takes a row and keeps it in registers, E scores per thread (E = 32:
+// rows up to 8192; E = 64: up to 16384), so the row is read from HBM exactly
+// once and every later step works on registers and a small shared-memory
+// stash. Each warp owns a contiguous eighth of the row and reads it with
+// 16-byte vector loads that cover 512 contiguous bytes per instruction; the
+// (vector, lane, element) order of a warp's scores is their index order, and
+// one packed warp scan turns per-vector hit counts into stash positions.
+// The design follows the bf16 small-row top-k of the sglang PR 39648 report
+// (实现拆解 2: one CTA per row, the row resident in registers, radix passes to
+// the exact k-th value, page-table transform on output):
 //
 //  1. Coarse pass over the whole row (it is in registers, so this costs no
 //     memory traffic): the 11-bit bin b1 of the k-th largest key, with the
 //     counts above it and in it. If the whole bin is selected, the census
 //     (4) follows at once.
 //  2. Filter: the scores in or above bin b1 go to the stash as (key, index),
-//     in index order (per-thread counts, one block prefix).
+//     in index order (per-vector counts, one packed warp scan, one block
+//     prefix over the warps).
 //  3. The finer passes (11, then 10 bits) over the stash entries of bin b1
 //     only, and emission in stash (= index) order with the streaming
 //     kernel's emit_rounds.
@@ -82,59 +86,91 @@ struct ShortParams {
 template <typename T>
 struct ScoreIn;
 
+// V consecutive scores per 16-byte vector, converted to order-preserving keys.
 template <>
 struct ScoreIn<float> {
-  // E consecutive scores from p (16-byte aligned when `vec`).
-  template <int E>
-  __device__ __forceinline__ static void load(const float* p, int nv, bool vec, uint32_t (&key)[E]) {
-    if (vec) {
-#pragma unroll
-      for (int q = 0; q < E / 4; ++q) {
-        const float4 x = __ldg(reinterpret_cast<const float4*>(p) + q);
-        key[4 * q + 0] = order_key(x.x);
-        key[4 * q + 1] = order_key(x.y);
-        key[4 * q + 2] = order_key(x.z);
-        key[4 * q + 3] = order_key(x.w);
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < E; ++j) key[j] = j < nv ? order_key(__ldg(p + j)) : 0u;
-    }
+  static constexpr int V = 4;
+  __device__ __forceinline__ static uint32_t key_at(const float* p) { return order_key(__ldg(p)); }
+  __device__ __forceinline__ static void vec(const float* p, uint32_t* key) {
+    const float4 x = __ldg(reinterpret_cast<const float4*>(p));
+    key[0] = order_key(x.x);
+    key[1] = order_key(x.y);
+    key[2] = order_key(x.z);
+    key[3] = order_key(x.w);
   }
-  static constexpr int kVecAlign = 16;
 };
 
 template <>
 struct ScoreIn<uint16_t> {
+  static constexpr int V = 8;
   // bf16 -> fp32 is exact: the bf16 bits are the float's high half.
   __device__ __forceinline__ static uint32_t key_of(uint32_t bits16) {
     return order_key(__uint_as_float(bits16 << 16));
   }
-  template <int E>
-  __device__ __forceinline__ static void load(const uint16_t* p, int nv, bool vec, uint32_t (&key)[E]) {
-    if (vec) {
+  __device__ __forceinline__ static uint32_t key_at(const uint16_t* p) { return key_of(__ldg(p)); }
+  __device__ __forceinline__ static void vec(const uint16_t* p, uint32_t* key) {
+    const uint4 x = __ldg(reinterpret_cast<const uint4*>(p));
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-      for (int q = 0; q < E / 8; ++q) {
-        const uint4 x = __ldg(reinterpret_cast<const uint4*>(p) + q);
-        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          key[8 * q + 2 * i + 0] = key_of(w[i] & 0xffffu);
-          key[8 * q + 2 * i + 1] = key_of(w[i] >> 16);
-        }
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < E; ++j) key[j] = j < nv ? key_of(__ldg(p + j)) : 0u;
+    for (int i = 0; i < 4; ++i) {
+      key[2 * i + 0] = key_of(w[i] & 0xffffu);
+      key[2 * i + 1] = key_of(w[i] >> 16);
     }
   }
-  static constexpr int kVecAlign = 16;
+};
+
+// Positions in index order inside one warp. Lane l's vector q covers the
+// warp's scores [q*32V + l*V, q*32V + l*V + V), so the warp's index order is
+// (q, lane, element). Given each lane's hit count per vector, run() leaves,
+// packed FB bits per vector, the hits of the lower lanes in each vector
+// (exc) and the warp's hits in each vector (tot): one inclusive warp scan of
+// PW packed words instead of one scan per vector.
+template <int NQ, int V>
+struct SlabScan {
+  static constexpr int FB = (32 * V < 256) ? 8 : 16;  // a field holds up to 32 * V
+  static constexpr int PW = (NQ * FB + 31) / 32;
+  static constexpr uint32_t kMask = (1u << FB) - 1u;
+  uint32_t exc[PW];
+  uint32_t tot[PW];
+
+  __device__ __forceinline__ void run(const uint32_t (&cnt)[NQ]) {
+    uint32_t inc[PW];
+#pragma unroll
+    for (int i = 0; i < PW; ++i) inc[i] = 0;
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) inc[(q * FB) / 32] |= cnt[q] << ((q * FB) % 32);
+    uint32_t own[PW];
+#pragma unroll
+    for (int i = 0; i < PW; ++i) own[i] = inc[i];
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+#pragma unroll
+      for (int i = 0; i < PW; ++i) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, inc[i], d);
+        if (lane >= d) inc[i] += y;  // fields never carry: each sum is at most 32 * V
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < PW; ++i) {
+      tot[i] = __shfl_sync(0xffffffffu, inc[i], 31);
+      exc[i] = inc[i] - own[i];
+    }
+  }
+  __device__ __forceinline__ static uint32_t field(const uint32_t (&a)[PW], int q) {
+    return (a[(q * FB) / 32] >> ((q * FB) % 32)) & kMask;
+  }
 };
 
 template <int E, int KMAX, bool PAGED, typename T>
 __global__ void __launch_bounds__(kThreads, E <= 32 ? 4 : 2) topk_short_kernel(const ShortParams p) {
   constexpr int C = ShortCap<KMAX>::value;
+  constexpr int V = ScoreIn<T>::V;
+  constexpr int NQ = E / V;  // vectors per lane
+  constexpr int CH = 32 * E;  // scores per warp
+  constexpr int NW = E / 32;  // words of per-score bit masks
   static_assert(E % 32 == 0 && E * kThreads <= kShortMaxRow, "a row must fit the CTA's registers");
+  static_assert(32 % V == 0, "a vector's bits stay in one mask word");
   __shared__ __align__(16) ShortSmem<C> S;
 
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
@@ -175,48 +211,59 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? 4 : 2) topk_short_kernel(c
   }
   const uint32_t kk = static_cast<uint32_t>(p.k);
 
-  // ---- this thread's E consecutive scores, as keys --------------------------
+  // ---- this lane's scores, as keys ------------------------------------------
+  // Warp w owns the row's scores [w*CH, (w+1)*CH); key[q*V + c] is the score
+  // at index w*CH + q*32V + lane*V + c, so each vector load of a warp reads
+  // 512 contiguous bytes.
   const T* rp = static_cast<const T*>(p.scores) + static_cast<int64_t>(row) * p.stride;
-  const int first = E * t;
-  const int nv = min(max(n - first, 0), E);  // valid scores of this thread
+  const int wbase = w * CH;
+  auto index_of = [&](int q, int c) -> uint32_t {
+    return static_cast<uint32_t>(wbase + q * 32 * V + lane * V + c);
+  };
   uint32_t key[E];
-  {
-    const T* tp = rp + first;
-    const bool vec = nv == E && (reinterpret_cast<uintptr_t>(tp) % ScoreIn<T>::kVecAlign) == 0;
-    if (nv > 0) {
-      ScoreIn<T>::template load<E>(tp, nv, vec, key);
-    } else {
+  uint32_t valid[NW];
+  const bool full = ((reinterpret_cast<uintptr_t>(rp) & 15u) == 0) && wbase + CH <= n;  // warp-uniform
+  if (full) {
 #pragma unroll
-      for (int j = 0; j < E; ++j) key[j] = 0u;
+    for (int q = 0; q < NQ; ++q) ScoreIn<T>::vec(rp + index_of(q, 0), &key[q * V]);
+#pragma unroll
+    for (int i = 0; i < NW; ++i) valid[i] = 0xffffffffu;
+  } else {
+#pragma unroll
+    for (int i = 0; i < NW; ++i) valid[i] = 0;
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+#pragma unroll
+      for (int c = 0; c < V; ++c) {
+        const int j = q * V + c;
+        const bool ok = index_of(q, c) < static_cast<uint32_t>(n);
+        key[j] = ok ? ScoreIn<T>::key_at(rp + index_of(q, c)) : 0u;
+        valid[j / 32] |= static_cast<uint32_t>(ok) << (j % 32);
+      }
     }
-  }
-  // valid[q]: bit j of word q set when score 32q + j of the thread exists
-  uint32_t valid[E / 32];
-#pragma unroll
-  for (int q = 0; q < E / 32; ++q) {
-    const int m = min(max(nv - 32 * q, 0), 32);
-    valid[q] = m >= 32 ? 0xffffffffu : ((1u << m) - 1u);
   }
   for (int i = t; i < kBins / 4; i += kThreads) reinterpret_cast<uint4*>(S.hist)[i] = make_uint4(0, 0, 0, 0);
   __syncthreads();
 
   int grp = 0;
-  // Block prefix of one packed count per thread: returns the count of lower
-  // threads (packed) and the total; one barrier.
-  auto block_prefix = [&](uint32_t c, uint32_t& before, uint32_t& total) {
-    const uint32_t incl = warp_incl_scan(c);
+  // Block prefix of one packed count per warp (the warp's lane 0 holds it):
+  // returns the count of lower warps (packed) and the total; one barrier.
+  auto warp_prefix = [&](uint32_t c, uint32_t& before, uint32_t& total) {
     const int par = grp & 1;
     ++grp;
-    if (lane == 31) S.tab[par][w] = incl;
+    if (lane == 0) S.tab[par][w] = c;
     __syncthreads();
     const uint32_t e = lane < kWarps ? S.tab[par][lane] : 0u;
-    before = __reduce_add_sync(0xffffffffu, lane < w ? e : 0u) + incl - c;
+    before = __reduce_add_sync(0xffffffffu, lane < w ? e : 0u);
     total = __reduce_add_sync(0xffffffffu, e);
+  };
+  auto vec_bits = [&](const uint32_t (&m)[NW], int q) -> uint32_t {
+    return (m[(q * V) / 32] >> ((q * V) % 32)) & ((1u << V) - 1u);
   };
 
   // ---- 1. the coarse bin of the k-th largest score, over the whole row -------
   uint32_t above, inbin;
-  if (nv == E) {  // every score of this thread exists (all threads but the row's last)
+  if (full) {
 #pragma unroll
     for (int j = 0; j < E; ++j) atomicAdd(&S.hist[key[j] >> 21], 1u);
   } else {
@@ -230,30 +277,39 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? 4 : 2) topk_short_kernel(c
     cut = Cut{21, b1, rem, true};  // the whole bin is selected: straight to the census
   } else if (p.sample_mode != 1 && above + inbin <= static_cast<uint32_t>(C)) {
     // ---- 2. the scores in or above that bin go to the stash, in index order --
-    uint32_t hit[E / 32];
-    uint32_t cnt = 0;
+    uint32_t hit[NW];
     const uint32_t lo1 = b1 << 21;  // the lowest key of bin b1
 #pragma unroll
-    for (int q = 0; q < E / 32; ++q) {
+    for (int i = 0; i < NW; ++i) {
       uint32_t m = 0;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) m |= static_cast<uint32_t>(key[32 * q + j] >= lo1) << j;
-      hit[q] = m & valid[q];
-      cnt += __popc(hit[q]);
+      for (int j = 0; j < 32; ++j) m |= static_cast<uint32_t>(key[32 * i + j] >= lo1) << j;
+      hit[i] = m & valid[i];
     }
+    uint32_t cnt[NQ];
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) cnt[q] = __popc(vec_bits(hit, q));
+    SlabScan<NQ, V> sc;
+    sc.run(cnt);
+    uint32_t wt = 0;
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) wt += SlabScan<NQ, V>::field(sc.tot, q);
     uint32_t before, total;
-    block_prefix(cnt, before, total);  // total == above + inbin
-    uint32_t pos = before;
+    warp_prefix(wt, before, total);  // total == above + inbin
+    uint32_t vbase = before;  // the warp's hits in the vectors before q
 #pragma unroll
-    for (int q = 0; q < E / 32; ++q) {
+    for (int q = 0; q < NQ; ++q) {
+      uint32_t pos = vbase + SlabScan<NQ, V>::field(sc.exc, q);
+      const uint32_t m = vec_bits(hit, q);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        if ((hit[q] >> j) & 1u) {
-          S.skey[pos] = key[32 * q + j];
-          S.sidx[pos] = static_cast<uint32_t>(first + 32 * q + j);
+      for (int c = 0; c < V; ++c) {
+        if ((m >> c) & 1u) {
+          S.skey[pos] = key[q * V + c];
+          S.sidx[pos] = index_of(q, c);
           ++pos;
         }
       }
+      vbase += SlabScan<NQ, V>::field(sc.tot, q);
     }
     if (PAGED) {  // the emission reads the row's page-table entries
       const int p1 = (n + p.page_size - 1) / p.page_size;
@@ -303,36 +359,54 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? 4 : 2) topk_short_kernel(c
   }
   // Census: scores above the cut and the first r tied ones (index order).
   if (p.counters != nullptr && t == 0) atomicAdd(&p.counters[kCntShortExact], 1u);
-  uint32_t gtm[E / 32], eqm[E / 32];
-  uint32_t c = 0;
+  uint32_t gtm[NW], eqm[NW];
 #pragma unroll
-  for (int q = 0; q < E / 32; ++q) {
+  for (int i = 0; i < NW; ++i) {
     uint32_t g = 0, e = 0;
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
-      const uint32_t hi = key[32 * q + j] >> cut.shift;
+      const uint32_t hi = key[32 * i + j] >> cut.shift;
       g |= static_cast<uint32_t>(hi > cut.P) << j;
       e |= static_cast<uint32_t>(hi == cut.P) << j;
     }
-    gtm[q] = g & valid[q];
-    eqm[q] = e & valid[q];
-    c += (static_cast<uint32_t>(__popc(gtm[q])) << 16) + static_cast<uint32_t>(__popc(eqm[q]));
+    gtm[i] = g & valid[i];
+    eqm[i] = e & valid[i];
+  }
+  uint32_t cg[NQ], ce[NQ];
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) {
+    cg[q] = __popc(vec_bits(gtm, q));
+    ce[q] = __popc(vec_bits(eqm, q));
+  }
+  SlabScan<NQ, V> sg, se;
+  sg.run(cg);
+  se.run(ce);
+  uint32_t wg = 0, we = 0;
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) {
+    wg += SlabScan<NQ, V>::field(sg.tot, q);
+    we += SlabScan<NQ, V>::field(se.tot, q);
   }
   uint32_t before, total;
-  block_prefix(c, before, total);
-  uint32_t gb = before >> 16, eb = before & 0xffffu;
+  warp_prefix((wg << 16) | we, before, total);
+  uint32_t gbase = before >> 16, ebase = before & 0xffffu;
 #pragma unroll
-  for (int q = 0; q < E / 32; ++q) {
+  for (int q = 0; q < NQ; ++q) {
+    uint32_t gb = gbase + SlabScan<NQ, V>::field(sg.exc, q);
+    uint32_t eb = ebase + SlabScan<NQ, V>::field(se.exc, q);
+    const uint32_t mg = vec_bits(gtm, q), me = vec_bits(eqm, q);
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const bool g = (gtm[q] >> j) & 1u, e = (eqm[q] >> j) & 1u;
+    for (int c = 0; c < V; ++c) {
+      const bool g = (mg >> c) & 1u, e = (me >> c) & 1u;
       if (g || (e && eb < cut.r)) {
         const uint32_t pos = gb + min(eb, cut.r);
-        if (pos < kk) out_row[pos] = map_index(static_cast<uint32_t>(first + 32 * q + j));
+        if (pos < kk) out_row[pos] = map_index(index_of(q, c));
       }
       gb += g;
       eb += e;
     }
+    gbase += SlabScan<NQ, V>::field(sg.tot, q);
+    ebase += SlabScan<NQ, V>::field(se.tot, q);
   }
 }
 

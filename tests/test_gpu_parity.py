@@ -451,3 +451,18 @@ def test_cluster_residency_answers():
             n = [tk.max_active_clusters(k, paged, g) for g in (2, 4, 8, 16)]
             assert n[0] > 0 and n[1] > 0 and n[2] > 0, n
             assert n[0] >= n[1] >= n[2] >= n[3] >= 0, n
+
+
+@pytest.mark.parametrize("B,stride,clustered", [(1, 262144, True), (4, 131072, True),
+                                                (64, 131072, True), (4, 32768, False),
+                                                (64, 65536, False), (200, 262144, False)])
+def test_automatic_cluster_policy(B, stride, clustered):
+    """Small batches of long rows run on clusters, short rows and larger
+    batches on one CTA per row (the gates the dispatch sweep measured); the
+    result is the oracle's either way."""
+    rng = np.random.default_rng(B + stride)
+    scores = rng.standard_normal((B, stride)).astype(np.float32)
+    lengths = rng.integers(stride * 4 // 5, stride + 1, B).astype(np.int32)
+    cnt = counters_tensor()
+    check_against_oracle(scores, lengths, 512, counters=cnt)
+    assert int(cnt[tk.Counter.CLUSTER_ROWS]) == (B if clustered else 0)
