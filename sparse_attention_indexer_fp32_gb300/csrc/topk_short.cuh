@@ -222,23 +222,33 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? 4 : 2) topk_short_kernel(c
   };
   uint32_t key[E];
   uint32_t valid[NW];
-  const bool full = ((reinterpret_cast<uintptr_t>(rp) & 15u) == 0) && wbase + CH <= n;  // warp-uniform
+  const bool aligned = (reinterpret_cast<uintptr_t>(rp) & 15u) == 0;
+  const bool full = aligned && wbase + CH <= n;  // warp-uniform
   if (full) {
 #pragma unroll
     for (int q = 0; q < NQ; ++q) ScoreIn<T>::vec(rp + index_of(q, 0), &key[q * V]);
 #pragma unroll
     for (int i = 0; i < NW; ++i) valid[i] = 0xffffffffu;
   } else {
+    // The warp holding the row's end (or any warp of a row that does not
+    // start on 16 bytes): whole vectors inside the row still load as vectors,
+    // the vector that holds the end score by score, the rest not at all.
 #pragma unroll
     for (int i = 0; i < NW; ++i) valid[i] = 0;
 #pragma unroll
     for (int q = 0; q < NQ; ++q) {
+      const int v0 = static_cast<int>(index_of(q, 0));
+      if (aligned && v0 + V <= n) {
+        ScoreIn<T>::vec(rp + v0, &key[q * V]);
+        valid[(q * V) / 32] |= ((1u << V) - 1u) << ((q * V) % 32);
+      } else {
 #pragma unroll
-      for (int c = 0; c < V; ++c) {
-        const int j = q * V + c;
-        const bool ok = index_of(q, c) < static_cast<uint32_t>(n);
-        key[j] = ok ? ScoreIn<T>::key_at(rp + index_of(q, c)) : 0u;
-        valid[j / 32] |= static_cast<uint32_t>(ok) << (j % 32);
+        for (int c = 0; c < V; ++c) {
+          const int j = q * V + c;
+          const bool ok = v0 + c < n;
+          key[j] = ok ? ScoreIn<T>::key_at(rp + v0 + c) : 0u;
+          valid[j / 32] |= static_cast<uint32_t>(ok) << (j % 32);
+        }
       }
     }
   }
