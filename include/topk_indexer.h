@@ -29,7 +29,10 @@
  *   that keeps fewer than m_b candidates makes the row be scanned again in full.
  *
  * Preconditions that are not checked (they would need a device read):
- *   - no NaN in scores[b, 0 .. n_b); values past n_b are never read;
+ *   - no NaN in scores[b, 0 .. n_b); values past n_b never affect the result
+ *     (rows of at most 16384 scores that start on 16 bytes may have the rest
+ *     of the 16-byte block holding their last score read, never beyond the
+ *     row's stride);
  *   - paged: every mapped slot fits in int32 (see topk_paged).
  *
  * Memory and execution:

@@ -126,21 +126,26 @@ int max_active_clusters(int G, int dev) {
 // Short-row kernel variant (E scores per thread).
 template <int E, int KMAX, bool PAGED, typename T>
 topk_status launch_short_variant(const ShortParams& p_in, int dev, int sm_count, cudaStream_t stream) {
-  // CTAs resident at once on this device (per device, found once).
+  constexpr size_t smem = sizeof(ShortSmem<ShortCap<KMAX>::value>);
+  // CTAs resident at once on this device (per device, found once, after the
+  // kernel's shared-memory attribute is set).
   static std::atomic<int> resident[64];
-  int per_sm = resident[dev].load(std::memory_order_relaxed);
+  int per_sm = resident[dev].load(std::memory_order_acquire);
   if (per_sm == 0) {
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_short_kernel<E, KMAX, PAGED, T>,
-                                                      kThreads, 0) != cudaSuccess)
+    if (cudaFuncSetAttribute(topk_short_kernel<E, KMAX, PAGED, T>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
       return TOPK_ECUDA;
-    resident[dev].store(per_sm, std::memory_order_relaxed);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_short_kernel<E, KMAX, PAGED, T>,
+                                                      kThreads, smem) != cudaSuccess)
+      return TOPK_ECUDA;
+    resident[dev].store(per_sm, std::memory_order_release);
   }
   ShortParams p = p_in;
   p.ahead = per_sm * sm_count;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.B), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   return cudaLaunchKernelEx(&cfg, topk_short_kernel<E, KMAX, PAGED, T>, p) == cudaSuccess
              ? TOPK_OK

@@ -59,12 +59,78 @@ template <int C>
 struct ShortSmem {
   uint32_t skey[C];
   uint32_t sidx[C];
-  uint32_t hist[kBins];
+  uint32_t hist[kBins];    // (emit_rounds' and the shared helpers' name for hbuf[0])
+  uint32_t hist2[kBins];   // the second histogram buffer
+  uint32_t tincl[kThreads];  // per-thread inclusive bin sums within the warp
   uint32_t tab[2][kWarps];
   uint32_t rtab[2][kWarps];
   uint32_t scan[kWarps];
   uint32_t res[4];
 };
+
+// Finds the bin holding the target-th largest element (1 <= target <= total)
+// of histogram `hist` with two CTA barriers and no broadcast: each thread
+// sums the BPT consecutive bins it owns, and after the second barrier every
+// warp locates, from the warp totals and the per-thread sums, the thread and
+// then the bin that holds the target, by itself. The bins are left as they
+// are: each thread instead zeroes its own bins of `other`, the buffer of the
+// previous search, which every warp finished reading before the first
+// barrier and which the next histogram fills after the second. Returns the
+// bin; *above = elements in higher bins; *inbin = elements in it.
+template <int BPT, class SM>
+__device__ uint32_t find_bin_all(SM& S, const uint32_t* hist, uint32_t* other, uint32_t target,
+                                 uint32_t* above, uint32_t* inbin) {
+  constexpr int nbins = BPT * kThreads;
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const int lo = nbins - BPT * (t + 1);  // lowest owned bin
+  __syncthreads();  // the histogram is complete; the previous search is over in every warp
+  uint32_t sum = 0;
+#pragma unroll
+  for (int q = 0; q < BPT; q += 4) {
+    const uint4 v = *reinterpret_cast<const uint4*>(&hist[lo + q]);
+    sum += v.x + v.y + v.z + v.w;
+  }
+  // (all 2048 bins of the other buffer, whatever this search's bin count)
+  reinterpret_cast<uint4*>(&other[kBins - 8 * (t + 1)])[0] = make_uint4(0, 0, 0, 0);
+  reinterpret_cast<uint4*>(&other[kBins - 8 * (t + 1)])[1] = make_uint4(0, 0, 0, 0);
+  const uint32_t incl = warp_incl_scan(sum);
+  S.tincl[t] = incl;
+  if (lane == 31) S.scan[w] = incl;
+  __syncthreads();
+  // the warp, then the thread, then the bin (each search redone by every warp)
+  const uint32_t e = lane < kWarps ? S.scan[lane] : 0u;
+  const uint32_t ie = warp_incl_scan<kWarps>(e);
+  const int ws = __ffs(__ballot_sync(0xffffffffu, lane < kWarps && ie >= target)) - 1;
+  const uint32_t wbefore = __shfl_sync(0xffffffffu, ie - e, ws);
+  const uint32_t ti = S.tincl[ws * 32 + lane];
+  const int ls = __ffs(__ballot_sync(0xffffffffu, wbefore + ti >= target)) - 1;
+  const uint32_t tprev = __shfl_sync(0xffffffffu, ti, ls > 0 ? ls - 1 : 0);
+  const uint32_t tbefore = wbefore + (ls > 0 ? tprev : 0u);
+  const int lo_s = nbins - BPT * (ws * 32 + ls + 1);
+  const uint32_t c = lane < BPT ? hist[lo_s + BPT - 1 - lane] : 0u;  // descending bins
+  const uint32_t ic = warp_incl_scan<BPT>(c);
+  const int ib = __ffs(__ballot_sync(0xffffffffu, lane < BPT && tbefore + ic >= target)) - 1;
+  *above = tbefore + __shfl_sync(0xffffffffu, ic - c, ib);
+  *inbin = __shfl_sync(0xffffffffu, c, ib);
+  return static_cast<uint32_t>(lo_s + BPT - 1 - ib);
+}
+
+// Histogram of stash keys into `hist`: entries e < n with (key >> fshift) ==
+// fval add one to bin (key >> dshift) & dmask.
+template <class SM>
+__device__ void short_stash_hist(SM& S, uint32_t* hist, int n, uint32_t fshift, uint32_t fval,
+                                 uint32_t dshift, uint32_t dmask) {
+  for (int base0 = 0; base0 < n; base0 += kRoundEntries) {
+    const int base = base0 + kRoundPerThread * threadIdx.x;
+    uint32_t kv[kRoundPerThread];
+    load_round(S.skey, base, n, kv);
+#pragma unroll
+    for (int c = 0; c < kRoundPerThread; ++c) {
+      const uint32_t key = kv[c];
+      if (base + c < n && (key >> fshift) == fval) atomicAdd(&hist[(key >> dshift) & dmask], 1u);
+    }
+  }
+}
 
 struct ShortParams {
   const void* scores;  // float or bf16 (as uint16) rows
@@ -171,7 +237,8 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? 4 : 2) topk_short_kernel(c
   constexpr int NW = E / 32;  // words of per-score bit masks
   static_assert(E % 32 == 0 && E * kThreads <= kShortMaxRow, "a row must fit the CTA's registers");
   static_assert(32 % V == 0, "a vector's bits stay in one mask word");
-  __shared__ __align__(16) ShortSmem<C> S;
+  extern __shared__ __align__(128) unsigned char short_smem_raw[];
+  ShortSmem<C>& S = *reinterpret_cast<ShortSmem<C>*>(short_smem_raw);
 
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
   const int row = static_cast<int>(blockIdx.x);
@@ -223,36 +290,46 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? 4 : 2) topk_short_kernel(c
   uint32_t key[E];
   uint32_t valid[NW];
   const bool aligned = (reinterpret_cast<uintptr_t>(rp) & 15u) == 0;
-  const bool full = aligned && wbase + CH <= n;  // warp-uniform
-  if (full) {
-#pragma unroll
-    for (int q = 0; q < NQ; ++q) ScoreIn<T>::vec(rp + index_of(q, 0), &key[q * V]);
-#pragma unroll
-    for (int i = 0; i < NW; ++i) valid[i] = 0xffffffffu;
-  } else {
-    // The warp holding the row's end (or any warp of a row that does not
-    // start on 16 bytes): whole vectors inside the row still load as vectors,
-    // the vector that holds the end score by score, the rest not at all.
-#pragma unroll
-    for (int i = 0; i < NW; ++i) valid[i] = 0;
+  if (aligned) {
+    // Every vector load is issued unconditionally, so that all of them are in
+    // flight together: a vector that starts at or past the row's end re-reads
+    // the row's first vector instead (an L1 hit) and is masked off below. A
+    // row that starts on 16 bytes has a stride that is a whole number of
+    // vectors, so the vector holding the last score lies inside the row's
+    // stride; its scores past the length are masked off too.
 #pragma unroll
     for (int q = 0; q < NQ; ++q) {
       const int v0 = static_cast<int>(index_of(q, 0));
-      if (aligned && v0 + V <= n) {
-        ScoreIn<T>::vec(rp + v0, &key[q * V]);
-        valid[(q * V) / 32] |= ((1u << V) - 1u) << ((q * V) % 32);
-      } else {
+      ScoreIn<T>::vec(rp + (v0 < n ? v0 : 0), &key[q * V]);
+    }
+    if (wbase + CH <= n) {  // warp-uniform: the whole warp lies inside the row
 #pragma unroll
-        for (int c = 0; c < V; ++c) {
-          const int j = q * V + c;
-          const bool ok = v0 + c < n;
-          key[j] = ok ? ScoreIn<T>::key_at(rp + v0 + c) : 0u;
-          valid[j / 32] |= static_cast<uint32_t>(ok) << (j % 32);
-        }
-      }
+      for (int i = 0; i < NW; ++i) valid[i] = 0xffffffffu;
+    } else {
+#pragma unroll
+      for (int i = 0; i < NW; ++i) valid[i] = 0;
+#pragma unroll
+      for (int j = 0; j < E; ++j)
+        valid[j / 32] |= static_cast<uint32_t>(static_cast<int>(index_of(j / V, j % V)) < n) << (j % 32);
+    }
+  } else {
+    // A row that does not start on 16 bytes: score by score, every load
+    // predicated (none is a branch), so they are all in flight together.
+#pragma unroll
+    for (int i = 0; i < NW; ++i) valid[i] = 0;
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+      const int idx = static_cast<int>(index_of(j / V, j % V));
+      const bool ok = idx < n;
+      key[j] = ScoreIn<T>::key_at(rp + (ok ? idx : 0));
+      valid[j / 32] |= static_cast<uint32_t>(ok) << (j % 32);
     }
   }
-  for (int i = t; i < kBins / 4; i += kThreads) reinterpret_cast<uint4*>(S.hist)[i] = make_uint4(0, 0, 0, 0);
+  const bool full = aligned && wbase + CH <= n;  // warp-uniform
+  for (int i = t; i < kBins / 4; i += kThreads) {
+    reinterpret_cast<uint4*>(S.hist)[i] = make_uint4(0, 0, 0, 0);
+    reinterpret_cast<uint4*>(S.hist2)[i] = make_uint4(0, 0, 0, 0);
+  }
   __syncthreads();
 
   int grp = 0;
@@ -280,7 +357,8 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? 4 : 2) topk_short_kernel(c
 #pragma unroll
     for (int j = 0; j < E; ++j) hist_add(S.hist, ((valid[j / 32] >> (j % 32)) & 1u) ? (key[j] >> 21) : 0xffffffffu);
   }
-  const uint32_t b1 = merged_find<1, 8>(S, kk, &above, &inbin);
+  // Searches alternate between the two buffers: S.hist, S.hist2, S.hist.
+  const uint32_t b1 = find_bin_all<8>(S, S.hist, S.hist2, kk, &above, &inbin);
   uint32_t rem = kk - above;
   Cut cut;
   if (rem == inbin) {
@@ -327,15 +405,15 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? 4 : 2) topk_short_kernel(c
     }
     // ---- 3. the exact cutoff inside bin b1 (its entries only), emission -------
     __syncthreads();  // the stash is complete
-    stash_hist(S, static_cast<int>(total), true, 21, b1, 10, 0x7ff);
-    const uint32_t b2 = merged_find<1, 8>(S, rem, &above, &inbin);
+    short_stash_hist(S, S.hist2, static_cast<int>(total), 21, b1, 10, 0x7ff);
+    const uint32_t b2 = find_bin_all<8>(S, S.hist2, S.hist, rem, &above, &inbin);
     const uint32_t p2 = (b1 << 11) | b2;
     rem -= above;
     if (rem == inbin) {
       cut = Cut{10, p2, rem, true};
     } else {
-      stash_hist(S, static_cast<int>(total), true, 10, p2, 0, 0x3ff);
-      const uint32_t b3 = merged_find<1, 4>(S, rem, &above, &inbin);
+      short_stash_hist(S, S.hist, static_cast<int>(total), 10, p2, 0, 0x3ff);
+      const uint32_t b3 = find_bin_all<4>(S, S.hist, S.hist2, rem, &above, &inbin);
       rem -= above;
       cut = Cut{0, (p2 << 10) | b3, rem, rem == inbin};
     }
@@ -349,9 +427,9 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? 4 : 2) topk_short_kernel(c
 #pragma unroll
     for (int j = 0; j < E; ++j) {
       const bool ok = ((valid[j / 32] >> (j % 32)) & 1u) && (key[j] >> 21) == b1;
-      hist_add(S.hist, ok ? ((key[j] >> 10) & 0x7ffu) : 0xffffffffu);
+      hist_add(S.hist2, ok ? ((key[j] >> 10) & 0x7ffu) : 0xffffffffu);
     }
-    const uint32_t b2 = merged_find<1, 8>(S, rem, &above, &inbin);
+    const uint32_t b2 = find_bin_all<8>(S, S.hist2, S.hist, rem, &above, &inbin);
     const uint32_t p2 = (b1 << 11) | b2;
     rem -= above;
     if (rem == inbin) {
@@ -362,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? 4 : 2) topk_short_kernel(c
         const bool ok = ((valid[j / 32] >> (j % 32)) & 1u) && (key[j] >> 10) == p2;
         hist_add(S.hist, ok ? (key[j] & 0x3ffu) : 0xffffffffu);
       }
-      const uint32_t b3 = merged_find<1, 4>(S, rem, &above, &inbin);
+      const uint32_t b3 = find_bin_all<4>(S, S.hist, S.hist2, rem, &above, &inbin);
       rem -= above;
       cut = Cut{0, (p2 << 10) | b3, rem, rem == inbin};
     }
