@@ -299,10 +299,6 @@ topk_status select_impl(const void* scores, bool bf16, int64_t stride, const int
     }
   }
 
-  // One CTA per row: each CTA warms the row of the block that will most
-  // likely take its place (kCtasPerSm CTAs per SM are resident at once).
-  p.ahead = G == 1 ? kCtasPerSm * info->sm_count : 0;
-
   const bool paged = page_table != nullptr;
   switch (kmax) {
     case 512: return paged ? tki::launch_k512_paged(p, G, dev, stream)

@@ -148,10 +148,6 @@ struct Params {
   uint32_t* ws_cnt;      // per split row and half: entries handed over, or kHalfFailed
   uint32_t* ws_key;      // per split row and half: k keys ...
   uint32_t* ws_idx;      // ... and indices, in index order
-  // One CTA per row: CTAs resident at once. Near its end a CTA brings into L2
-  // the start of the row that block (its own + ahead) streams, the block most
-  // likely to take its place next. 0: off.
-  int32_t ahead;
 };
 
 // Cutoff description: an entry is selected if (key >> shift) > P, or if
@@ -487,9 +483,6 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
   int32_t* out_row = p.out + static_cast<int64_t>(row) * p.k;
   const int32_t* pt_row = PAGED ? p.page_table + static_cast<int64_t>(row) * p.pt_stride : nullptr;
   const bool leader = (t == 0 && part == 0);
-  // The row whose start this CTA brings into L2 near its end (see Params::ahead).
-  const int warm_row = (G == 1 && !split && p.ahead > 0) ? row + p.ahead : p.split_first;
-  const int64_t warm_len = (t == 0 && warm_row < p.split_first) ? p.lengths[warm_row] : 0;
 
   // Read-only loads (the table is never written during the call), so the
   // emission's lookups need not wait for its earlier output stores; a
@@ -893,33 +886,6 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
 
   stream_pass();
 
-  // ---- the start of the next row into L2 ------------------------------------
-  // While this CTA finds its cutoff and writes its row, the CTA most likely
-  // to take its place next will want the first ring stages and the sample
-  // chunks of its row: bring them into L2 now, so that its prologue does not
-  // wait on HBM. Issued late on purpose (L2 turns over in tens of
-  // microseconds while every SM streams). A hint only: no data is returned.
-  auto warm_next_row = [&]() {
-    if (t != 0 || warm_row >= p.split_first) return;
-    const int wn = static_cast<int>(warm_len < 0 ? 0 : (warm_len > p.stride ? p.stride : warm_len));
-    if (wn <= p.k) return;
-    const float* wrp = p.scores + static_cast<int64_t>(warm_row) * p.stride;
-    const int wmis = static_cast<int>((reinterpret_cast<uintptr_t>(wrp) >> 2) & 3);
-    const int wh = min((4 - wmis) & 3, wn);
-    const int wnb = ((wn - wh) >> 2) << 2;
-    const float* wbody = wrp + wh;
-    const int first = min(wnb, kStages * kStageFloats);
-    if (first > 0) bulk_prefetch_l2(wbody, static_cast<uint32_t>(first) * 4u);
-    const bool wsampled = wnb >= 2 * 4 * kSampleVec4 &&
-                          (p.sample_mode == 2 || (p.sample_mode == 0 && wn >= p.sample_min_n));
-    if (wsampled) {
-      const int step4 = ((wnb >> 2) - kSampleChunkVec4) / (kSampleChunks - 1);
-      for (int c = 0; c < kSampleChunks; ++c)
-        bulk_prefetch_l2(reinterpret_cast<const float4*>(wbody) + c * step4, kSampleChunkVec4 * 16u);
-    }
-  };
-  if (!sampled) warm_next_row();  // (a sampled row warms after its underflow check)
-
   // ---- underflow: the sampled cutoff kept fewer than k candidates -----------
   // (fewer than min(k, its scores) for the half of a split row)
   const uint32_t need = split ? min(kk, static_cast<uint32_t>(n_part)) : kk;
@@ -945,7 +911,6 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
       prime();
       stream_pass();
     }
-    warm_next_row();
   }
 
   // A wait timed out: let copies still in flight land (bounded) before the
