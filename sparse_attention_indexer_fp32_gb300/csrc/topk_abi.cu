@@ -299,6 +299,8 @@ topk_status select_impl(const void* scores, bool bf16, int64_t stride, const int
     }
   }
 
+  p.resident = kCtasPerSm * info->sm_count;
+
   const bool paged = page_table != nullptr;
   switch (kmax) {
     case 512: return paged ? tki::launch_k512_paged(p, G, dev, stream)
