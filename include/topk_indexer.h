@@ -301,7 +301,7 @@ int32_t topk_abi_version(void);
  *                   CTA per row, so cluster_size must be 0 or 1)
  *   workspace,      as for topk_ragged_ws; NULL = none (no row is split, and
  *   workspace_bytes split_rows must be 0 or -1)
- *   short_rows      0 automatic (FP32 rows of width <= 8192 take the short-row
+ *   short_rows      0 automatic (FP32 rows of width <= 16384 take the short-row
  *                   kernel unless cluster_size, stash_capacity, probe_stage or
  *                   split_rows > 0 is given); -1 never; 1 always (width <= 16384
  *                   and none of those options). In the short-row kernel

@@ -18,11 +18,11 @@ constexpr int kMaxDevices = 64;
 // the full stream, 8.1 against 14.7 us for one 16384-score row; shorter rows
 // have no room for the 4096-score sample).
 constexpr int kDefaultSampleMinN = 8192;
-// FP32 rows of at most this width take the short-row kernel by default. The
-// sweep measured the streaming kernel faster from width 16384 on (B = 1024
-// rows of 16384: 34 against 42 us), the short-row kernel faster at 8192 and
-// below (B = 1024 rows of 8192: 22 against 64 us).
-constexpr int64_t kShortAutoWidth = 8192;
+// FP32 rows of at most this width take the short-row kernel by default (its
+// whole range). On the dispatch sweep it is faster than the streaming kernel
+// at every width up to 16384 from a few hundred rows on: B = 2048 rows of
+// 80-100 % of 16384 at k = 2048, 67 against 80 us; of 8192, 34 against 123 us.
+constexpr int64_t kShortAutoWidth = 16384;
 // Default margin of the sampled rank, in standard deviations. At 5 a row
 // whose sampled cutoff lands above its k-th largest score (and is streamed
 // again) is a ~3e-7 event for the B=1024 workloads; 4 was 1.4 % faster on
@@ -298,8 +298,6 @@ topk_status select_impl(const void* scores, bool bf16, int64_t stride, const int
       p.ws_idx = p.ws_key + static_cast<size_t>(m) * 2 * static_cast<size_t>(k);
     }
   }
-
-  p.resident = kCtasPerSm * info->sm_count;
 
   const bool paged = page_table != nullptr;
   switch (kmax) {

@@ -148,7 +148,6 @@ struct Params {
   uint32_t* ws_cnt;      // per split row and half: entries handed over, or kHalfFailed
   uint32_t* ws_key;      // per split row and half: k keys ...
   uint32_t* ws_idx;      // ... and indices, in index order
-  int32_t resident;      // G == 1: CTAs resident at once, the most the persistent grid holds
 };
 
 // Cutoff description: an entry is selected if (key >> shift) > P, or if
@@ -452,33 +451,8 @@ __device__ void emit_rounds(SM& S, int n, Cut cut, uint32_t gt0, uint32_t eq0, S
   }
 }
 
-// One item of work: a whole row, one half of a split row, or (G > 1) this
-// CTA's slice of a row, with its geometry, its sampling decision and its
-// sample (loaded ahead of use).
-struct RowItem {
-  int row, part, parts;
-  bool split, trivial, sampled;
-  int n;            // valid length of the row
-  int h, nb, tail;  // scalar head up to 16-byte alignment, bulk body, scalar tail
-  int nstages, nfull, s0, s1, n_part;
-  int snb, sn;      // the sampled region's body length and score count
-  const float* rp;
-  const float* body;
-  const float* sbody;
-  uint32_t target;  // rank of the cutoff in the sample
-  float4 sx[4];     // this thread's sample scores
-  uint32_t smask;   // which of them exist
-};
-
 // PAGED: the output indices go through the page table (p.page_table is
 // not null); the ragged kernel carries no page-table code at all.
-//
-// With one CTA per row (G == 1) the kernel is persistent: the grid holds at
-// most as many CTAs as are resident at once, and CTA c takes items c, c +
-// gridDim.x, ...; the ring, its barriers and the histogram carry over from
-// item to item, and the next item's first ring stages and sample are loaded
-// while the current item finds its cutoff and writes its output. With
-// clusters (G > 1) every cluster takes one row.
 template <int KMAX, int G, bool PAGED>
 __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) {
   constexpr int C = StashCap<KMAX>::value;
@@ -486,111 +460,102 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
   Smem<C>& S = *reinterpret_cast<Smem<C>*>(smem_raw);
 
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
-  const uint32_t kk = static_cast<uint32_t>(p.k);
+  // The row, and which of its `parts` contiguous slices this CTA streams:
+  // the cluster rank for G > 1, the half of a split row, or the whole row.
+  int row, part = 0, parts = 1;
+  if constexpr (G > 1) {
+    row = static_cast<int>(blockIdx.x) / G;
+    part = static_cast<int>(cluster_ctarank());
+    parts = G;
+  } else if (static_cast<int>(blockIdx.x) < p.split_first) {
+    row = static_cast<int>(blockIdx.x);
+  } else {
+    const int q = static_cast<int>(blockIdx.x) - p.split_first;
+    row = p.split_first + (q >> 1);
+    part = q & 1;
+    parts = 2;
+  }
+  const int rank = (G > 1) ? part : 0;  // rank in the cluster
+  const bool split = (G == 1) && parts == 2;
+
+  const int64_t len_raw = p.lengths[row];
+  const int n = static_cast<int>(len_raw < 0 ? 0 : (len_raw > p.stride ? p.stride : len_raw));
+  int32_t* out_row = p.out + static_cast<int64_t>(row) * p.k;
+  const int32_t* pt_row = PAGED ? p.page_table + static_cast<int64_t>(row) * p.pt_stride : nullptr;
+  const bool leader = (t == 0 && part == 0);
+
+  // Read-only loads (the table is never written during the call), so the
+  // emission's lookups need not wait for its earlier output stores; a
+  // power-of-two page size maps with a shift and a mask.
+  auto map_index = [&](uint32_t i) -> int32_t {
+    if constexpr (!PAGED) return static_cast<int32_t>(i);
+    const uint32_t ps = static_cast<uint32_t>(p.page_size);
+    const uint32_t page = p.page_shift >= 0 ? (i >> p.page_shift) : i / ps;
+    return static_cast<int32_t>(static_cast<int64_t>(__ldg(pt_row + page)) * ps + (i - page * ps));
+  };
+
+  if (p.counters != nullptr && leader) {
+    atomicAdd(&p.counters[kCntRows], 1u);
+    if (G > 1) atomicAdd(&p.counters[kCntClusterRows], 1u);
+  }
+
+  // ---- rows with no more than k scores: every index is selected -----------
+  if (n <= p.k) {
+    if (split && part == 1) return;  // the first half writes the row
+    for (int j = rank * kThreads + t; j < p.k; j += kThreads * G)
+      out_row[j] = (j < n) ? map_index(static_cast<uint32_t>(j)) : -1;
+    if (p.counters != nullptr && leader) atomicAdd(&p.counters[kCntTrivial], 1u);
+    return;  // uniform over the cluster: no cluster barrier has been used yet
+  }
+  const uint32_t kk = static_cast<uint32_t>(p.k);  // n > k: exactly k slots are filled
   const uint32_t cap = static_cast<uint32_t>(p.cap);
 
-  // Items: rows [0, split_first) whole, then both halves of every split row.
-  const int n_items = G > 1 ? p.B : p.split_first + 2 * (p.B - p.split_first);
-  const int item_step = G > 1 ? p.B : static_cast<int>(gridDim.x);
-  int item = G > 1 ? static_cast<int>(blockIdx.x) / G : static_cast<int>(blockIdx.x);
+  // ---- row geometry: scalar head up to 16-byte alignment, bulk body, tail --
+  const float* rp = p.scores + static_cast<int64_t>(row) * p.stride;
+  const int mis = static_cast<int>((reinterpret_cast<uintptr_t>(rp) >> 2) & 3);
+  const int h = min((4 - mis) & 3, n);
+  const int nb = ((n - h) >> 2) << 2;
+  const int tail = n - h - nb;
+  const float* body = rp + h;
+  const int nstages = (nb + kStageFloats - 1) / kStageFloats;
+  const int nfull = nb / kStageFloats;  // stages of a full kStageFloats scores
+  const int lg_parts = __ffs(parts) - 1;  // parts is 1, 2, 4, 8 or 16
+  const int s0 = (nstages * part) >> lg_parts;
+  const int s1 = (nstages * (part + 1)) >> lg_parts;
+  // This part's scores: its stages of the body, plus the head / the tail.
+  const int b0 = s0 * kStageFloats, b1 = min(s1 * kStageFloats, nb);
+  const int n_part = (part == 0 ? h : 0) + (b1 - b0) + (part == parts - 1 ? tail : 0);
+  // The sampled region: the whole body for one CTA or a cluster (whose CTAs
+  // share one cutoff), this half's stages for a split row.
+  const float* sbody = split ? body + b0 : body;
+  const int snb = split ? b1 - b0 : nb;
+  const int sn = split ? n_part : n;
 
-  // Ring bookkeeping, over all items of the CTA. Stage j of a pass goes to
-  // slot (pass start + j - s0) % kStages; `consumed` (stages taken from the
-  // ring so far) is uniform. Thread 0 fills the ring at the start of a pass;
-  // afterwards the last warp to finish with a slot refills it with the stage
-  // kStages further on.
-  uint32_t consumed = 0, t0_seen = 0;
-  bool abort = false;
-
-  // One thread; the caller has made the slot's earlier shared-memory reads
-  // visible to the bulk copy (fence_proxy_async_smem).
-  auto issue_stage_of = [&](const float* body, int nb, int j, uint32_t slot) {
-    const int cnt = min(kStageFloats, nb - j * kStageFloats);
-    mbar_arrive_expect_tx(&S.full[slot], static_cast<uint32_t>(cnt) * 4u);
-    bulk_load(&S.ring[slot][0], body + static_cast<int64_t>(j) * kStageFloats,
-              static_cast<uint32_t>(cnt) * 4u, &S.full[slot]);
-  };
-  auto prime_of = [&](const RowItem& I) {
-    if (t == 0 && !abort) {
-      const int m = min(I.s1 - I.s0, kStages);
-      fence_proxy_async_smem();
-      for (int u = 0; u < m; ++u) issue_stage_of(I.body, I.nb, I.s0 + u, (consumed + u) % kStages);
-      S.issued += m;
-    }
-  };
-
-  // The item's row, which of its `parts` contiguous slices this CTA streams
-  // (the cluster rank for G > 1, the half of a split row, or the whole row),
-  // its geometry and its sampling decision.
-  auto make_item = [&](int it) -> RowItem {
-    RowItem I;
-    I.part = 0;
-    I.parts = 1;
-    if constexpr (G > 1) {
-      I.row = it;
-      I.part = static_cast<int>(cluster_ctarank());
-      I.parts = G;
-    } else if (it < p.split_first) {
-      I.row = it;
-    } else {
-      const int q = it - p.split_first;
-      I.row = p.split_first + (q >> 1);
-      I.part = q & 1;
-      I.parts = 2;
-    }
-    I.split = (G == 1) && I.parts == 2;
-    const int64_t len_raw = p.lengths[I.row];
-    I.n = static_cast<int>(len_raw < 0 ? 0 : (len_raw > p.stride ? p.stride : len_raw));
-    I.trivial = I.n <= p.k;
-    // ---- row geometry: scalar head up to 16-byte alignment, bulk body, tail --
-    I.rp = p.scores + static_cast<int64_t>(I.row) * p.stride;
-    const int mis = static_cast<int>((reinterpret_cast<uintptr_t>(I.rp) >> 2) & 3);
-    I.h = min((4 - mis) & 3, I.n);
-    I.nb = ((I.n - I.h) >> 2) << 2;
-    I.tail = I.n - I.h - I.nb;
-    I.body = I.rp + I.h;
-    I.nstages = (I.nb + kStageFloats - 1) / kStageFloats;
-    I.nfull = I.nb / kStageFloats;  // stages of a full kStageFloats scores
-    const int lg_parts = __ffs(I.parts) - 1;  // parts is 1, 2, 4, 8 or 16
-    I.s0 = (I.nstages * I.part) >> lg_parts;
-    I.s1 = (I.nstages * (I.part + 1)) >> lg_parts;
-    // This part's scores: its stages of the body, plus the head / the tail.
-    const int b0 = I.s0 * kStageFloats, b1 = min(I.s1 * kStageFloats, I.nb);
-    I.n_part = (I.part == 0 ? I.h : 0) + (b1 - b0) + (I.part == I.parts - 1 ? I.tail : 0);
-    // The sampled region: the whole body for one CTA or a cluster (whose CTAs
-    // share one cutoff), this half's stages for a split row.
-    I.sbody = I.split ? I.body + b0 : I.body;
-    I.snb = I.split ? b1 - b0 : I.nb;
-    I.sn = I.split ? I.n_part : I.n;
-    // ---- sampled cutoff: the decision ------------------------------------------
-    I.sampled = false;
-    I.target = 0;
-    const bool long_enough = I.snb >= 2 * 4 * kSampleVec4;
-    const bool want = !I.trivial && long_enough &&
-                      (p.sample_mode == 2 || (p.sample_mode == 0 && I.sn >= p.sample_min_n));
+  // ---- sampled cutoff: decision and sample loads (issued first, and only
+  // consumed after the ring setup, so that their latency overlaps it) ---------
+  uint32_t thr = 0;
+  bool sampled = false;
+  uint32_t target = 0;
+  float4 sx[4];
+  uint32_t smask = 0;
+  {
+    const bool long_enough = snb >= 2 * 4 * kSampleVec4;
+    const bool want = long_enough && (p.sample_mode == 2 || (p.sample_mode == 0 && sn >= p.sample_min_n));
     if (want) {
-      const float mu = static_cast<float>(kk) * (4.0f * kSampleVec4) * __frcp_rn(static_cast<float>(I.sn));
+      const float mu = static_cast<float>(kk) * (4.0f * kSampleVec4) * __frcp_rn(static_cast<float>(sn));
       float rf = ceilf(mu + p.sample_z * sqrtf(mu)) + 1.0f;
       rf = fmaxf(rf, 1.0f);
       if (rf < 4.0f * kSampleVec4) {
-        I.sampled = true;
-        I.target = static_cast<uint32_t>(rf);
+        sampled = true;
+        target = static_cast<uint32_t>(rf);
       }
     }
 #pragma unroll
-    for (int v = 0; v < 4; ++v) I.sx[v] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    I.smask = 0;
-    return I;
-  };
-  // The item's sample loads (consumed after the ring set-up, so that their
-  // latency overlaps it) and its first ring stages.
-  auto start_item = [&](RowItem& I) {
-    if (I.trivial) return;
-    if (I.sampled) {
-      const int nb4 = I.snb >> 2;
+    for (int v = 0; v < 4; ++v) sx[v] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if (sampled) {
+      const int nb4 = snb >> 2;
       const int step4 = (nb4 - kSampleChunkVec4) / (kSampleChunks - 1);  // float4s between chunk starts
       constexpr int per_rank = kSampleVec4 / G;
-      const int rank = (G > 1) ? I.part : 0;
 #pragma unroll
       for (int v = 0; v < 4; ++v) {
         const int f = t + v * kThreads;
@@ -598,14 +563,55 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
           const int gf = rank * per_rank + f;
           const int chunk = gf / kSampleChunkVec4, within = gf % kSampleChunkVec4;
           const int off4 = chunk * step4 + within;
-          I.sx[v] = __ldg(reinterpret_cast<const float4*>(I.sbody) + off4);
-          I.smask |= 0xfu << (4 * v);
+          sx[v] = __ldg(reinterpret_cast<const float4*>(sbody) + off4);
+          smask |= 0xfu << (4 * v);
         }
       }
     }
-    prime_of(I);
-  };
+  }
 
+  // Ring bookkeeping. Stage j of a pass goes to slot (pass start + j - s0) %
+  // kStages; `consumed` (stages taken from the ring so far) is uniform.
+  // Thread 0 fills the ring at the start of a pass; afterwards the last warp
+  // to finish with a slot refills it with the stage kStages further on.
+  uint32_t consumed = 0, t0_seen = 0;
+  bool abort = false;
+
+  // One thread; the caller has made the slot's earlier shared-memory reads
+  // visible to the bulk copy (fence_proxy_async_smem).
+  auto issue_stage = [&](int j, uint32_t slot) {
+    const int cnt = min(kStageFloats, nb - j * kStageFloats);
+    mbar_arrive_expect_tx(&S.full[slot], static_cast<uint32_t>(cnt) * 4u);
+    bulk_load(&S.ring[slot][0], body + static_cast<int64_t>(j) * kStageFloats,
+              static_cast<uint32_t>(cnt) * 4u, &S.full[slot]);
+  };
+  auto prime = [&]() {
+    if (t == 0 && !abort) {
+      const int m = min(s1 - s0, kStages);
+      fence_proxy_async_smem();
+      for (int u = 0; u < m; ++u) issue_stage(s0 + u, (consumed + u) % kStages);
+      S.issued += m;
+    }
+  };
+  // Called by every thread once it no longer reads ring slot `slot` (stage
+  // j) nor, when `two`, the next slot (stage j + 1). The last warp refills
+  // both with the stages kStages further on.
+  auto release_slots = [&](int j, uint32_t slot, bool two) {
+    __syncwarp();
+    if (lane == 0 && atom_add_acq_rel_cta(&S.rel[slot], 1u) == kWarps - 1) {
+      S.rel[slot] = 0;
+      if (!abort && j + kStages < s1) {
+        fence_proxy_async_smem();
+        issue_stage(j + kStages, slot);
+        uint32_t m = 1;
+        if (two && j + 1 + kStages < s1) {
+          issue_stage(j + 1 + kStages, (slot + 1) % kStages);
+          ++m;
+        }
+        atomicAdd(&S.issued, m);
+      }
+    }
+  };
   if (t == 0) {
 #pragma unroll
     for (int s = 0; s < kStages; ++s) {
@@ -616,8 +622,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
     S.issued = 0;
     fence_mbar_init();
   }
-  RowItem cur = make_item(item);
-  start_item(cur);  // the first stages are in flight during the setup and the sample passes
+  prime();  // the first stages are in flight during the setup and the sample passes
   for (int i = t; i < kBins; i += kThreads) S.hist[i] = 0;
   __syncthreads();
   // In a cluster, every CTA's histogram increments go to rank 0's histogram,
@@ -625,535 +630,443 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
   HistDst<G> hdst{0u, true};
   if constexpr (G > 1) {
     hdst.h0 = map_rank(smem_addr(&S.hist[0]), 0);
-    hdst.local = cur.part == 0;
+    hdst.local = rank == 0;
     cluster_sync();
   }
 
-  RowItem nxt;
-  bool nxt_started = false;
-
-  // One item, from its sample passes to its output (returns at its end).
-  auto run_item = [&](const RowItem& I, int next_it) {
-    const int row = I.row, part = I.part, parts = I.parts;
-    const bool split = I.split;
-    const int rank = (G > 1) ? part : 0;  // rank in the cluster
-    const int n = I.n, h = I.h, nb = I.nb, tail = I.tail;
-    const int nfull = I.nfull, s0 = I.s0, s1 = I.s1, n_part = I.n_part;
-    const float* rp = I.rp;
-    const bool sampled = I.sampled;
-    const uint32_t target = I.target;
-    int32_t* out_row = p.out + static_cast<int64_t>(row) * p.k;
-    const int32_t* pt_row = PAGED ? p.page_table + static_cast<int64_t>(row) * p.pt_stride : nullptr;
-    const bool leader = (t == 0 && part == 0);
-
-    // Read-only loads (the table is never written during the call), so the
-    // emission's lookups need not wait for its earlier output stores; a
-    // power-of-two page size maps with a shift and a mask.
-    auto map_index = [&](uint32_t i) -> int32_t {
-      if constexpr (!PAGED) return static_cast<int32_t>(i);
-      const uint32_t ps = static_cast<uint32_t>(p.page_size);
-      const uint32_t page = p.page_shift >= 0 ? (i >> p.page_shift) : i / ps;
-      return static_cast<int32_t>(static_cast<int64_t>(__ldg(pt_row + page)) * ps + (i - page * ps));
-    };
-
-    if (p.counters != nullptr && leader) {
-      atomicAdd(&p.counters[kCntRows], 1u);
-      if (G > 1) atomicAdd(&p.counters[kCntClusterRows], 1u);
+  // ---- sampled cutoff: two 11-bit radix passes over the sample ---------------
+  if (sampled) {
+    uint32_t above, inbin;
+    uint32_t sk[16];
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      sk[4 * v + 0] = order_key(sx[v].x);
+      sk[4 * v + 1] = order_key(sx[v].y);
+      sk[4 * v + 2] = order_key(sx[v].z);
+      sk[4 * v + 3] = order_key(sx[v].w);
     }
-
-    // ---- rows with no more than k scores: every index is selected -----------
-    if (I.trivial) {
-      if (split && part == 1) return;  // the first half writes the row
-      for (int j = rank * kThreads + t; j < p.k; j += kThreads * G)
-        out_row[j] = (j < n) ? map_index(static_cast<uint32_t>(j)) : -1;
-      if (p.counters != nullptr && leader) atomicAdd(&p.counters[kCntTrivial], 1u);
-      return;  // uniform over the cluster: no cluster barrier has been used yet
+#pragma unroll
+    for (int i = 0; i < 16; ++i) hist_inc<G>(S.hist, hdst, ((smask >> i) & 1u) ? (sk[i] >> 21) : 0xffffffffu);
+    const uint32_t b1 = merged_find<G, 8>(S, target, &above, &inbin, hdst.local);
+    const uint32_t rem = target - above;
+    if (rem == inbin) {
+      thr = b1 << 21;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const bool ok = ((smask >> i) & 1u) && (sk[i] >> 21) == b1;
+        hist_inc<G>(S.hist, hdst, ok ? ((sk[i] >> 10) & 0x7ffu) : 0xffffffffu);
+      }
+      const uint32_t b2 = merged_find<G, 8>(S, rem, &above, &inbin, hdst.local);
+      thr = (b1 << 21) | (b2 << 10);
     }
+  }
 
-    auto issue_stage = [&](int j, uint32_t slot) { issue_stage_of(I.body, nb, j, slot); };
-    auto prime = [&]() { prime_of(I); };
-    // Called by every thread once it no longer reads ring slot `slot` (stage
-    // j) nor, when `two`, the next slot (stage j + 1). The last warp refills
-    // both with the stages kStages further on.
-    auto release_slots = [&](int j, uint32_t slot, bool two) {
-      __syncwarp();
-      if (lane == 0 && atom_add_acq_rel_cta(&S.rel[slot], 1u) == kWarps - 1) {
-        S.rel[slot] = 0;
-        if (!abort && j + kStages < s1) {
-          fence_proxy_async_smem();
-          issue_stage(j + kStages, slot);
-          uint32_t m = 1;
-          if (two && j + 1 + kStages < s1) {
-            issue_stage(j + 1 + kStages, (slot + 1) % kStages);
-            ++m;
-          }
-          atomicAdd(&S.issued, m);
-        }
+  // ---- streaming filter into the stash --------------------------------------
+  uint32_t n_st = 0;        // stash entries (uniform)
+  uint32_t grp = 0;         // groups processed (uniform), selects the count table half
+  uint32_t compactions = 0;
+  float bound = float_bound(thr);
+
+  auto compact = [&]() {
+    const Cut cut = select_stash<1>(S, static_cast<int>(n_st), kk);
+    emit_rounds(S, static_cast<int>(n_st), cut, 0u, 0u, [&](bool sel, uint32_t pos, uint32_t key, uint32_t idx) {
+      if (sel && pos < kk) {  // exactly kk entries are selected; the guard only bounds a corrupted cut
+        S.skey[pos] = key;
+        S.sidx[pos] = idx;
       }
-    };
-    uint32_t thr = 0;
-    // ---- sampled cutoff: two 11-bit radix passes over the sample ---------------
-    if (sampled) {
-      uint32_t above, inbin;
-      uint32_t sk[16];
+    });
+    __syncthreads();
+    n_st = kk;
+    thr = max(thr, (cut.P << cut.shift) + 1u);
+    bound = float_bound(thr);
+    ++compactions;
+  };
+
+  // Exact hit mask: bit e set when score e of this thread's group (index
+  // order) has a key >= thr. `bound` is the float whose key is thr, so a float
+  // comparison is exact unless bound is a zero, where -0 < +0 must come from
+  // the keys.
+  auto hit_mask = [&](const float4 (&v)[4], int rot, uint32_t valid) -> uint32_t {
+    uint32_t pl = 0;  // in load order: v[j] at bits 4j .. 4j + 3
+    if (bound != 0.0f) {
 #pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        sk[4 * v + 0] = order_key(I.sx[v].x);
-        sk[4 * v + 1] = order_key(I.sx[v].y);
-        sk[4 * v + 2] = order_key(I.sx[v].z);
-        sk[4 * v + 3] = order_key(I.sx[v].w);
+      for (int j = 0; j < 4; ++j) {
+        pl |= (static_cast<uint32_t>(v[j].x >= bound) | (static_cast<uint32_t>(v[j].y >= bound) << 1) |
+               (static_cast<uint32_t>(v[j].z >= bound) << 2) | (static_cast<uint32_t>(v[j].w >= bound) << 3))
+              << (4 * j);
       }
+    } else {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) hist_inc<G>(S.hist, hdst, ((I.smask >> i) & 1u) ? (sk[i] >> 21) : 0xffffffffu);
-      const uint32_t b1 = merged_find<G, 8>(S, target, &above, &inbin, hdst.local);
-      const uint32_t rem = target - above;
-      if (rem == inbin) {
-        thr = b1 << 21;
-      } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const bool ok = ((I.smask >> i) & 1u) && (sk[i] >> 21) == b1;
-          hist_inc<G>(S.hist, hdst, ok ? ((sk[i] >> 10) & 0x7ffu) : 0xffffffffu);
-        }
-        const uint32_t b2 = merged_find<G, 8>(S, rem, &above, &inbin, hdst.local);
-        thr = (b1 << 21) | (b2 << 10);
+      for (int j = 0; j < 4; ++j) {
+        pl |= (static_cast<uint32_t>(order_key(v[j].x) >= thr) |
+               (static_cast<uint32_t>(order_key(v[j].y) >= thr) << 1) |
+               (static_cast<uint32_t>(order_key(v[j].z) >= thr) << 2) |
+               (static_cast<uint32_t>(order_key(v[j].w) >= thr) << 3))
+              << (4 * j);
       }
     }
+    // v[j] holds the scores 4 * ((j + rot) & 3) ..: rotate the 16 bits left by 4 * rot
+    const uint32_t pl2 = pl | (pl << 16);
+    return (pl2 >> (16 - 4 * rot)) & valid;
+  };
 
-    // ---- streaming filter into the stash --------------------------------------
-    uint32_t n_st = 0;        // stash entries (uniform)
-    uint32_t grp = 0;         // groups processed (uniform), selects the count table half
-    uint32_t compactions = 0;
-    float bound = float_bound(thr);
-
-    auto compact = [&]() {
-      const Cut cut = select_stash<1>(S, static_cast<int>(n_st), kk);
-      emit_rounds(S, static_cast<int>(n_st), cut, 0u, 0u, [&](bool sel, uint32_t pos, uint32_t key, uint32_t idx) {
-        if (sel && pos < kk) {  // exactly kk entries are selected; the guard only bounds a corrupted cut
-          S.skey[pos] = key;
-          S.sidx[pos] = idx;
-        }
-      });
-      __syncthreads();
-      n_st = kk;
-      thr = max(thr, (cut.P << cut.shift) + 1u);
-      bound = float_bound(thr);
-      ++compactions;
-    };
-
-    // Exact hit mask: bit e set when score e of this thread's group (index
-    // order) has a key >= thr. `bound` is the float whose key is thr, so a float
-    // comparison is exact unless bound is a zero, where -0 < +0 must come from
-    // the keys.
-    auto hit_mask = [&](const float4 (&v)[4], int rot, uint32_t valid) -> uint32_t {
-      uint32_t pl = 0;  // in load order: v[j] at bits 4j .. 4j + 3
-      if (bound != 0.0f) {
+  // Hit mask of this thread's 16 scores of a ring stage (ts points at them;
+  // scores past the stage's end are stale and masked off by `valid`). The
+  // float4 reads are rotated by `rot` so that they are bank-conflict free.
+  // (No per-thread maximum is tested first: in a warp of 512 scores some
+  // lane nearly always passes, so such a prefilter only added work.)
+  // A scalar group (ts == nullptr) has one score, sx, present when bit 0 of
+  // `valid` is set.
+  auto group_mask = [&](const float* ts, float sx, int rot, uint32_t valid) -> uint32_t {
+    if (ts == nullptr) return ((valid & 1u) != 0u && order_key(sx) >= thr) ? 1u : 0u;
+    float4 v[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          pl |= (static_cast<uint32_t>(v[j].x >= bound) | (static_cast<uint32_t>(v[j].y >= bound) << 1) |
-                 (static_cast<uint32_t>(v[j].z >= bound) << 2) | (static_cast<uint32_t>(v[j].w >= bound) << 3))
-                << (4 * j);
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          pl |= (static_cast<uint32_t>(order_key(v[j].x) >= thr) |
-                 (static_cast<uint32_t>(order_key(v[j].y) >= thr) << 1) |
-                 (static_cast<uint32_t>(order_key(v[j].z) >= thr) << 2) |
-                 (static_cast<uint32_t>(order_key(v[j].w) >= thr) << 3))
-                << (4 * j);
-        }
-      }
-      // v[j] holds the scores 4 * ((j + rot) & 3) ..: rotate the 16 bits left by 4 * rot
-      const uint32_t pl2 = pl | (pl << 16);
-      return (pl2 >> (16 - 4 * rot)) & valid;
-    };
+    for (int jj = 0; jj < 4; ++jj) v[jj] = *reinterpret_cast<const float4*>(ts + 4 * ((jj + rot) & 3));
+    return hit_mask(v, rot, valid);
+  };
 
-    // Hit mask of this thread's 16 scores of a ring stage (ts points at them;
-    // scores past the stage's end are stale and masked off by `valid`). The
-    // float4 reads are rotated by `rot` so that they are bank-conflict free.
-    // (No per-thread maximum is tested first: in a warp of 512 scores some
-    // lane nearly always passes, so such a prefilter only added work.)
-    // A scalar group (ts == nullptr) has one score, sx, present when bit 0 of
-    // `valid` is set.
-    auto group_mask = [&](const float* ts, float sx, int rot, uint32_t valid) -> uint32_t {
-      if (ts == nullptr) return ((valid & 1u) != 0u && order_key(sx) >= thr) ? 1u : 0u;
-      float4 v[4];
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) v[jj] = *reinterpret_cast<const float4*>(ts + 4 * ((jj + rot) & 3));
-      return hit_mask(v, rot, valid);
-    };
+  // Base (lower warps) and total of the packed per-warp counts in table half `par`.
+  auto read_table = [&](int par, uint32_t& base, uint32_t& total) {
+    const uint32_t e = lane < kWarps ? S.tab[par][lane] : 0u;  // lane i: warp i's word
+    base = __reduce_add_sync(0xffffffffu, lane < w ? e : 0u);
+    total = __reduce_add_sync(0xffffffffu, e);
+  };
 
-    // Base (lower warps) and total of the packed per-warp counts in table half `par`.
-    auto read_table = [&](int par, uint32_t& base, uint32_t& total) {
-      const uint32_t e = lane < kWarps ? S.tab[par][lane] : 0u;  // lane i: warp i's word
-      base = __reduce_add_sync(0xffffffffu, lane < w ? e : 0u);
-      total = __reduce_add_sync(0xffffffffu, e);
-    };
+  // Publishes this warp's packed count and error flag and synchronises the
+  // CTA. Returns this lane's inclusive packed count in the warp, and the
+  // packed counts of the lower warps (base) and of all warps (total).
+  auto publish = [&](uint32_t cnt, bool err, uint32_t& incl, uint32_t& base, uint32_t& total) {
+    const uint32_t wtot = __reduce_add_sync(0xffffffffu, cnt);  // off the scan's critical path
+    incl = warp_incl_scan(cnt);
+    const bool werr = __any_sync(0xffffffffu, err);
+    const int par = static_cast<int>(grp & 1u);
+    ++grp;
+    if (lane == 0) S.tab[par][w] = wtot + (werr ? kErrUnit : 0u);
+    __syncthreads();
+    read_table(par, base, total);
+  };
 
-    // Publishes this warp's packed count and error flag and synchronises the
-    // CTA. Returns this lane's inclusive packed count in the warp, and the
-    // packed counts of the lower warps (base) and of all warps (total).
-    auto publish = [&](uint32_t cnt, bool err, uint32_t& incl, uint32_t& base, uint32_t& total) {
-      const uint32_t wtot = __reduce_add_sync(0xffffffffu, cnt);  // off the scan's critical path
-      incl = warp_incl_scan(cnt);
-      const bool werr = __any_sync(0xffffffffu, err);
-      const int par = static_cast<int>(grp & 1u);
-      ++grp;
-      if (lane == 0) S.tab[par][w] = wtot + (werr ? kErrUnit : 0u);
-      __syncthreads();
-      read_table(par, base, total);
-    };
-
-    // Appends this lane's hits (bits of m, in index order) from stash position
-    // pos on; score e is ts[e] (or sx for a scalar group), its index idx0 + e.
-    auto write_hits = [&](uint32_t m, uint32_t pos, const float* ts, float sx, uint32_t idx0) {
-      while (m != 0u) {  // two at a time
-        const int e0 = __ffs(m) - 1;
-        m &= m - 1u;
-        const bool two = m != 0u;
-        const int e1 = two ? __ffs(m) - 1 : e0;
-        if (two) m &= m - 1u;
-        const float x0 = ts != nullptr ? ts[e0] : sx;
-        const float x1 = ts != nullptr ? ts[e1] : sx;
-        const uint32_t k0 = order_key(x0), k1 = order_key(x1);
-        S.skey[pos] = k0;
-        S.sidx[pos] = idx0 + e0;
+  // Appends this lane's hits (bits of m, in index order) from stash position
+  // pos on; score e is ts[e] (or sx for a scalar group), its index idx0 + e.
+  auto write_hits = [&](uint32_t m, uint32_t pos, const float* ts, float sx, uint32_t idx0) {
+    while (m != 0u) {  // two at a time
+      const int e0 = __ffs(m) - 1;
+      m &= m - 1u;
+      const bool two = m != 0u;
+      const int e1 = two ? __ffs(m) - 1 : e0;
+      if (two) m &= m - 1u;
+      const float x0 = ts != nullptr ? ts[e0] : sx;
+      const float x1 = ts != nullptr ? ts[e1] : sx;
+      const uint32_t k0 = order_key(x0), k1 = order_key(x1);
+      S.skey[pos] = k0;
+      S.sidx[pos] = idx0 + e0;
+      ++pos;
+      if (two) {
+        S.skey[pos] = k1;
+        S.sidx[pos] = idx0 + e1;
         ++pos;
-        if (two) {
-          S.skey[pos] = k1;
-          S.sidx[pos] = idx0 + e1;
-          ++pos;
-        }
       }
-    };
-
-    // One group: two consecutive ring stages A and B (B absent when tsB is
-    // null), or one scalar group as A. Thread t's 16 scores of stage A start at
-    // tsA and have indices idxA + e (present where bit e of validA is set);
-    // likewise for B. Hits of A precede those of B in the stash, each in index
-    // order, so the stash stays in index order. One block barrier per group
-    // (more only when the stash must be compacted). Every thread of the CTA
-    // calls it.
-    auto process_group = [&](const float* tsA, const float* tsB, float sx, int rot, uint32_t validA,
-                             uint32_t validB, uint32_t idxA, uint32_t idxB, bool err) {
-      uint32_t pmA = group_mask(tsA, sx, rot, validA);
-      uint32_t pmB = tsB != nullptr ? group_mask(tsB, sx, rot, validB) : 0u;
-      uint32_t cnt = __popc(pmA) + (static_cast<uint32_t>(__popc(pmB)) << kFieldB);
-      uint32_t incl, base, total;
-      publish(cnt, err, incl, base, total);
-      if ((total & kErrMask) != 0u) abort = true;
-      if (abort) return;  // uniform
-      uint32_t tA = total & kFieldMask, tB = (total >> kFieldB) & kFieldMask;
-      if (tA + tB == 0u) return;  // uniform
-      if (n_st + tA + tB > cap) {
-        if (n_st > kk) {  // keep the exact top-k so far and raise the cutoff
-          compact();
-          pmA = group_mask(tsA, sx, rot, validA);
-          pmB = tsB != nullptr ? group_mask(tsB, sx, rot, validB) : 0u;
-          cnt = __popc(pmA) + (static_cast<uint32_t>(__popc(pmB)) << kFieldB);
-          publish(cnt, false, incl, base, total);
-          tA = total & kFieldMask;
-          tB = (total >> kFieldB) & kFieldMask;
-        }
-        if (n_st + tA + tB > cap) {
-          // More hits than the stash has room for, even above a raised cutoff.
-          // Quarters of the group (half the CTA on one stage, at most
-          // kMinStashRoom hits each) append in index order, compacting in
-          // between (a quarter overflows only when the stash holds more than
-          // k entries).
-          for (int part = 0; part < 4; ++part) {
-            const bool second = part >= 2;
-            if (second && tsB == nullptr) break;  // uniform
-            const bool mine = (w >> 2) == (part & 1);
-            const float* ts = second ? tsB : tsA;
-            const uint32_t valid = second ? validB : validA;
-            uint32_t pm = mine ? group_mask(ts, sx, rot, valid) : 0u;
-            uint32_t c = __popc(pm);
-            publish(c, false, incl, base, total);
-            if (n_st + (total & kFieldMask) > cap) {
-              compact();
-              pm = mine ? group_mask(ts, sx, rot, valid) : 0u;
-              c = __popc(pm);
-              publish(c, false, incl, base, total);
-            }
-            write_hits(pm, n_st + (base & kFieldMask) + incl - c, ts, sx, second ? idxB : idxA);
-            n_st += total & kFieldMask;
-          }
-          return;
-        }
-      }
-      const uint32_t before = incl - cnt;  // packed hits of the lower lanes of this warp
-      write_hits(pmA, n_st + (base & kFieldMask) + (before & kFieldMask), tsA, sx, idxA);
-      write_hits(pmB, n_st + tA + ((base >> kFieldB) & kFieldMask) + ((before >> kFieldB) & kFieldMask),
-                 tsB, sx, idxB);
-      n_st += tA + tB;
-    };
-
-    // Scalar group: thread t < cnt holds the score at index first + t.
-    auto scalar_group = [&](int first, int cnt) {
-      float sx = 0.0f;
-      uint32_t valid = 0;
-      if (t < cnt) {
-        sx = rp[first + t];
-        valid = 1u;
-      }
-      process_group(nullptr, nullptr, sx, 0, valid, 0u, static_cast<uint32_t>(first + t), 0u, false);
-    };
-
-    // Takes stage j from the ring: waits for it (bounded) and returns this
-    // thread's 16 scores in it, with the mask of those present.
-    const bool probing = p.probe_stage >= 0;  // test only
-    auto take_stage = [&](int j, bool& err, uint32_t& valid, uint32_t& slot) -> const float* {
-      slot = consumed % kStages;
-      const uint32_t parity = (consumed / kStages) & 1u;
-      ++consumed;
-      if (!abort) {
-        if (probing && j - s0 == p.probe_stage) {
-          err |= !mbar_wait_bounded(&S.never, 0u, 1000ull * p.probe_wait_us);  // runs out
-        } else if (mbar_wait_bounded(&S.full[slot], parity, kWaitLimitNs)) {
-          ++t0_seen;  // in order: stages [t0_seen, issued) are unobserved
-        } else {
-          err = true;
-        }
-      }
-      if (j < nfull) {
-        valid = 0xffffu;
-      } else {  // the last, partial stage
-        const int have = (nb - j * kStageFloats) - kPerThread * t;
-        valid = have >= kPerThread ? 0xffffu : (have <= 0 ? 0u : (1u << have) - 1u);
-      }
-      return &S.ring[slot][kPerThread * t];
-    };
-
-    auto stream_pass = [&]() {
-      const int rot = (t >> 1) & 3;  // rotates the float4 order: conflict-free shared loads
-      if (part == 0 && h > 0) scalar_group(0, h);
-      for (int j = s0; j < s1; j += 2) {
-        const bool two = j + 1 < s1;
-        bool err = false;
-        uint32_t validA, validB = 0, slotA, slotB;
-        const float* tsA = take_stage(j, err, validA, slotA);
-        const float* tsB = two ? take_stage(j + 1, err, validB, slotB) : nullptr;
-        const uint32_t idxA = static_cast<uint32_t>(h + j * kStageFloats + kPerThread * t);
-        process_group(tsA, tsB, 0.0f, rot, validA, validB, idxA, idxA + kStageFloats, err);
-        release_slots(j, slotA, two);
-      }
-      if (part == parts - 1 && tail > 0) scalar_group(h + nb, tail);
-    };
-
-    stream_pass();
-
-    // ---- underflow: the sampled cutoff kept fewer than k candidates -----------
-    // (fewer than min(k, its scores) for the half of a split row)
-    const uint32_t need = split ? min(kk, static_cast<uint32_t>(n_part)) : kk;
-    if (sampled) {
-      uint32_t total = n_st;
-      if constexpr (G > 1) {
-        if (t == 0) S.pub[0] = n_st;
-        cluster_sync();
-        if (w == 0) {  // lane r reads rank r's count
-          uint32_t v = lane < G ? ld_dsmem_u32(map_rank(smem_addr(&S.pub[0]), lane)) : 0u;
-          v = __reduce_add_sync(0xffffffffu, v);
-          if (lane == 0) S.res[3] = v;
-        }
-        cluster_sync();  // every CTA has read every count; S.res[3] is visible
-        total = S.res[3];
-      }
-      if (total < need) {  // uniform over the cluster
-        if (p.counters != nullptr && t == 0 && rank == 0) atomicAdd(&p.counters[kCntRescan], 1u);
-        thr = 0;
-        bound = float_bound(thr);
-        n_st = 0;
-        __syncthreads();  // (the histogram is zero: every search leaves it so)
-        prime();
-        stream_pass();
-      }
-    }
-
-    // ---- the next item's prologue, overlapped with this one's epilogue ----------
-    // Every warp is done with the ring: the next item's first stages and its
-    // sample loads are issued now, and land while this item finds its cutoff
-    // and writes its output.
-    if constexpr (G == 1) {
-      if (!abort && next_it < n_items) {
-        __syncthreads();
-        nxt = make_item(next_it);
-        start_item(nxt);
-        nxt_started = true;
-      }
-    }
-
-    // A wait timed out: let copies still in flight land (bounded) before the
-    // CTA moves on or leaves, so that no bulk copy writes into shared memory
-    // that is no longer its stage's.
-    auto drain = [&]() {
-      if (abort && t == 0) {
-        for (uint32_t u = t0_seen; u < S.issued; ++u)
-          (void)mbar_wait_bounded(&S.full[u % kStages], (u / kStages) & 1u, kWaitLimitNs);
-        t0_seen = S.issued;  // every copy issued has landed (or will never be waited for again)
-        if (p.counters != nullptr) atomicAdd(&p.counters[kCntDeviceErrors], 1u);
-      }
-    };
-    auto poison_row = [&]() {  // marks the row as failed: no result can be mistaken for one
-      for (int j = t; j < p.k; j += kThreads) out_row[j] = static_cast<int32_t>(0x80000000u);
-    };
-
-    if (split) {
-      // ---- split row: this half's exact top-k goes to the workspace; the half
-      // that finishes second merges both (no CTA ever waits for another) -------
-      const int slot = row - p.split_first;
-      const size_t off = static_cast<size_t>(2 * slot + part) * kk;
-      uint32_t handed = 0;
-      if (!abort) {
-        if (n_st > need) {
-          const Cut c = select_stash<1>(S, static_cast<int>(n_st), need);
-          emit_rounds(S, static_cast<int>(n_st), c, 0u, 0u, [&](bool sel, uint32_t pos, uint32_t key, uint32_t idx) {
-            if (sel && pos < need) {
-              p.ws_key[off + pos] = key;
-              p.ws_idx[off + pos] = idx;
-            }
-          });
-          handed = need;
-        } else {
-          for (int e = t; e < static_cast<int>(n_st); e += kThreads) {
-            p.ws_key[off + e] = S.skey[e];
-            p.ws_idx[off + e] = S.sidx[e];
-          }
-          handed = n_st;
-        }
-      }
-      drain();
-      if (p.counters != nullptr && t == 0) {
-        if (compactions) atomicAdd(&p.counters[kCntCompactions], compactions);
-        if (part == 0 && sampled) atomicAdd(&p.counters[kCntSampled], 1u);
-      }
-      if (t == 0) p.ws_cnt[2 * slot + part] = abort ? kHalfFailed : handed;
-      __threadfence();  // the hand-over is visible before the arrival is counted
-      __syncthreads();
-      if (t == 0) S.res[3] = atomicAdd(&p.ws_ctr[slot], 1u);
-      __syncthreads();
-      if (S.res[3] == 0u) return;  // first to finish: the other half merges
-      __threadfence();
-      if (t == 0) p.ws_ctr[slot] = 0u;  // both halves have arrived: ready for the next call
-      const uint32_t c0 = __ldcg(&p.ws_cnt[2 * slot]), c1 = __ldcg(&p.ws_cnt[2 * slot + 1]);
-      if (c0 == kHalfFailed || c1 == kHalfFailed) {
-        poison_row();
-        return;
-      }
-      if (PAGED) {  // as below, for the whole row
-        const int p1 = (n + p.page_size - 1) / p.page_size;
-        for (int q = 32 * t; q < p1; q += 32 * kThreads) prefetch_l2(pt_row + q);
-        if (t == 0) prefetch_l2(pt_row + p1 - 1);
-      }
-      for (int i = t; i < kBins; i += kThreads) S.hist[i] = 0;
-      __syncthreads();  // the local emission has read the stash; the histogram is clear
-      // Half 0's entries precede half 1's: the merged stash is in index order.
-      const size_t base0 = static_cast<size_t>(2 * slot) * kk;
-      for (int e = t; e < static_cast<int>(c0 + c1); e += kThreads) {
-        const size_t src = static_cast<uint32_t>(e) < c0 ? base0 + e : base0 + kk + (e - c0);
-        const uint32_t key = __ldcg(&p.ws_key[src]);
-        S.skey[e] = key;
-        S.sidx[e] = __ldcg(&p.ws_idx[src]);
-      }
-      const Cut c = select_stash<1>(S, static_cast<int>(c0 + c1), kk);
-      emit_rounds(S, static_cast<int>(c0 + c1), c, 0u, 0u, [&](bool sel, uint32_t pos, uint32_t, uint32_t idx) {
-        const int32_t v = map_index(idx);
-        if (sel && pos < kk) out_row[pos] = v;
-      });
-      if (p.counters != nullptr && t == 0) atomicAdd(&p.counters[kCntSplitRows], 1u);
-      return;
-    }
-
-    if constexpr (G == 1) {
-      if (abort) {  // uniform: nothing is selected from an incomplete stash, and
-        drain();    // the poison is the only store this CTA makes to its row
-        poison_row();
-        return;
-      }
-    }
-
-    // ---- exact cutoff over the stash(es) and emission --------------------------
-    if (PAGED && !abort) {
-      // The emission maps every selected index through the page table: start
-      // bringing this CTA's part of the table row into L2 while the cutoff is
-      // found (one line per 32 entries).
-      const int first = rank == 0 ? 0 : h + s0 * kStageFloats;
-      const int last = rank == G - 1 ? n : h + s1 * kStageFloats;
-      const int p0 = first / p.page_size, p1 = (last + p.page_size - 1) / p.page_size;
-      for (int q = p0 + 32 * t; q < p1; q += 32 * kThreads) prefetch_l2(pt_row + q);
-      if (t == 0 && p1 > p0) prefetch_l2(pt_row + p1 - 1);  // the last line, if no start fell in it
-    }
-    const Cut cut = select_stash<G>(S, static_cast<int>(n_st), kk, hdst);
-    uint32_t gt0 = 0, eq0 = 0;
-    if constexpr (G > 1) {
-      // Entries above / at the cutoff in this CTA's stash; lower ranks come first.
-      if (t == 0) {
-        S.pub[1] = 0;
-        S.pub[2] = 0;
-      }
-      __syncthreads();
-      uint32_t lg = 0, le = 0;
-      for (int e = t; e < static_cast<int>(n_st); e += kThreads) {
-        const uint32_t hi = S.skey[e] >> cut.shift;
-        lg += hi > cut.P;
-        le += hi == cut.P;
-      }
-      for (int d = 16; d > 0; d >>= 1) {
-        lg += __shfl_xor_sync(0xffffffffu, lg, d);
-        le += __shfl_xor_sync(0xffffffffu, le, d);
-      }
-      if (lane == 0) {
-        atomicAdd(&S.pub[1], lg);
-        atomicAdd(&S.pub[2], le);
-      }
-      cluster_sync();
-      if (w == 0) {  // lane r < rank reads rank r's counts
-        uint32_t g = 0, e = 0;
-        if (lane < rank) {
-          g = ld_dsmem_u32(map_rank(smem_addr(&S.pub[1]), lane));
-          e = ld_dsmem_u32(map_rank(smem_addr(&S.pub[2]), lane));
-        }
-        g = __reduce_add_sync(0xffffffffu, g);
-        e = __reduce_add_sync(0xffffffffu, e);
-        if (lane == 0) {
-          S.off[0] = g;
-          S.off[1] = e;
-        }
-      }
-      __syncthreads();
-      gt0 = S.off[0];
-      eq0 = S.off[1];
-    }
-    emit_rounds(S, static_cast<int>(n_st), cut, gt0, eq0,
-                [&](bool sel, uint32_t pos, uint32_t, uint32_t idx) {
-                  const int32_t v = map_index(idx);
-                  if (sel && pos < kk) out_row[pos] = v;
-                });
-
-    if constexpr (G > 1) cluster_sync();  // no CTA leaves while others may read its shared memory
-
-    if (p.counters != nullptr && t == 0) {
-      if (compactions) atomicAdd(&p.counters[kCntCompactions], compactions);
-      if (rank == 0 && sampled) atomicAdd(&p.counters[kCntSampled], 1u);
-    }
-    if (abort) {  // a cluster CTA: the cluster barrier above orders every
-      drain();    // emission store of the cluster before the poison
-      poison_row();
     }
   };
 
-  for (;;) {
-    nxt_started = false;
-    run_item(cur, item + item_step);
-    item += item_step;
-    if (item >= n_items) break;
-    if (!nxt_started) {  // (after a row without streaming, or a failed one)
-      __syncthreads();
-      nxt = make_item(item);
-      start_item(nxt);
+  // One group: two consecutive ring stages A and B (B absent when tsB is
+  // null), or one scalar group as A. Thread t's 16 scores of stage A start at
+  // tsA and have indices idxA + e (present where bit e of validA is set);
+  // likewise for B. Hits of A precede those of B in the stash, each in index
+  // order, so the stash stays in index order. One block barrier per group
+  // (more only when the stash must be compacted). Every thread of the CTA
+  // calls it.
+  auto process_group = [&](const float* tsA, const float* tsB, float sx, int rot, uint32_t validA,
+                           uint32_t validB, uint32_t idxA, uint32_t idxB, bool err) {
+    uint32_t pmA = group_mask(tsA, sx, rot, validA);
+    uint32_t pmB = tsB != nullptr ? group_mask(tsB, sx, rot, validB) : 0u;
+    uint32_t cnt = __popc(pmA) + (static_cast<uint32_t>(__popc(pmB)) << kFieldB);
+    uint32_t incl, base, total;
+    publish(cnt, err, incl, base, total);
+    if ((total & kErrMask) != 0u) abort = true;
+    if (abort) return;  // uniform
+    uint32_t tA = total & kFieldMask, tB = (total >> kFieldB) & kFieldMask;
+    if (tA + tB == 0u) return;  // uniform
+    if (n_st + tA + tB > cap) {
+      if (n_st > kk) {  // keep the exact top-k so far and raise the cutoff
+        compact();
+        pmA = group_mask(tsA, sx, rot, validA);
+        pmB = tsB != nullptr ? group_mask(tsB, sx, rot, validB) : 0u;
+        cnt = __popc(pmA) + (static_cast<uint32_t>(__popc(pmB)) << kFieldB);
+        publish(cnt, false, incl, base, total);
+        tA = total & kFieldMask;
+        tB = (total >> kFieldB) & kFieldMask;
+      }
+      if (n_st + tA + tB > cap) {
+        // More hits than the stash has room for, even above a raised cutoff.
+        // Quarters of the group (half the CTA on one stage, at most
+        // kMinStashRoom hits each) append in index order, compacting in
+        // between (a quarter overflows only when the stash holds more than
+        // k entries).
+        for (int part = 0; part < 4; ++part) {
+          const bool second = part >= 2;
+          if (second && tsB == nullptr) break;  // uniform
+          const bool mine = (w >> 2) == (part & 1);
+          const float* ts = second ? tsB : tsA;
+          const uint32_t valid = second ? validB : validA;
+          uint32_t pm = mine ? group_mask(ts, sx, rot, valid) : 0u;
+          uint32_t c = __popc(pm);
+          publish(c, false, incl, base, total);
+          if (n_st + (total & kFieldMask) > cap) {
+            compact();
+            pm = mine ? group_mask(ts, sx, rot, valid) : 0u;
+            c = __popc(pm);
+            publish(c, false, incl, base, total);
+          }
+          write_hits(pm, n_st + (base & kFieldMask) + incl - c, ts, sx, second ? idxB : idxA);
+          n_st += total & kFieldMask;
+        }
+        return;
+      }
     }
-    cur = nxt;
+    const uint32_t before = incl - cnt;  // packed hits of the lower lanes of this warp
+    write_hits(pmA, n_st + (base & kFieldMask) + (before & kFieldMask), tsA, sx, idxA);
+    write_hits(pmB, n_st + tA + ((base >> kFieldB) & kFieldMask) + ((before >> kFieldB) & kFieldMask),
+               tsB, sx, idxB);
+    n_st += tA + tB;
+  };
+
+  // Scalar group: thread t < cnt holds the score at index first + t.
+  auto scalar_group = [&](int first, int cnt) {
+    float sx = 0.0f;
+    uint32_t valid = 0;
+    if (t < cnt) {
+      sx = rp[first + t];
+      valid = 1u;
+    }
+    process_group(nullptr, nullptr, sx, 0, valid, 0u, static_cast<uint32_t>(first + t), 0u, false);
+  };
+
+  // Takes stage j from the ring: waits for it (bounded) and returns this
+  // thread's 16 scores in it, with the mask of those present.
+  const bool probing = p.probe_stage >= 0;  // test only
+  auto take_stage = [&](int j, bool& err, uint32_t& valid, uint32_t& slot) -> const float* {
+    slot = consumed % kStages;
+    const uint32_t parity = (consumed / kStages) & 1u;
+    ++consumed;
+    if (!abort) {
+      if (probing && j - s0 == p.probe_stage) {
+        err |= !mbar_wait_bounded(&S.never, 0u, 1000ull * p.probe_wait_us);  // runs out
+      } else if (mbar_wait_bounded(&S.full[slot], parity, kWaitLimitNs)) {
+        ++t0_seen;  // in order: stages [t0_seen, issued) are unobserved
+      } else {
+        err = true;
+      }
+    }
+    if (j < nfull) {
+      valid = 0xffffu;
+    } else {  // the last, partial stage
+      const int have = (nb - j * kStageFloats) - kPerThread * t;
+      valid = have >= kPerThread ? 0xffffu : (have <= 0 ? 0u : (1u << have) - 1u);
+    }
+    return &S.ring[slot][kPerThread * t];
+  };
+
+  auto stream_pass = [&]() {
+    const int rot = (t >> 1) & 3;  // rotates the float4 order: conflict-free shared loads
+    if (part == 0 && h > 0) scalar_group(0, h);
+    for (int j = s0; j < s1; j += 2) {
+      const bool two = j + 1 < s1;
+      bool err = false;
+      uint32_t validA, validB = 0, slotA, slotB;
+      const float* tsA = take_stage(j, err, validA, slotA);
+      const float* tsB = two ? take_stage(j + 1, err, validB, slotB) : nullptr;
+      const uint32_t idxA = static_cast<uint32_t>(h + j * kStageFloats + kPerThread * t);
+      process_group(tsA, tsB, 0.0f, rot, validA, validB, idxA, idxA + kStageFloats, err);
+      release_slots(j, slotA, two);
+    }
+    if (part == parts - 1 && tail > 0) scalar_group(h + nb, tail);
+  };
+
+  stream_pass();
+
+  // ---- underflow: the sampled cutoff kept fewer than k candidates -----------
+  // (fewer than min(k, its scores) for the half of a split row)
+  const uint32_t need = split ? min(kk, static_cast<uint32_t>(n_part)) : kk;
+  if (sampled) {
+    uint32_t total = n_st;
+    if constexpr (G > 1) {
+      if (t == 0) S.pub[0] = n_st;
+      cluster_sync();
+      if (w == 0) {  // lane r reads rank r's count
+        uint32_t v = lane < G ? ld_dsmem_u32(map_rank(smem_addr(&S.pub[0]), lane)) : 0u;
+        v = __reduce_add_sync(0xffffffffu, v);
+        if (lane == 0) S.res[3] = v;
+      }
+      cluster_sync();  // every CTA has read every count; S.res[3] is visible
+      total = S.res[3];
+    }
+    if (total < need) {  // uniform over the cluster
+      if (p.counters != nullptr && t == 0 && rank == 0) atomicAdd(&p.counters[kCntRescan], 1u);
+      thr = 0;
+      bound = float_bound(thr);
+      n_st = 0;
+      __syncthreads();  // (the histogram is zero: every search leaves it so)
+      prime();
+      stream_pass();
+    }
+  }
+
+  // A wait timed out: let copies still in flight land (bounded) before the
+  // CTA leaves, so that no bulk copy writes into shared memory it no longer owns.
+  auto drain = [&]() {
+    if (abort && t == 0) {
+      for (uint32_t u = t0_seen; u < S.issued; ++u)
+        (void)mbar_wait_bounded(&S.full[u % kStages], (u / kStages) & 1u, kWaitLimitNs);
+      if (p.counters != nullptr) atomicAdd(&p.counters[kCntDeviceErrors], 1u);
+    }
+  };
+  auto poison_row = [&]() {  // marks the row as failed: no result can be mistaken for one
+    for (int j = t; j < p.k; j += kThreads) out_row[j] = static_cast<int32_t>(0x80000000u);
+  };
+
+  if (split) {
+    // ---- split row: this half's exact top-k goes to the workspace; the half
+    // that finishes second merges both (no CTA ever waits for another) -------
+    const int slot = row - p.split_first;
+    const size_t off = static_cast<size_t>(2 * slot + part) * kk;
+    uint32_t handed = 0;
+    if (!abort) {
+      if (n_st > need) {
+        const Cut c = select_stash<1>(S, static_cast<int>(n_st), need);
+        emit_rounds(S, static_cast<int>(n_st), c, 0u, 0u, [&](bool sel, uint32_t pos, uint32_t key, uint32_t idx) {
+          if (sel && pos < need) {
+            p.ws_key[off + pos] = key;
+            p.ws_idx[off + pos] = idx;
+          }
+        });
+        handed = need;
+      } else {
+        for (int e = t; e < static_cast<int>(n_st); e += kThreads) {
+          p.ws_key[off + e] = S.skey[e];
+          p.ws_idx[off + e] = S.sidx[e];
+        }
+        handed = n_st;
+      }
+    }
+    drain();
+    if (p.counters != nullptr && t == 0) {
+      if (compactions) atomicAdd(&p.counters[kCntCompactions], compactions);
+      if (part == 0 && sampled) atomicAdd(&p.counters[kCntSampled], 1u);
+    }
+    if (t == 0) p.ws_cnt[2 * slot + part] = abort ? kHalfFailed : handed;
+    __threadfence();  // the hand-over is visible before the arrival is counted
+    __syncthreads();
+    if (t == 0) S.res[3] = atomicAdd(&p.ws_ctr[slot], 1u);
+    __syncthreads();
+    if (S.res[3] == 0u) return;  // first to finish: the other half merges
+    __threadfence();
+    if (t == 0) p.ws_ctr[slot] = 0u;  // both halves have arrived: ready for the next call
+    const uint32_t c0 = __ldcg(&p.ws_cnt[2 * slot]), c1 = __ldcg(&p.ws_cnt[2 * slot + 1]);
+    if (c0 == kHalfFailed || c1 == kHalfFailed) {
+      poison_row();
+      return;
+    }
+    if (PAGED) {  // as below, for the whole row
+      const int p1 = (n + p.page_size - 1) / p.page_size;
+      for (int q = 32 * t; q < p1; q += 32 * kThreads) prefetch_l2(pt_row + q);
+      if (t == 0) prefetch_l2(pt_row + p1 - 1);
+    }
+    for (int i = t; i < kBins; i += kThreads) S.hist[i] = 0;
+    __syncthreads();  // the local emission has read the stash; the histogram is clear
+    // Half 0's entries precede half 1's: the merged stash is in index order.
+    const size_t base0 = static_cast<size_t>(2 * slot) * kk;
+    for (int e = t; e < static_cast<int>(c0 + c1); e += kThreads) {
+      const size_t src = static_cast<uint32_t>(e) < c0 ? base0 + e : base0 + kk + (e - c0);
+      const uint32_t key = __ldcg(&p.ws_key[src]);
+      S.skey[e] = key;
+      S.sidx[e] = __ldcg(&p.ws_idx[src]);
+    }
+    const Cut c = select_stash<1>(S, static_cast<int>(c0 + c1), kk);
+    emit_rounds(S, static_cast<int>(c0 + c1), c, 0u, 0u, [&](bool sel, uint32_t pos, uint32_t, uint32_t idx) {
+      const int32_t v = map_index(idx);
+      if (sel && pos < kk) out_row[pos] = v;
+    });
+    if (p.counters != nullptr && t == 0) atomicAdd(&p.counters[kCntSplitRows], 1u);
+    return;
+  }
+
+  if constexpr (G == 1) {
+    if (abort) {  // uniform: nothing is selected from an incomplete stash, and
+      drain();    // the poison is the only store this CTA makes to its row
+      poison_row();
+      return;
+    }
+  }
+
+  // ---- exact cutoff over the stash(es) and emission --------------------------
+  if (PAGED && !abort) {
+    // The emission maps every selected index through the page table: start
+    // bringing this CTA's part of the table row into L2 while the cutoff is
+    // found (one line per 32 entries).
+    const int first = rank == 0 ? 0 : h + s0 * kStageFloats;
+    const int last = rank == G - 1 ? n : h + s1 * kStageFloats;
+    const int p0 = first / p.page_size, p1 = (last + p.page_size - 1) / p.page_size;
+    for (int q = p0 + 32 * t; q < p1; q += 32 * kThreads) prefetch_l2(pt_row + q);
+    if (t == 0 && p1 > p0) prefetch_l2(pt_row + p1 - 1);  // the last line, if no start fell in it
+  }
+  const Cut cut = select_stash<G>(S, static_cast<int>(n_st), kk, hdst);
+  uint32_t gt0 = 0, eq0 = 0;
+  if constexpr (G > 1) {
+    // Entries above / at the cutoff in this CTA's stash; lower ranks come first.
+    if (t == 0) {
+      S.pub[1] = 0;
+      S.pub[2] = 0;
+    }
+    __syncthreads();
+    uint32_t lg = 0, le = 0;
+    for (int e = t; e < static_cast<int>(n_st); e += kThreads) {
+      const uint32_t hi = S.skey[e] >> cut.shift;
+      lg += hi > cut.P;
+      le += hi == cut.P;
+    }
+    for (int d = 16; d > 0; d >>= 1) {
+      lg += __shfl_xor_sync(0xffffffffu, lg, d);
+      le += __shfl_xor_sync(0xffffffffu, le, d);
+    }
+    if (lane == 0) {
+      atomicAdd(&S.pub[1], lg);
+      atomicAdd(&S.pub[2], le);
+    }
+    cluster_sync();
+    if (w == 0) {  // lane r < rank reads rank r's counts
+      uint32_t g = 0, e = 0;
+      if (lane < rank) {
+        g = ld_dsmem_u32(map_rank(smem_addr(&S.pub[1]), lane));
+        e = ld_dsmem_u32(map_rank(smem_addr(&S.pub[2]), lane));
+      }
+      g = __reduce_add_sync(0xffffffffu, g);
+      e = __reduce_add_sync(0xffffffffu, e);
+      if (lane == 0) {
+        S.off[0] = g;
+        S.off[1] = e;
+      }
+    }
+    __syncthreads();
+    gt0 = S.off[0];
+    eq0 = S.off[1];
+  }
+  emit_rounds(S, static_cast<int>(n_st), cut, gt0, eq0,
+              [&](bool sel, uint32_t pos, uint32_t, uint32_t idx) {
+                const int32_t v = map_index(idx);
+                if (sel && pos < kk) out_row[pos] = v;
+              });
+
+  if constexpr (G > 1) cluster_sync();  // no CTA leaves while others may read its shared memory
+
+  if (p.counters != nullptr && t == 0) {
+    if (compactions) atomicAdd(&p.counters[kCntCompactions], compactions);
+    if (rank == 0 && sampled) atomicAdd(&p.counters[kCntSampled], 1u);
+  }
+  if (abort) {  // a cluster CTA: the cluster barrier above orders every
+    drain();    // emission store of the cluster before the poison
+    poison_row();
   }
 }
 

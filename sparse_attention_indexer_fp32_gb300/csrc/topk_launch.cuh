@@ -80,12 +80,9 @@ topk_status launch_variant(const Params& p, int dev, cudaStream_t stream) {
   const topk_status prep = prepare_variant<KMAX, G, PAGED>(dev);
   if (prep != TOPK_OK) return prep;
   cudaLaunchConfig_t cfg = {};
-  // G CTAs per row; or, persistent, one CTA per item (a row, or a half of a
-  // split row) up to the CTAs resident at once.
-  const unsigned items = static_cast<unsigned>(p.B) + static_cast<unsigned>(p.B - p.split_first);
+  // G CTAs per row, or one per row plus one more per split row.
   const unsigned grid = G > 1 ? static_cast<unsigned>(p.B) * G
-                              : (items < static_cast<unsigned>(p.resident) ? items
-                                                                           : static_cast<unsigned>(p.resident));
+                              : static_cast<unsigned>(p.B) + static_cast<unsigned>(p.B - p.split_first);
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;

@@ -80,17 +80,17 @@ def test_short_rows_fall_back_to_the_exact_path():
 
 @pytest.mark.parametrize("config", [6, 7])
 def test_prefill_workload_rows(config):
-    """The first rows of the prefill-shaped workloads, ragged and paged: rows
-    of 8192 take the short-row kernel automatically, rows of 16384 the
-    streaming kernel (faster there on the dispatch sweep); both forced onto
-    the short-row kernel too."""
+    """The first rows of the prefill-shaped workloads take the short-row
+    kernel automatically; ragged and paged; and the streaming kernel forced."""
     w = make_workload(config, B=96)
     cnt = counters_tensor()
     check_against_oracle(w.scores, w.lengths, w.k, counters=cnt)
-    assert int(cnt[tk.Counter.SHORT_ROWS]) == (w.B if w.stride <= 8192 else 0)
-    cnt = counters_tensor()
-    check_against_oracle(w.scores, w.lengths, w.k, short_rows=1, counters=cnt)
     assert int(cnt[tk.Counter.SHORT_ROWS]) == w.B
+    cnt = counters_tensor()
+    check_against_oracle(w.scores, w.lengths, w.k, short_rows=-1, counters=cnt)
+    assert int(cnt[tk.Counter.SHORT_ROWS]) == 0
+    cnt = counters_tensor()
+    check_against_oracle(w.scores, w.lengths, w.k, counters=cnt)
     # nearly every row through the stash (a row whose k-th largest score's
     # coarse bin is selected whole, or holds too many scores, is served from
     # registers instead)
