@@ -229,7 +229,7 @@ struct SlabScan {
 };
 
 template <int E, int KMAX, bool PAGED, typename T>
-__global__ void __launch_bounds__(kThreads, E <= 32 ? (KMAX <= 1024 ? 5 : 4) : 2) topk_short_kernel(const ShortParams p) {
+__global__ void __launch_bounds__(kThreads, E <= 32 ? (KMAX <= 1024 ? 5 : 4) : 3) topk_short_kernel(const ShortParams p) {
   constexpr int C = ShortCap<KMAX>::value;
   constexpr int V = ScoreIn<T>::V;
   constexpr int NQ = E / V;  // vectors per lane
