@@ -53,6 +53,7 @@ KERNEL_SOURCES = {
     "topk_short_kernel": _LAUNCH_FILES + ("topk_short.cuh",) + tuple(f"topk_short_k{k}.cu"
                                                                    for k in (512, 1024, 2048)),
     "amax8_kernel": ("ptx.cuh", "topk_kernel.cuh", "topk_blocks.cu"),
+    "sort_blocks_kernel": ("ptx.cuh", "topk_kernel.cuh", "topk_blocks.cu"),
 }
 
 
@@ -325,7 +326,7 @@ def bench_prefill(config: int, local: int, steps: int, warmup: int, world: int, 
             "rows_per_s": w.B / (us * 1e-6), "steps": steps,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": f"{peak_kind} hbm_gbs (burst copy)",
-                         "traffic": None if bf16 else profiled_traffic(w.name),
+                         "traffic": profiled_traffic(w.name + ("_bf16" if bf16 else "")),
                          "algorithmic_bytes_per_launch": algo},
             "config": {"workload": w.name, "B": w.B, "stride": w.stride, "k": w.k,
                        "dtype": "bf16" if bf16 else "f32",
@@ -347,11 +348,14 @@ def two_level_rooflines(res: dict, nb: np.ndarray, keys_stride: int, B: int, k_b
         algo_keys, res["amax8_varlen"]["us_per_call"],
         profiled_traffic("amax8_varlen_" + workload.split("_k")[0]))
     # top-k over the keys: the keys read and the block ids written
+    shape = workload.split("_k")[0]
     algo_sel = algorithmic_bytes(nb, keys_stride, B, k_blocks)
-    res["topk_over_keys"]["roofline"] = hbm_roofline(algo_sel, res["topk_over_keys"]["us_per_call"])
+    res["topk_over_keys"]["roofline"] = hbm_roofline(
+        algo_sel, res["topk_over_keys"]["us_per_call"], profiled_traffic("topk_over_keys_" + shape))
     algo_table = 4 * B * k_blocks * 4
     res["sort_candidate_blocks"]["roofline"] = hbm_roofline(
-        algo_table, res["sort_candidate_blocks"]["us_per_call"])
+        algo_table, res["sort_candidate_blocks"]["us_per_call"],
+        profiled_traffic("sort_candidate_blocks_" + shape))
 
 
 def bench_two_level(local: int, steps: int, warmup: int, world: int):
