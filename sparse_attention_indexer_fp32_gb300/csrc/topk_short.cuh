@@ -409,8 +409,10 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? (KMAX <= 1024 ? 5 : 4) : 3
     const uint32_t b2 = find_bin_all<8>(S, S.hist2, S.hist, rem, &above, &inbin);
     const uint32_t p2 = (b1 << 11) | b2;
     rem -= above;
-    if (rem == inbin) {
-      cut = Cut{10, p2, rem, true};
+    if (rem == inbin || sizeof(T) == 2) {
+      // (BF16: a key's low 16 bits follow from its high 16, so the entries
+      // of bin p2 are all equal and the first rem of them are taken)
+      cut = Cut{10, p2, rem, rem == inbin};
     } else {
       short_stash_hist(S, S.hist, static_cast<int>(total), 10, p2, 0, 0x3ff);
       const uint32_t b3 = find_bin_all<4>(S, S.hist, S.hist2, rem, &above, &inbin);
@@ -432,8 +434,8 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? (KMAX <= 1024 ? 5 : 4) : 3
     const uint32_t b2 = find_bin_all<8>(S, S.hist2, S.hist, rem, &above, &inbin);
     const uint32_t p2 = (b1 << 11) | b2;
     rem -= above;
-    if (rem == inbin) {
-      cut = Cut{10, p2, rem, true};
+    if (rem == inbin || sizeof(T) == 2) {  // (BF16: as above)
+      cut = Cut{10, p2, rem, rem == inbin};
     } else {
 #pragma unroll
       for (int j = 0; j < E; ++j) {
