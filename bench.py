@@ -9,7 +9,7 @@ B=1024 x 131072, k=2048 ragged workload is measured too and reported under
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
-``--impl reference`` times the CPU oracle (the reference arm of this build) on
+``--impl reference`` times the CPU oracle (the reference arm) on
 a bounded sample of the same workload instead.
 """
 
