@@ -314,6 +314,17 @@ def test_paged_full_mapping():
     check_against_oracle(scores, lengths, 512, pt, ps)
 
 
+@pytest.mark.parametrize("cluster", [2, 4, 8, 16])
+def test_paged_output_from_clusters(cluster):
+    """Paged output written by every CTA of a cluster (each maps its own
+    share of the selection through the table), with an odd page size too."""
+    w = make_workload(4, B=6)
+    check_against_oracle(w.scores, w.lengths, w.k, w.page_table, w.page_size, cluster_size=cluster)
+    rng = np.random.default_rng(cluster)
+    pt = rng.permutation(6 * 40000).astype(np.int32).reshape(6, 40000)
+    check_against_oracle(w.scores, w.lengths, 1024, pt, 7, cluster_size=cluster, sample_mode=2)
+
+
 def test_status_codes():
     s = torch.zeros((2, 64), dtype=torch.float32, device="cuda:0")
     l = torch.full((2,), 64, dtype=torch.int32, device="cuda:0")

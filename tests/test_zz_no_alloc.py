@@ -137,3 +137,24 @@ def test_noalloc_deterministic_over_100_calls():
         differing += int(not torch.equal(out, first))
     assert differing == 0
     assert torch.equal(first, tk.topk_paged(s, l, w.k, pt, w.page_size, split=False))
+
+
+@pytest.mark.parametrize("B,stride,k", [(300, 8192, 512), (200, 16384, 2048), (4, 262144, 512),
+                                        (40, 98307, 1024)])
+def test_noalloc_without_scratch_paths(B, stride, k):
+    """Calls that split no row (short rows, a small batch on clusters, rows
+    narrower than the split gate) go through the same entry point and match
+    the regular call and the oracle."""
+    lib = tk.load_library()
+    rng = np.random.default_rng(B + stride)
+    scores = rng.standard_normal((B, stride)).astype(np.float32)
+    lengths = rng.integers(stride * 4 // 5, stride + 1, B).astype(np.int32)
+    s, l = to_dev(scores), to_dev(lengths)
+    want = tk.topk_ragged(s, l, k)
+    got = torch.full_like(want, -7)
+    assert _noalloc(lib, s, l, k, got) == tk.Status.OK
+    torch.cuda.synchronize()
+    assert torch.equal(got, want)
+    rows = np.arange(0, B, max(1, B // 6))
+    assert_parity(scores[rows], lengths[rows], k, got.cpu().numpy()[rows],
+                  run_oracle(scores[rows], lengths[rows], k), rows=rows)
