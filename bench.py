@@ -52,6 +52,8 @@ KERNEL_SOURCES = {
                                               for o in ("ragged", "paged")),
     "topk_short_kernel": _LAUNCH_FILES + ("topk_short.cuh",) + tuple(f"topk_short_k{k}.cu"
                                                                    for k in (512, 1024, 2048)),
+    "topk_short_bf16_kernel": _LAUNCH_FILES + ("topk_short.cuh", "topk_short_bf16.cuh")
+    + tuple(f"topk_short_k{k}.cu" for k in (512, 1024, 2048)),
     "amax8_kernel": ("ptx.cuh", "topk_kernel.cuh", "topk_blocks.cu"),
     "sort_blocks_kernel": ("ptx.cuh", "topk_kernel.cuh", "topk_blocks.cu"),
 }

@@ -10,6 +10,7 @@
 #include "topk_indexer.h"
 #include "topk_kernel.cuh"
 #include "topk_short.cuh"
+#include "topk_short_bf16.cuh"
 
 namespace tki {
 
@@ -123,20 +124,17 @@ int max_active_clusters(int G, int dev) {
 }
 
 
-// Short-row kernel variant (E scores per thread).
-template <int E, int KMAX, bool PAGED, typename T>
-topk_status launch_short_variant(const ShortParams& p_in, int dev, int sm_count, cudaStream_t stream) {
-  constexpr size_t smem = sizeof(ShortSmem<ShortCap<KMAX>::value>);
-  // CTAs resident at once on this device (per device, found once, after the
-  // kernel's shared-memory attribute is set).
-  static std::atomic<int> resident[64];
+// Launches one short-row kernel (one CTA per row) with its dynamic shared
+// memory; `resident` caches, per device, the CTAs an SM holds at once
+// (found once, after the kernel's shared-memory attribute is set).
+inline topk_status launch_short_grid(void (*kern)(ShortParams), size_t smem, std::atomic<int>* resident,
+                                     const ShortParams& p_in, int dev, int sm_count, cudaStream_t stream) {
   int per_sm = resident[dev].load(std::memory_order_acquire);
   if (per_sm == 0) {
-    if (cudaFuncSetAttribute(topk_short_kernel<E, KMAX, PAGED, T>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+        cudaSuccess)
       return TOPK_ECUDA;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_short_kernel<E, KMAX, PAGED, T>,
-                                                      kThreads, smem) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess)
       return TOPK_ECUDA;
     resident[dev].store(per_sm, std::memory_order_release);
   }
@@ -147,9 +145,23 @@ topk_status launch_short_variant(const ShortParams& p_in, int dev, int sm_count,
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  return cudaLaunchKernelEx(&cfg, topk_short_kernel<E, KMAX, PAGED, T>, p) == cudaSuccess
-             ? TOPK_OK
-             : TOPK_ECUDA;
+  return cudaLaunchKernelEx(&cfg, kern, p) == cudaSuccess ? TOPK_OK : TOPK_ECUDA;
+}
+
+// FP32 short-row kernel variant (E scores per thread).
+template <int E, int KMAX, bool PAGED>
+topk_status launch_short_variant(const ShortParams& p, int dev, int sm_count, cudaStream_t stream) {
+  static std::atomic<int> resident[64];
+  return launch_short_grid(topk_short_kernel<E, KMAX, PAGED>, sizeof(ShortSmem<ShortCap<KMAX>::value>), resident,
+                           p, dev, sm_count, stream);
+}
+
+// BF16 short-row kernel variant (E scores per thread).
+template <int E, int KMAX, bool PAGED>
+topk_status launch_short_bf16_variant(const ShortParams& p, int dev, int sm_count, cudaStream_t stream) {
+  static std::atomic<int> resident[64];
+  return launch_short_grid(topk_short_bf16_kernel<E, KMAX, PAGED>, sizeof(ShortSmemBf16<ShortCap<KMAX>::value>),
+                           resident, p, dev, sm_count, stream);
 }
 
 // Rows of at most 8192 scores take E = 32, longer ones (up to 16384) E = 64.
@@ -159,16 +171,16 @@ topk_status launch_short_bucket(const ShortParams& p, bool bf16, int dev, int sm
   const bool narrow = p.stride <= 32 * kThreads;
   if (bf16) {
     if (narrow)
-      return paged ? launch_short_variant<32, KMAX, true, uint16_t>(p, dev, sms, stream)
-                   : launch_short_variant<32, KMAX, false, uint16_t>(p, dev, sms, stream);
-    return paged ? launch_short_variant<64, KMAX, true, uint16_t>(p, dev, sms, stream)
-                 : launch_short_variant<64, KMAX, false, uint16_t>(p, dev, sms, stream);
+      return paged ? launch_short_bf16_variant<32, KMAX, true>(p, dev, sms, stream)
+                   : launch_short_bf16_variant<32, KMAX, false>(p, dev, sms, stream);
+    return paged ? launch_short_bf16_variant<64, KMAX, true>(p, dev, sms, stream)
+                 : launch_short_bf16_variant<64, KMAX, false>(p, dev, sms, stream);
   }
   if (narrow)
-    return paged ? launch_short_variant<32, KMAX, true, float>(p, dev, sms, stream)
-                 : launch_short_variant<32, KMAX, false, float>(p, dev, sms, stream);
-  return paged ? launch_short_variant<64, KMAX, true, float>(p, dev, sms, stream)
-               : launch_short_variant<64, KMAX, false, float>(p, dev, sms, stream);
+    return paged ? launch_short_variant<32, KMAX, true>(p, dev, sms, stream)
+                 : launch_short_variant<32, KMAX, false>(p, dev, sms, stream);
+  return paged ? launch_short_variant<64, KMAX, true>(p, dev, sms, stream)
+               : launch_short_variant<64, KMAX, false>(p, dev, sms, stream);
 }
 
 // Defined in topk_short_k{512,1024,2048}.cu.

@@ -1,5 +1,5 @@
-// Exact per-row top-k for short rows (at most 16384 scores), FP32 or BF16
-// scores: the prefill side of the indexer, where a batch holds thousands of
+// Exact per-row top-k for short rows (at most 16384 FP32 scores): the
+// prefill side of the indexer, where a batch holds thousands of
 // rows of a few thousand scores each.
 //
 // The streaming kernel's per-row fixed costs (sample loads, ring set-up,
@@ -149,41 +149,14 @@ struct ShortParams {
   int32_t ahead;  // CTAs resident at once: the block that will take this CTA's slot next
 };
 
-template <typename T>
-struct ScoreIn;
-
-// V consecutive scores per 16-byte vector, converted to order-preserving keys.
-template <>
-struct ScoreIn<float> {
-  static constexpr int V = 4;
-  __device__ __forceinline__ static uint32_t key_at(const float* p) { return order_key(__ldg(p)); }
-  __device__ __forceinline__ static void vec(const float* p, uint32_t* key) {
-    const float4 x = __ldg(reinterpret_cast<const float4*>(p));
-    key[0] = order_key(x.x);
-    key[1] = order_key(x.y);
-    key[2] = order_key(x.z);
-    key[3] = order_key(x.w);
-  }
-};
-
-template <>
-struct ScoreIn<uint16_t> {
-  static constexpr int V = 8;
-  // bf16 -> fp32 is exact: the bf16 bits are the float's high half.
-  __device__ __forceinline__ static uint32_t key_of(uint32_t bits16) {
-    return order_key(__uint_as_float(bits16 << 16));
-  }
-  __device__ __forceinline__ static uint32_t key_at(const uint16_t* p) { return key_of(__ldg(p)); }
-  __device__ __forceinline__ static void vec(const uint16_t* p, uint32_t* key) {
-    const uint4 x = __ldg(reinterpret_cast<const uint4*>(p));
-    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      key[2 * i + 0] = key_of(w[i] & 0xffffu);
-      key[2 * i + 1] = key_of(w[i] >> 16);
-    }
-  }
-};
+// The keys of four consecutive scores (one 16-byte vector).
+__device__ __forceinline__ void load_keys4(const float* p, uint32_t* key) {
+  const float4 x = __ldg(reinterpret_cast<const float4*>(p));
+  key[0] = order_key(x.x);
+  key[1] = order_key(x.y);
+  key[2] = order_key(x.z);
+  key[3] = order_key(x.w);
+}
 
 // Positions in index order inside one warp. Lane l's vector q covers the
 // warp's scores [q*32V + l*V, q*32V + l*V + V), so the warp's index order is
@@ -228,10 +201,10 @@ struct SlabScan {
   }
 };
 
-template <int E, int KMAX, bool PAGED, typename T>
+template <int E, int KMAX, bool PAGED>
 __global__ void __launch_bounds__(kThreads, E <= 32 ? (KMAX <= 1024 ? 5 : 4) : 3) topk_short_kernel(const ShortParams p) {
   constexpr int C = ShortCap<KMAX>::value;
-  constexpr int V = ScoreIn<T>::V;
+  constexpr int V = 4;        // scores per 16-byte vector
   constexpr int NQ = E / V;  // vectors per lane
   constexpr int CH = 32 * E;  // scores per warp
   constexpr int NW = E / 32;  // words of per-score bit masks
@@ -248,10 +221,10 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? (KMAX <= 1024 ? 5 : 4) : 3
     const int nr = row + p.ahead;
     const int64_t ln = p.lengths[nr];
     const int len = static_cast<int>(ln < 0 ? 0 : (ln > p.stride ? p.stride : ln));
-    const char* base = reinterpret_cast<const char*>(static_cast<const T*>(p.scores) +
+    const char* base = reinterpret_cast<const char*>(static_cast<const float*>(p.scores) +
                                                      static_cast<int64_t>(nr) * p.stride);
     const uintptr_t a0 = (reinterpret_cast<uintptr_t>(base) + 15u) & ~static_cast<uintptr_t>(15u);
-    const uintptr_t a1 = (reinterpret_cast<uintptr_t>(base) + static_cast<uintptr_t>(len) * sizeof(T)) &
+    const uintptr_t a1 = (reinterpret_cast<uintptr_t>(base) + static_cast<uintptr_t>(len) * sizeof(float)) &
                          ~static_cast<uintptr_t>(15u);
     if (a1 > a0) bulk_prefetch_l2(reinterpret_cast<const void*>(a0), static_cast<uint32_t>(a1 - a0));
   }
@@ -282,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? (KMAX <= 1024 ? 5 : 4) : 3
   // Warp w owns the row's scores [w*CH, (w+1)*CH); key[q*V + c] is the score
   // at index w*CH + q*32V + lane*V + c, so each vector load of a warp reads
   // 512 contiguous bytes.
-  const T* rp = static_cast<const T*>(p.scores) + static_cast<int64_t>(row) * p.stride;
+  const float* rp = static_cast<const float*>(p.scores) + static_cast<int64_t>(row) * p.stride;
   const int wbase = w * CH;
   auto index_of = [&](int q, int c) -> uint32_t {
     return static_cast<uint32_t>(wbase + q * 32 * V + lane * V + c);
@@ -300,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? (KMAX <= 1024 ? 5 : 4) : 3
 #pragma unroll
     for (int q = 0; q < NQ; ++q) {
       const int v0 = static_cast<int>(index_of(q, 0));
-      ScoreIn<T>::vec(rp + (v0 < n ? v0 : 0), &key[q * V]);
+      load_keys4(rp + (v0 < n ? v0 : 0), &key[q * V]);
     }
     if (wbase + CH <= n) {  // warp-uniform: the whole warp lies inside the row
 #pragma unroll
@@ -321,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? (KMAX <= 1024 ? 5 : 4) : 3
     for (int j = 0; j < E; ++j) {
       const int idx = static_cast<int>(index_of(j / V, j % V));
       const bool ok = idx < n;
-      key[j] = ScoreIn<T>::key_at(rp + (ok ? idx : 0));
+      key[j] = order_key(__ldg(rp + (ok ? idx : 0)));
       valid[j / 32] |= static_cast<uint32_t>(ok) << (j % 32);
     }
   }
@@ -409,10 +382,8 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? (KMAX <= 1024 ? 5 : 4) : 3
     const uint32_t b2 = find_bin_all<8>(S, S.hist2, S.hist, rem, &above, &inbin);
     const uint32_t p2 = (b1 << 11) | b2;
     rem -= above;
-    if (rem == inbin || sizeof(T) == 2) {
-      // (BF16: a key's low 16 bits follow from its high 16, so the entries
-      // of bin p2 are all equal and the first rem of them are taken)
-      cut = Cut{10, p2, rem, rem == inbin};
+    if (rem == inbin) {
+      cut = Cut{10, p2, rem, true};
     } else {
       short_stash_hist(S, S.hist, static_cast<int>(total), 10, p2, 0, 0x3ff);
       const uint32_t b3 = find_bin_all<4>(S, S.hist, S.hist2, rem, &above, &inbin);
@@ -434,8 +405,8 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? (KMAX <= 1024 ? 5 : 4) : 3
     const uint32_t b2 = find_bin_all<8>(S, S.hist2, S.hist, rem, &above, &inbin);
     const uint32_t p2 = (b1 << 11) | b2;
     rem -= above;
-    if (rem == inbin || sizeof(T) == 2) {  // (BF16: as above)
-      cut = Cut{10, p2, rem, rem == inbin};
+    if (rem == inbin) {
+      cut = Cut{10, p2, rem, true};
     } else {
 #pragma unroll
       for (int j = 0; j < E; ++j) {
