@@ -25,7 +25,10 @@
 //     prefix over the warps).
 //  3. The finer passes (11, then 10 bits) over the stash entries of bin b1
 //     only, and emission in stash (= index) order with the streaming
-//     kernel's emit_rounds.
+//     kernel's emit_rounds. The 11-bit pass also counts its entries per
+//     group of 32 bins, so that every warp finds its bin after one barrier
+//     (the group among 64 sums, then the bin among 32) instead of scanning
+//     all 2048 bins.
 //  4. Exact register path: when bin b1 and above hold more entries than the
 //     stash (ties, narrow rows), the finer passes run over the registers and
 //     a census writes the selection straight from them.
@@ -61,6 +64,7 @@ struct ShortSmem {
   uint32_t sidx[C];
   uint32_t hist[kBins];    // (emit_rounds' and the shared helpers' name for hbuf[0])
   uint32_t hist2[kBins];   // the second histogram buffer
+  uint32_t sum64[64];      // pass-2 group sums: bins 32g .. 32g + 31 of hist2
   uint32_t tincl[kThreads];  // per-thread inclusive bin sums within the warp
   uint32_t tab[2][kWarps];
   uint32_t rtab[2][kWarps];
@@ -113,6 +117,33 @@ __device__ uint32_t find_bin_all(SM& S, const uint32_t* hist, uint32_t* other, u
   *above = tbefore + __shfl_sync(0xffffffffu, ic - c, ib);
   *inbin = __shfl_sync(0xffffffffu, c, ib);
   return static_cast<uint32_t>(lo_s + BPT - 1 - ib);
+}
+
+// Finds the bin holding the target-th largest element of a 2048-bin
+// histogram that carries per-group sums (sum64[g] = bins 32g .. 32g + 31),
+// after one barrier and with no broadcast: every warp locates the group from
+// the 64 sums, then the bin among its 32. The bins are left as they are.
+__device__ __forceinline__ uint32_t find_bin_grouped(const uint32_t* hist, const uint32_t* sum64, uint32_t target,
+                                                     uint32_t* above, uint32_t* inbin) {
+  const int lane = threadIdx.x & 31;
+  __syncthreads();  // the histogram and its sums are complete
+  const uint2 g = *reinterpret_cast<const uint2*>(&sum64[62 - 2 * lane]);  // groups 62 - 2l, 63 - 2l
+  const uint32_t s2 = g.x + g.y;
+  const uint32_t inc = warp_incl_scan(s2);  // descending groups
+  const int ls = __ffs(__ballot_sync(0xffffffffu, inc >= target)) - 1;
+  uint32_t before = __shfl_sync(0xffffffffu, inc - s2, ls);
+  const uint32_t gy = __shfl_sync(0xffffffffu, g.y, ls);
+  int grp = 63 - 2 * ls;
+  if (before + gy < target) {
+    before += gy;
+    --grp;
+  }
+  const uint32_t c = hist[32 * grp + 31 - lane];  // descending bins
+  const uint32_t ic = warp_incl_scan(c);
+  const int ib = __ffs(__ballot_sync(0xffffffffu, before + ic >= target)) - 1;
+  *above = before + __shfl_sync(0xffffffffu, ic - c, ib);
+  *inbin = __shfl_sync(0xffffffffu, c, ib);
+  return static_cast<uint32_t>(32 * grp + 31 - ib);
 }
 
 // Histogram of stash keys into `hist`: entries e < n with (key >> fshift) ==
@@ -303,6 +334,7 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? (KMAX <= 1024 ? 5 : 4) : 3
     reinterpret_cast<uint4*>(S.hist)[i] = make_uint4(0, 0, 0, 0);
     reinterpret_cast<uint4*>(S.hist2)[i] = make_uint4(0, 0, 0, 0);
   }
+  if (t < 64) S.sum64[t] = 0;
   __syncthreads();
 
   int grp = 0;
@@ -357,6 +389,10 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? (KMAX <= 1024 ? 5 : 4) : 3
     for (int q = 0; q < NQ; ++q) wt += SlabScan<NQ, V>::field(sc.tot, q);
     uint32_t before, total;
     warp_prefix(wt, before, total);  // total == above + inbin
+    // Every warp is past its coarse search, which left S.hist as it was:
+    // clear it for a third pass.
+    reinterpret_cast<uint4*>(&S.hist[8 * t])[0] = make_uint4(0, 0, 0, 0);
+    reinterpret_cast<uint4*>(&S.hist[8 * t])[1] = make_uint4(0, 0, 0, 0);
     uint32_t vbase = before;  // the warp's hits in the vectors before q
 #pragma unroll
     for (int q = 0; q < NQ; ++q) {
@@ -378,8 +414,19 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? (KMAX <= 1024 ? 5 : 4) : 3
     }
     // ---- 3. the exact cutoff inside bin b1 (its entries only), emission -------
     __syncthreads();  // the stash is complete
-    short_stash_hist(S, S.hist2, static_cast<int>(total), 21, b1, 10, 0x7ff);
-    const uint32_t b2 = find_bin_all<8>(S, S.hist2, S.hist, rem, &above, &inbin);
+    for (int base0 = 0; base0 < static_cast<int>(total); base0 += kRoundEntries) {
+      const int base = base0 + kRoundPerThread * t;
+      uint32_t kv[kRoundPerThread];
+      load_round(S.skey, base, static_cast<int>(total), kv);
+#pragma unroll
+      for (int c = 0; c < kRoundPerThread; ++c) {
+        if (base + c < static_cast<int>(total) && (kv[c] >> 21) == b1) {
+          atomicAdd(&S.hist2[(kv[c] >> 10) & 0x7ffu], 1u);
+          atomicAdd(&S.sum64[(kv[c] >> 15) & 63u], 1u);
+        }
+      }
+    }
+    const uint32_t b2 = find_bin_grouped(S.hist2, S.sum64, rem, &above, &inbin);
     const uint32_t p2 = (b1 << 11) | b2;
     rem -= above;
     if (rem == inbin) {
