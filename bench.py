@@ -773,6 +773,12 @@ def run_gpu_arm(args):
     rank, local, world = dist_setup(args.gpus)
     primary = WORKLOADS[args.workload]
     secondary = 3 if primary == 4 else 4
+    if args.bf16:  # profiling runs of the BF16 short-row kernel
+        res = bench_prefill(primary, local, args.steps, args.warmup, world, bf16=True)
+        if rank == 0:
+            print(json.dumps({"quick": True, "workload": res["workload"], "B": res["config"]["B"],
+                              "us_per_call": res["us_per_call"], "roofline": res["roofline"]}), flush=True)
+        return
     res = bench_workload(primary, args.steps, args.warmup, world, local, with_e2e=not args.quick,
                          e2e_steps=args.e2e_steps, clocks=not args.quick, rows=args.rows)
     also = latency = prefill = two_level = None
@@ -922,6 +928,9 @@ def main(argv=None):
                     help="use only the first ROWS rows of the workload (profiling runs)")
     ap.add_argument("--quick", action="store_true",
                     help="primary workload only, no e2e / clocks / CPU baseline (profiling runs)")
+    ap.add_argument("--bf16", action="store_true",
+                    help="with --quick and a prefill workload: its scores rounded to BF16, through "
+                         "topk_select_bf16 (profiling runs)")
     ap.add_argument("--sweep", action="store_true",
                     help="time every path over batch x width x k instead (dispatch sweep)")
     ap.add_argument("--sweep-out", default="gpurun_out",
@@ -929,6 +938,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.bf16 and not (args.quick and WORKLOADS[args.workload] in (6, 7)):
+        ap.error("--bf16 needs --quick and a prefill workload")
     if args.sweep:
         run_sweep(args)
     elif args.impl == "reference":
