@@ -182,3 +182,54 @@ def test_short_rows_deterministic_over_100_calls():
     for _ in range(99):
         assert torch.equal(tk.topk_ragged(s, l, w.k), first)
     torch.cuda.synchronize()
+
+
+def _bf16_dev(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to("cuda:0").view(torch.bfloat16)
+
+
+@pytest.mark.parametrize("width", [8192, 16384, 9001, 4000])
+@pytest.mark.parametrize("k", [1, 17, 700, 2048])
+def test_bf16_adversarial_rows(width, k):
+    """The adversarial rows (constant rows, dense ties, +-inf, +-0, lengths
+    around k and the width) rounded to BF16: both register layouts (32 and 64
+    keys per thread), an odd width (rows that do not start on 16 bytes: scalar
+    loads), the stash path and the register census, ragged and paged with an
+    odd page size."""
+    scores, lengths = _short_rows(width)
+    bits = to_bf16_bits(scores)
+    vals = bf16_bits_to_float(bits)
+    s, l = _bf16_dev(bits), to_dev(lengths)
+    out = tk.topk_select_bf16(s, l, k)
+    torch.cuda.synchronize()
+    assert_parity(vals, lengths, k, out.cpu().numpy(), run_oracle(vals, lengths, k))
+    rng = np.random.default_rng(width * 7 + k)
+    pages = -(-width // 7)
+    pt = rng.permutation(scores.shape[0] * pages).astype(np.int32).reshape(scores.shape[0], pages)
+    out = tk.topk_select_bf16(s, l, k, to_dev(pt), 7)
+    torch.cuda.synchronize()
+    assert_parity(vals, lengths, k, out.cpu().numpy(), run_oracle(vals, lengths, k, pt, 7), page_table=pt)
+
+
+@pytest.mark.parametrize("width,k", [(8192, 512), (16384, 2048)])
+def test_bf16_and_fp32_kernels_agree(width, k):
+    """The BF16 kernel's 16-bit keys are the high halves of the FP32 keys of
+    the same values, with the same tie rule: on BF16-representable scores it
+    returns exactly what the FP32 short-row kernel returns, slot by slot."""
+    scores, lengths = _short_rows(width)
+    bits = to_bf16_bits(scores)
+    vals = np.ascontiguousarray(bf16_bits_to_float(bits))
+    got16 = tk.topk_select_bf16(_bf16_dev(bits), to_dev(lengths), k)
+    got32 = tk.topk_select_ex(to_dev(vals), to_dev(lengths), k, short_rows=1)
+    torch.cuda.synchronize()
+    assert torch.equal(got16, got32)
+
+
+def test_bf16_deterministic_over_100_calls():
+    w = make_workload(6, B=300)
+    bits = to_bf16_bits(w.scores)
+    s, l = _bf16_dev(bits), to_dev(w.lengths)
+    first = tk.topk_select_bf16(s, l, w.k).clone()
+    for _ in range(99):
+        assert torch.equal(tk.topk_select_bf16(s, l, w.k), first)
+    torch.cuda.synchronize()
