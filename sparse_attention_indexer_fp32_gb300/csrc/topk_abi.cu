@@ -21,7 +21,7 @@ constexpr int kDefaultSampleMinN = 8192;
 // FP32 rows of at most this width take the short-row kernel by default (its
 // whole range). On the dispatch sweep it is faster than the streaming kernel
 // at every width up to 16384 from a few hundred rows on: B = 2048 rows of
-// 80-100 % of 16384 at k = 2048, 67 against 80 us; of 8192, 34 against 123 us.
+// 80-100 % of 16384 at k = 2048, 62 against 78 us; of 8192, 32 against 122 us.
 constexpr int64_t kShortAutoWidth = 16384;
 // Default margin of the sampled rank, in standard deviations. At 5 a row
 // whose sampled cutoff lands above its k-th largest score (and is streamed
