@@ -31,8 +31,10 @@
  * Preconditions that are not checked (they would need a device read):
  *   - no NaN in scores[b, 0 .. n_b); values past n_b never affect the result
  *     (rows of at most 16384 scores that start on 16 bytes may have the rest
- *     of the 16-byte block holding their last score read, never beyond the
- *     row's stride);
+ *     of the 16-byte block holding their last score read: when the stride is
+ *     not a multiple of 16 bytes that is up to 12 bytes past the row's
+ *     stride, past the end of `scores` for its last row, but never on
+ *     another page);
  *   - paged: every mapped slot fits in int32 (see topk_paged).
  *
  * Memory and execution:

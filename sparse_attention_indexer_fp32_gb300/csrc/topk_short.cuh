@@ -297,10 +297,11 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? (KMAX <= 1024 ? 5 : 4) : 3
   if (aligned) {
     // Every vector load is issued unconditionally, so that all of them are in
     // flight together: a vector that starts at or past the row's end re-reads
-    // the row's first vector instead (an L1 hit) and is masked off below. A
-    // row that starts on 16 bytes has a stride that is a whole number of
-    // vectors, so the vector holding the last score lies inside the row's
-    // stride; its scores past the length are masked off too.
+    // the row's first vector instead (an L1 hit) and is masked off below.
+    // The vector holding the last score is the 16-byte block around it: it
+    // can end up to 12 bytes past the row's stride when the stride is not a
+    // whole number of vectors (never on another page); its scores past the
+    // length are masked off too.
 #pragma unroll
     for (int q = 0; q < NQ; ++q) {
       const int v0 = static_cast<int>(index_of(q, 0));
