@@ -712,7 +712,7 @@ def sweep_markdown(doc: dict) -> str:
              f"launch cost; small shapes stay in L2). Times in us per call. `frac` = algorithmic "
              f"bytes / time / {peak:.0f} GB/s.",
              "",
-             "Clusters resident at once (the driver's answer, ragged kernel): " +
+             "Clusters resident at once (the CUDA driver's answer, ragged kernel): " +
              ", ".join(f"{n} {v}" for n, v in doc.get("max_active_clusters", {}).items()) + ".",
              ""]
     lines += ["## Automatic policy against the best forced path (ragged lengths)", "",

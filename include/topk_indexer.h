@@ -253,7 +253,7 @@ topk_status topk_select_noalloc(const float* scores, int64_t stride, const int32
  * topk_max_active_clusters - diagnostic: writes to *clusters how many
  * thread-block clusters of cluster_size (2, 4, 8 or 16) CTAs of the streaming
  * kernel for this k (ragged output when paged == 0, paged otherwise) can be
- * resident at once on the current device, as the driver answers it
+ * resident at once on the current device, as the CUDA driver answers it
  * (cudaOccupancyMaxActiveClusters; the CTAs of a cluster must share one GPC,
  * so this can be less than the SM count times the CTAs per SM, divided by
  * the cluster size). The automatic policy gives a row a cluster only while

@@ -11,7 +11,7 @@ CUDA kernels (``_build/libtopk_indexer.so``):
 * :func:`amax8_varlen`, :func:`sort_candidate_blocks` - the two-level
   indexer's block-max keys and sorted candidate block table;
 * :func:`topk_select_ex` - diagnostics: a forced internal path, path counters;
-  :func:`max_active_clusters` - the driver's cluster residency per size.
+  :func:`max_active_clusters` - the CUDA driver's cluster residency per size.
 
 PyTorch only provides device memory and streams.
 """

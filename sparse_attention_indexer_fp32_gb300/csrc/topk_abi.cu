@@ -105,7 +105,7 @@ int max_clusters(int kmax, bool paged, int G, int dev) {
 
 // CTAs per row when the batch is too small to occupy the GPU: the largest
 // cluster size G in {16, 8, 4} whose clusters for every row fit on the GPU at
-// once (the driver's answer for clusters of that size, which must each sit
+// once (the CUDA driver's answer for clusters of that size, which must each sit
 // in one GPC) while every CTA keeps a long slice of the row; else one CTA per
 // row. Clusters of 2 are never chosen: on the dispatch sweep they were never
 // faster than one CTA per row, two split halves, or clusters of 4.

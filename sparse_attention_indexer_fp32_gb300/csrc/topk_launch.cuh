@@ -42,7 +42,7 @@ topk_status prepare_variant(int dev) {
 }
 
 // Clusters of G CTAs of this variant that can be resident at once on device
-// `dev`, as the driver answers it (cudaOccupancyMaxActiveClusters): a
+// `dev`, as the CUDA driver answers it (cudaOccupancyMaxActiveClusters): a
 // cluster's CTAs must share one GPC, so this can fall short of the SM count
 // times the CTAs per SM, divided by G. Found once per device; 0 when none fit
 // or the query fails.

@@ -455,7 +455,7 @@ def test_cuda_graph_replay_with_mutated_lengths(paged, split):
 
 
 def test_cluster_residency_answers():
-    """The driver's cluster residency answers that the automatic policy uses:
+    """The CUDA driver's cluster residency answers that the automatic policy uses:
     clusters of 2, 4 and 8 fit; larger clusters never fit more at once."""
     for k in (512, 2048):
         for paged in (False, True):
