@@ -233,3 +233,41 @@ def test_bf16_deterministic_over_100_calls():
     for _ in range(99):
         assert torch.equal(tk.topk_select_bf16(s, l, w.k), first)
     torch.cuda.synchronize()
+
+
+def _group_rows(width, rng):
+    """Rows whose cutoff falls inside the coarse bin of [1, 1.25) (or of
+    (-1.25, -1]) with that bin's entries in group 0, in group 63, across all
+    64 groups of 32 second-pass bins, or sharing their top 22 key bits (a
+    third pass); the rest of each row far below."""
+    def fill(m_lo, m_hi, count, sign=1.0):
+        m = rng.integers(m_lo, m_hi, size=count, dtype=np.int64)
+        x = (1.0 + m.astype(np.float64) * 2.0 ** -23).astype(np.float32)
+        return sign * x
+    rows = []
+    for sign in (1.0, -1.0):
+        for lo, hi in ((0, 1 << 15), (63 << 15, 64 << 15), (0, 1 << 21), (0, 1 << 10)):
+            r = np.full(width, -8.0 if sign > 0 else -64.0, dtype=np.float32)
+            pos = rng.choice(width, size=900, replace=False)
+            r[pos] = fill(lo, hi, 900, sign)
+            rows.append(r)
+    return np.stack(rows)
+
+
+@pytest.mark.parametrize("width", [8192, 16384])
+@pytest.mark.parametrize("k", [512, 700, 2048])
+def test_short_rows_grouped_second_pass_extremes(width, k):
+    """The second pass's group sums at their extremes (every entry of the
+    cutoff bin in the first or the last group of 32 bins, or spread over all
+    64) and a third pass over a shared 22-bit prefix, for positive and
+    negative cutoffs, on the short-row kernel and through the default call."""
+    rng = np.random.default_rng(width + k)
+    scores = _group_rows(width, rng)
+    lengths = np.full(scores.shape[0], width, dtype=np.int32)
+    lengths[1::3] = width - 7
+    cnt = counters_tensor()
+    check_against_oracle(scores, lengths, k, short_rows=1, counters=cnt)
+    assert int(cnt[tk.Counter.SHORT_ROWS]) == scores.shape[0]
+    out = tk.topk_ragged(to_dev(scores), to_dev(lengths), k)
+    torch.cuda.synchronize()
+    assert_parity(scores, lengths, k, out.cpu().numpy(), run_oracle(scores, lengths, k))
