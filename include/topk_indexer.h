@@ -284,8 +284,8 @@ int32_t topk_abi_version(void);
  *   stash_capacity  0 = default; otherwise the candidate-buffer size to use,
  *                   in [k + 2048, default]: small values force the in-buffer
  *                   compaction path on ordinary inputs. The default is
- *                   min(b + 4096, 5120) entries, b = 512, 1024 or 2048 the
- *                   smallest of these not below k
+ *                   b + 2048 entries for b = 512 and min(b + 4096, 5120)
+ *                   for b = 1024 or 2048, b the smallest of these not below k
  *   sample_z        0 = default margin; otherwise the number of standard
  *                   deviations added to the sampled rank (negative values make
  *                   the sampled cutoff too high and force the full rescan)

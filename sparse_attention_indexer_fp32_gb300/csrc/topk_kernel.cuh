@@ -58,7 +58,7 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kStageFloats = 4096;                     // one ring stage: 16 KiB of scores
 constexpr int kPerThread = kStageFloats / kThreads;    // 16 consecutive scores per thread
-constexpr int kStages = 4;                             // ring depth: 64 KiB
+constexpr int kStages = 4;                             // ring depth: 64 KiB (k > 512; see RingStages)
 constexpr int kSampleVec4 = 1024;                    // 4096 sampled scores ...
 constexpr int kSampleChunkVec4 = 64;                 // ... in 16 chunks of 256
 constexpr int kSampleChunks = kSampleVec4 / kSampleChunkVec4;
@@ -91,28 +91,39 @@ enum : int {
 // Entry count a split-row half hands over when one of its waits timed out.
 constexpr uint32_t kHalfFailed = 0xffffffffu;
 
+// Smallest stash capacity beyond k: the hits of half a CTA on one stage.
+constexpr int kMinStashRoom = kStageFloats / 2;
+
 template <int KMAX>
 struct StashCap {
   // (a multiple of kRoundPerThread, as the round reads assume)
-  // Room for k kept candidates plus the new ones of one stage, at most 5120
-  // entries so that two CTAs with a four-stage ring fit on an SM.
-  static constexpr int value = KMAX + kStageFloats < 5120 ? KMAX + kStageFloats : 5120;
+  // k <= 512: room for k kept candidates plus half a stage of new ones (a
+  // sampled cutoff keeps ~800 entries), so that a fifth ring stage fits.
+  // Larger k: room for k plus one stage, at most 5120 entries, so that two
+  // CTAs with a four-stage ring fit on an SM.
+  static constexpr int value = KMAX <= 512 ? KMAX + kMinStashRoom
+                                           : (KMAX + kStageFloats < 5120 ? KMAX + kStageFloats : 5120);
+};
+
+// Ring stages of the k bucket: the smaller stash of k <= 512 leaves shared
+// memory for a fifth (80 KiB in flight per CTA; a CTA whose SM neighbour is
+// in its fixed per-row phases streams faster).
+template <int KMAX>
+struct RingStages {
+  static constexpr int value = KMAX <= 512 ? 5 : kStages;
 };
 static_assert(StashCap<512>::value % kRoundPerThread == 0 && StashCap<1024>::value % kRoundPerThread == 0 &&
                   StashCap<2048>::value % kRoundPerThread == 0,
               "round reads must stay inside the stash");
-// Smallest stash capacity beyond k: the hits of half a CTA on one stage.
-constexpr int kMinStashRoom = kStageFloats / 2;
-
-template <int C>
+template <int C, int NS>
 struct __align__(128) Smem {
-  float ring[kStages][kStageFloats];
+  float ring[NS][kStageFloats];
   uint32_t skey[C];
   uint32_t sidx[C];
   uint32_t hist[kBins];
-  uint64_t full[kStages];
+  uint64_t full[NS];
   uint64_t never;                   // an mbarrier nothing arrives on (the wait-limit test)
-  uint32_t rel[kStages];            // warps done with each ring slot (the last one refills it)
+  uint32_t rel[NS];                 // warps done with each ring slot (the last one refills it)
   uint32_t issued;                  // stages issued into the ring (for the error drain)
   uint32_t tab[2][kWarps];          // per-group per-warp packed hit counts and wait-error flags
   uint32_t rtab[2][kWarps];         // per-round per-warp (above << 16 | tied) counts
@@ -187,7 +198,7 @@ __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
 }
 
 // The helpers below take any shared-memory layout SM with the members they
-// use (scan, res, hist, skey, sidx, rtab): the streaming kernel's Smem<C>
+// use (scan, res, hist, skey, sidx, rtab): the streaming kernel's Smem<C, NS>
 // and the short-row kernel's layout.
 template <class SM>
 __device__ __forceinline__ uint32_t block_incl_scan(uint32_t v, SM& S) {
@@ -456,8 +467,9 @@ __device__ void emit_rounds(SM& S, int n, Cut cut, uint32_t gt0, uint32_t eq0, S
 template <int KMAX, int G, bool PAGED>
 __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) {
   constexpr int C = StashCap<KMAX>::value;
+  constexpr int NS = RingStages<KMAX>::value;  // ring stages
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  Smem<C>& S = *reinterpret_cast<Smem<C>*>(smem_raw);
+  Smem<C, NS>& S = *reinterpret_cast<Smem<C, NS>*>(smem_raw);
 
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
   // The row, and which of its `parts` contiguous slices this CTA streams:
@@ -571,9 +583,9 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
   }
 
   // Ring bookkeeping. Stage j of a pass goes to slot (pass start + j - s0) %
-  // kStages; `consumed` (stages taken from the ring so far) is uniform.
+  // NS; `consumed` (stages taken from the ring so far) is uniform.
   // Thread 0 fills the ring at the start of a pass; afterwards the last warp
-  // to finish with a slot refills it with the stage kStages further on.
+  // to finish with a slot refills it with the stage NS further on.
   uint32_t consumed = 0, t0_seen = 0;
   bool abort = false;
 
@@ -587,25 +599,25 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
   };
   auto prime = [&]() {
     if (t == 0 && !abort) {
-      const int m = min(s1 - s0, kStages);
+      const int m = min(s1 - s0, NS);
       fence_proxy_async_smem();
-      for (int u = 0; u < m; ++u) issue_stage(s0 + u, (consumed + u) % kStages);
+      for (int u = 0; u < m; ++u) issue_stage(s0 + u, (consumed + u) % NS);
       S.issued += m;
     }
   };
   // Called by every thread once it no longer reads ring slot `slot` (stage
   // j) nor, when `two`, the next slot (stage j + 1). The last warp refills
-  // both with the stages kStages further on.
+  // both with the stages NS further on.
   auto release_slots = [&](int j, uint32_t slot, bool two) {
     __syncwarp();
     if (lane == 0 && atom_add_acq_rel_cta(&S.rel[slot], 1u) == kWarps - 1) {
       S.rel[slot] = 0;
-      if (!abort && j + kStages < s1) {
+      if (!abort && j + NS < s1) {
         fence_proxy_async_smem();
-        issue_stage(j + kStages, slot);
+        issue_stage(j + NS, slot);
         uint32_t m = 1;
-        if (two && j + 1 + kStages < s1) {
-          issue_stage(j + 1 + kStages, (slot + 1) % kStages);
+        if (two && j + 1 + NS < s1) {
+          issue_stage(j + 1 + NS, (slot + 1) % NS);
           ++m;
         }
         atomicAdd(&S.issued, m);
@@ -614,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
   };
   if (t == 0) {
 #pragma unroll
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < NS; ++s) {
       mbar_init(&S.full[s], 1);
       S.rel[s] = 0;
     }
@@ -847,8 +859,8 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
   // thread's 16 scores in it, with the mask of those present.
   const bool probing = p.probe_stage >= 0;  // test only
   auto take_stage = [&](int j, bool& err, uint32_t& valid, uint32_t& slot) -> const float* {
-    slot = consumed % kStages;
-    const uint32_t parity = (consumed / kStages) & 1u;
+    slot = consumed % NS;
+    const uint32_t parity = (consumed / NS) & 1u;
     ++consumed;
     if (!abort) {
       if (probing && j - s0 == p.probe_stage) {
@@ -918,7 +930,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
   auto drain = [&]() {
     if (abort && t == 0) {
       for (uint32_t u = t0_seen; u < S.issued; ++u)
-        (void)mbar_wait_bounded(&S.full[u % kStages], (u / kStages) & 1u, kWaitLimitNs);
+        (void)mbar_wait_bounded(&S.full[u % NS], (u / NS) & 1u, kWaitLimitNs);
       if (p.counters != nullptr) atomicAdd(&p.counters[kCntDeviceErrors], 1u);
     }
   };

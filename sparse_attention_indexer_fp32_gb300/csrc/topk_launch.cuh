@@ -31,7 +31,7 @@ topk_status prepare_variant(int dev) {
   std::atomic<uint64_t>& flags = attr_flags<KMAX, G, PAGED>();
   if ((flags.load(std::memory_order_acquire) & bit) == 0) {
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(sizeof(Smem<C>))) != cudaSuccess)
+                             static_cast<int>(sizeof(Smem<C, RingStages<KMAX>::value>))) != cudaSuccess)
       return TOPK_ECUDA;
     if (G > 8 && cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
                      cudaSuccess)
@@ -56,7 +56,7 @@ int max_active_clusters_variant(int dev) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(G, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = sizeof(Smem<StashCap<KMAX>::value>);
+    cfg.dynamicSmemBytes = sizeof(Smem<StashCap<KMAX>::value, RingStages<KMAX>::value>);
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = G;
@@ -77,7 +77,7 @@ template <int KMAX, int G, bool PAGED>
 topk_status launch_variant(const Params& p, int dev, cudaStream_t stream) {
   constexpr int C = StashCap<KMAX>::value;
   auto kernel = topk_rows_kernel<KMAX, G, PAGED>;
-  const size_t smem = sizeof(Smem<C>);
+  const size_t smem = sizeof(Smem<C, RingStages<KMAX>::value>);
   const topk_status prep = prepare_variant<KMAX, G, PAGED>(dev);
   if (prep != TOPK_OK) return prep;
   cudaLaunchConfig_t cfg = {};

@@ -142,7 +142,8 @@ def test_debug_option_checks_need_no_gpu(lib):
 
     bad = [
         dict(sample_mode=-1), dict(sample_mode=3),
-        dict(stash_capacity=512 + 2047), dict(stash_capacity=512 + 4096 + 1),  # [k + 2048, default]
+        dict(stash_capacity=512 + 2047), dict(stash_capacity=512 + 2048 + 1),  # [k + 2048, default]
+        dict(stash_capacity=512 + 4096 + 1),
         dict(cluster_size=3), dict(cluster_size=32), dict(cluster_size=-1),
         dict(counters=0x1002),  # misaligned
         dict(probe_stage=-1), dict(probe_stage=1, probe_wait_us=0),

@@ -212,7 +212,7 @@ def test_capacity_boundaries_without_sampling():
     """Row lengths around the candidate-buffer capacity: the buffer fills
     exactly, one short of, and one past its end."""
     rng = np.random.default_rng(11)
-    for k, cap in ((512, 4608), (1024, 5120), (2048, 5120)):
+    for k, cap in ((512, 2560), (1024, 5120), (2048, 5120)):
         ns = [cap - 1, cap, cap + 1, cap + 2047, cap + 2048, cap + 2049, 2 * cap + 5]
         stride = max(ns) + 3
         scores = rng.standard_normal((len(ns), stride)).astype(np.float32)
