@@ -280,7 +280,8 @@ int32_t topk_abi_version(void);
  *                   2 use it on every row long enough to sample
  *   cluster_size    0 automatic, 1 one CTA per row, or 2 / 4 / 8 / 16 CTAs
  *                   of a thread-block cluster per row (16 is a non-portable
- *                   cluster size; the automatic policy uses at most 8)
+ *                   cluster size; the automatic policy takes 16 only for
+ *                   batches of a few long rows)
  *   stash_capacity  0 = default; otherwise the candidate-buffer size to use,
  *                   in [k + 2048, default]: small values force the in-buffer
  *                   compaction path on ordinary inputs. The default is

@@ -36,6 +36,15 @@ constexpr float kDefaultSampleZ = 5.0f;
 constexpr int64_t kMinClusterSlice = 16384;
 constexpr int64_t kMinClusterSliceWide = 32768;
 constexpr int32_t kSmallClusterBatch = 16;
+// A handful of rows of at least 65536 scores take clusters of 16 down to
+// 4096-score slices: on the sweep, one and four rows of 65536 to 196608 ran
+// 5-11 % faster on clusters of 16 than on the 8 or 4 that the slice floor
+// above allows (one row of 131072 at k = 512: 13.1 against 14.1 us); 32768
+// wide rows stay fastest on one CTA each, and at 16 rows clusters of 16 no
+// longer fit at once.
+constexpr int32_t kTinyClusterBatch = 4;
+constexpr int64_t kMinTinyClusterWidth = 65536;
+constexpr int64_t kMinClusterSliceTiny = 4096;
 // Workspace layout: per split row one arrival counter (the first 4 KiB,
 // which persist between calls and are zero outside a call), two hand-over
 // counts (the next 8 KiB), then per split row and half k keys and k indices.
@@ -110,7 +119,9 @@ int max_clusters(int kmax, bool paged, int G, int dev) {
 // row. Clusters of 2 are never chosen: on the dispatch sweep they were never
 // faster than one CTA per row, two split halves, or clusters of 4.
 int auto_cluster_size(int32_t B, int64_t stride, int kmax, bool paged, int dev) {
-  const int64_t slice_min = B <= kSmallClusterBatch ? kMinClusterSlice : kMinClusterSliceWide;
+  const int64_t slice_min = (B <= kTinyClusterBatch && stride >= kMinTinyClusterWidth) ? kMinClusterSliceTiny
+                            : B <= kSmallClusterBatch                                  ? kMinClusterSlice
+                                                                                        : kMinClusterSliceWide;
   for (int G = 16; G >= 4; G /= 2) {
     if (stride / G < slice_min) continue;
     const int fit = max_clusters(kmax, paged, G, dev);
