@@ -29,22 +29,25 @@ constexpr int64_t kShortAutoWidth = 16384;
 // the 131072-wide rows but makes such a rescan (a latency spike) a few-percent
 // event per call, 6 keeps ~6 % more candidates.
 constexpr float kDefaultSampleZ = 5.0f;
-// A cluster CTA's slice of the row should hold at least this many scores:
-// 16384 for batches of at most kSmallClusterBatch rows, 32768 for larger
-// ones (the sweep: 64 rows of 65536 took 19.2 us on clusters of 4 and 15.7
-// us on one CTA per row; 64 rows of 131072, 21.1 against 23.9 us).
-constexpr int64_t kMinClusterSlice = 16384;
+// Cluster sizes for batches too small to occupy the GPU with one CTA per
+// row, from the dispatch sweep (B = 1, 4, 8, 16, 32 and 64 rows of 65536 to
+// 262144 scores, k = 512 / 1024 / 2048):
+//  - rows under 65536 scores stay on one CTA each (32768-wide rows: one CTA
+//    per row was fastest at every batch);
+//  - up to 4 rows: clusters of 16 (one row of 131072 at k = 512: 13.1 us
+//    against 14.1 on 8);
+//  - up to 8 rows: 8 (8 rows of 262144 at k = 2048: 20.2 us against 24.0 on
+//    16, which stop fitting well past a handful of rows);
+//  - up to 16 rows: 4, except 8 for k <= 512 from 196608 scores (16 rows of
+//    131072 at k = 2048: 19.4 against 22.1 us on 8; of 196608 at k = 512:
+//    17.6 on 8 against 19.7 on 4);
+//  - up to 32 rows: 4 from 131072 scores (32 rows of 262144 at k = 2048: 26.7
+//    against 29.6 us on 8), else one CTA per row;
+//  - more rows: 4 while each CTA keeps at least 32768 scores (64 rows of
+//    131072: 21.1 against 23.9 us on one CTA; 64 rows of 65536: 19.2 on 4
+//    against 15.7 on one).
+constexpr int64_t kMinClusterWidth = 65536;
 constexpr int64_t kMinClusterSliceWide = 32768;
-constexpr int32_t kSmallClusterBatch = 16;
-// A handful of rows of at least 65536 scores take clusters of 16 down to
-// 4096-score slices: on the sweep, one and four rows of 65536 to 196608 ran
-// 5-11 % faster on clusters of 16 than on the 8 or 4 that the slice floor
-// above allows (one row of 131072 at k = 512: 13.1 against 14.1 us); 32768
-// wide rows stay fastest on one CTA each, and at 16 rows clusters of 16 no
-// longer fit at once.
-constexpr int32_t kTinyClusterBatch = 4;
-constexpr int64_t kMinTinyClusterWidth = 65536;
-constexpr int64_t kMinClusterSliceTiny = 4096;
 // Workspace layout: per split row one arrival counter (the first 4 KiB,
 // which persist between calls and are zero outside a call), two hand-over
 // counts (the next 8 KiB), then per split row and half k keys and k indices.
@@ -112,20 +115,30 @@ int max_clusters(int kmax, bool paged, int G, int dev) {
   }
 }
 
-// CTAs per row when the batch is too small to occupy the GPU: the largest
-// cluster size G in {16, 8, 4} whose clusters for every row fit on the GPU at
-// once (the CUDA driver's answer for clusters of that size, which must each sit
-// in one GPC) while every CTA keeps a long slice of the row; else one CTA per
-// row. Clusters of 2 are never chosen: on the dispatch sweep they were never
-// faster than one CTA per row, two split halves, or clusters of 4.
+// CTAs per row when the batch is too small to occupy the GPU (the table
+// above), shrunk while the clusters of every row would not fit on the GPU at
+// once (the CUDA driver's answer for clusters of that size, which must each
+// sit in one GPC). Clusters of 2 are never chosen: on the dispatch sweep they
+// were never faster than one CTA per row, two split halves, or clusters of 4.
 int auto_cluster_size(int32_t B, int64_t stride, int kmax, bool paged, int dev) {
-  const int64_t slice_min = (B <= kTinyClusterBatch && stride >= kMinTinyClusterWidth) ? kMinClusterSliceTiny
-                            : B <= kSmallClusterBatch                                  ? kMinClusterSlice
-                                                                                        : kMinClusterSliceWide;
-  for (int G = 16; G >= 4; G /= 2) {
-    if (stride / G < slice_min) continue;
+  int G = 1;
+  if (B <= 32 && stride >= kMinClusterWidth) {
+    if (B <= 4) {
+      G = 16;
+    } else if (B <= 8) {
+      G = 8;
+    } else if (B <= 16) {
+      G = (kmax <= 512 && stride >= 196608) ? 8 : 4;
+    } else {
+      G = stride >= 131072 ? 4 : 1;
+    }
+  } else if (stride / 4 >= kMinClusterSliceWide) {
+    G = 4;
+  }
+  while (G >= 4) {
     const int fit = max_clusters(kmax, paged, G, dev);
     if (fit > 0 && B <= fit) return G;
+    G /= 2;
   }
   return 1;
 }

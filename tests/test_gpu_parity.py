@@ -465,8 +465,10 @@ def test_cluster_residency_answers():
 
 
 @pytest.mark.parametrize("B,stride,clustered", [(1, 262144, True), (4, 131072, True),
-                                                (2, 65536, True), (64, 131072, True),
-                                                (4, 32768, False), (64, 65536, False),
+                                                (2, 65536, True), (8, 262144, True),
+                                                (16, 131072, True), (32, 131072, True),
+                                                (64, 131072, True), (4, 32768, False),
+                                                (32, 65536, False), (64, 65536, False),
                                                 (200, 262144, False)])
 def test_automatic_cluster_policy(B, stride, clustered):
     """Small batches of long rows run on clusters, short rows and larger
