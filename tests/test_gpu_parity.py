@@ -466,7 +466,9 @@ def test_cluster_residency_answers():
 
 @pytest.mark.parametrize("B,stride,clustered", [(1, 262144, True), (4, 131072, True),
                                                 (2, 65536, True), (8, 262144, True),
-                                                (16, 131072, True), (32, 131072, True),
+                                                (5, 131072, True), (9, 196608, True),
+                                                (16, 131072, True), (17, 131072, True),
+                                                (32, 131072, True), (33, 131072, True),
                                                 (64, 131072, True), (4, 32768, False),
                                                 (32, 65536, False), (64, 65536, False),
                                                 (200, 262144, False)])
