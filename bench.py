@@ -573,7 +573,7 @@ def cpu_baseline_parallel(config: int, rows_per_core: int = 8):
 # ------------------------------------------------------------- dispatch sweep
 
 SWEEP_WIDTHS = (4096, 8192, 16384, 32768, 65536, 131072, 196608, 262144)
-SWEEP_BATCHES = (1, 4, 8, 16, 32, 64, 256, 1024, 2048)
+SWEEP_BATCHES = (1, 4, 8, 16, 32, 48, 64, 96, 128, 192, 256, 1024, 2048)
 SWEEP_KS = (512, 1024, 2048)
 SWEEP_MAX_ELEMS = 2048 * 262144  # 2 GiB of scores at most
 

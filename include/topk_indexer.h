@@ -125,9 +125,10 @@ topk_status topk_paged(const float* scores, int64_t stride, const int32_t* lengt
  * pages' cluster split (sglang PR 39648 report, 实现拆解 4) needs the CTAs of a
  * row to run together.
  *
- * The library chooses how many rows to split from B and the SM count (none
- * when the batch leaves no idle slot, or when rows are short), at most as
- * many as the workspace holds.
+ * The library chooses how many rows to split from B, the row width, k and
+ * the SM count (none when one CTA per row already keeps HBM busy, or when
+ * rows are short), at most as many as the workspace holds; a few dozen long
+ * rows that it can all split are split rather than given clusters.
  *
  *   workspace        DEVICE memory owned by the caller, 16-byte aligned, at
  *                    least 12 KiB. Its first 4 KiB must be zero before its

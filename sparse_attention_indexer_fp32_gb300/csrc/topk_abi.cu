@@ -61,20 +61,37 @@ size_t ws_bytes_for(int32_t k, int64_t split_rows) {
   return kWsHeaderBytes + static_cast<size_t>(split_rows) * 2 * static_cast<size_t>(k) * 8;
 }
 
-// Rows narrower than this are not split: each half pays the fixed costs of
-// a row (sampling, hand-over, and for one of them the merge), which on GB300
-// outweighs the shorter tail unless a half still streams ~80K scores or more
-// (measured: a gain at width 262144, a loss at 131072).
-constexpr int64_t kMinSplitWidth = 196608;
+// Rows to split over two CTAs each (one-CTA rows only, with a workspace),
+// from the dispatch sweep. Each half pays a row's fixed costs (sampling, its
+// own cutoff, the hand-over; one of them the merge), so a split pays only
+// when it puts HBM bandwidth to work that one CTA per row leaves idle:
+//  - rows under 131072 scores: none (at 65536 one CTA per row was fastest at
+//    every batch);
+//  - a batch of at least one full wave of one-CTA rows (B >= slots, two CTAs
+//    per SM), rows of at least 196608 scores: the rows of the last partial
+//    wave, or the ones that fill its idle slots (the B = 1024 x 262144 line);
+//  - a partial wave: every row up to half the slots, then the rows that fill
+//    the idle slots, while one CTA per row would leave HBM short (up to ~200
+//    rows: 192 rows of 262144, 47.7 against 51.2 us unsplit; 256 rows, 52.1
+//    against 51.0 unsplit: none); at 131072 to 196608 scores only for k <=
+//    1024 beyond 74 rows (128 rows of 131072 at k = 2048: 29.6 split
+//    against 26.5 us unsplit; at k = 512: 23.0 against 23.9).
+constexpr int64_t kMinSplitWidth = 131072;
+constexpr int64_t kMinTailSplitWidth = 196608;
+constexpr int32_t kMaxPartialWaveSplitBatch = 200;
+constexpr int32_t kMaxWideKSplitBatch = 74;
 
-// Rows to split: enough of the last ones to fill the slots that the final
-// partial wave of one-CTA rows leaves idle, and no more (each split row takes
-// two slots).
-int auto_split_rows(int32_t B, int64_t stride, int sm_count) {
+int auto_split_rows(int32_t B, int64_t stride, int kmax, int sm_count) {
   const int64_t slots = static_cast<int64_t>(kCtasPerSm) * sm_count;
   if (stride < kMinSplitWidth || slots <= 0) return 0;
-  const int64_t r = B >= slots ? B % slots : B;
-  return static_cast<int>(r < slots - r ? r : slots - r);
+  if (B >= slots) {
+    if (stride < kMinTailSplitWidth) return 0;
+    const int64_t r = B % slots;
+    return static_cast<int>(r < slots - r ? r : slots - r);
+  }
+  if (B > kMaxPartialWaveSplitBatch) return 0;
+  if (stride < kMinTailSplitWidth && kmax > 1024 && B > kMaxWideKSplitBatch) return 0;
+  return static_cast<int>(B < slots - B ? B : slots - B);
 }
 
 struct DeviceInfo {
@@ -120,7 +137,13 @@ int max_clusters(int kmax, bool paged, int G, int dev) {
 // once (the CUDA driver's answer for clusters of that size, which must each
 // sit in one GPC). Clusters of 2 are never chosen: on the dispatch sweep they
 // were never faster than one CTA per row, two split halves, or clusters of 4.
-int auto_cluster_size(int32_t B, int64_t stride, int kmax, bool paged, int dev) {
+int auto_cluster_size(int32_t B, int64_t stride, int kmax, bool paged, int dev, bool can_split_all) {
+  // 41 to 74 rows of 131072 to 196608 scores: every row split in two, when a
+  // workspace holds them, beat clusters of 4 (64 rows of 131072 at k =
+  // 1024: 21.9 against 24.8 us; at 32 rows clusters of 4 still win).
+  if (can_split_all && B > 40 && B <= kMaxWideKSplitBatch && stride >= kMinSplitWidth &&
+      stride < 262144)
+    return 1;
   int G = 1;
   if (B <= 32 && stride >= kMinClusterWidth) {
     if (B <= 4) {
@@ -297,17 +320,20 @@ topk_status select_impl(const void* scores, bool bf16, int64_t stride, const int
   const topk_status st = device_info(&dev, &info);
   if (st != TOPK_OK) return st;
   if (split_rows > 0) G = 1;
-  if (G == 0) G = auto_cluster_size(B, stride, kmax, page_table != nullptr, dev);
+  const int64_t ws_room = workspace != nullptr
+                             ? static_cast<int64_t>((workspace_bytes - kWsHeaderBytes) / (static_cast<size_t>(k) * 16))
+                             : 0;
+  if (G == 0)
+    G = auto_cluster_size(B, stride, kmax, page_table != nullptr, dev,
+                          split_rows == 0 && ws_room >= B && B <= kMaxSplitRows);
   if (static_cast<int64_t>(B) * G > INT32_MAX) return TOPK_EINVAL;
 
   // Split rows: the last m rows each run as two independent CTAs.
   if (workspace != nullptr && G == 1 && split_rows >= 0) {
-    const int64_t room = static_cast<int64_t>((workspace_bytes - kWsHeaderBytes) /
-                                              (static_cast<size_t>(k) * 16));
-    const int64_t hold = room < kMaxSplitRows ? room : kMaxSplitRows;
+    const int64_t hold = ws_room < kMaxSplitRows ? ws_room : kMaxSplitRows;
     int64_t m = split_rows;
     if (m == 0) {
-      m = auto_split_rows(B, stride, info->sm_count);
+      m = auto_split_rows(B, stride, kmax, info->sm_count);
       if (m > hold) m = hold;
     } else if (m > hold) {
       return TOPK_EINVAL;
@@ -451,8 +477,12 @@ topk_status topk_select_noalloc(const float* scores, int64_t stride, const int32
   // (the same policy as the call it makes: rows of at most kShortMaxRow scores
   // take the short-row kernel, which splits nothing)
   const int kmax = k <= 512 ? 512 : (k <= 1024 ? 1024 : 2048);
-  const int G = stride <= kShortAutoWidth ? 0 : auto_cluster_size(B, stride, kmax, page_table != nullptr, dev);
-  const int m = G == 1 ? auto_split_rows(B, stride, info->sm_count) : 0;
+  const int64_t static_room = static_cast<int64_t>((kStaticWsBytes - kWsHeaderBytes) / (static_cast<size_t>(k) * 16));
+  const int G = stride <= kShortAutoWidth
+                    ? 0
+                    : auto_cluster_size(B, stride, kmax, page_table != nullptr, dev,
+                                        static_room >= B && B <= kMaxSplitRows);
+  const int m = G == 1 ? auto_split_rows(B, stride, kmax, info->sm_count) : 0;
   if (ws_bytes_for(k, m) > kStaticWsBytes) return TOPK_ESCRATCH;
   void* ws = nullptr;
   st = static_workspace(dev, cs, &ws);

@@ -482,3 +482,38 @@ def test_automatic_cluster_policy(B, stride, clustered):
     cnt = counters_tensor()
     check_against_oracle(scores, lengths, 512, counters=cnt)
     assert int(cnt[tk.Counter.CLUSTER_ROWS]) == (B if clustered else 0)
+
+
+def _sm_count():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+@pytest.mark.parametrize("B,stride,k,expect", [
+    (64, 131072, 1024, "all"),       # a few dozen rows: every row split, not clustered
+    (33, 131072, 1024, "clusters"),  # up to 40 rows: clusters of 4
+    (128, 131072, 512, "all"),       # up to half the slots: every row
+    (128, 131072, 2048, "none"),     # 131072 scores, k = 2048, beyond 74 rows: none
+    (192, 262144, 512, "fill"),      # beyond half the slots: the rows that fill the idle ones
+    (256, 262144, 512, "none"),      # beyond 200 rows one CTA per row keeps HBM busy
+])
+def test_automatic_split_policy(B, stride, k, expect):
+    """With a workspace the automatic policy splits the rows the dispatch
+    sweep found faster split, gives small batches clusters instead, and
+    matches the unsplit call and the oracle either way."""
+    slots = 2 * _sm_count()
+    want_split = {"all": B, "fill": slots - B, "none": 0, "clusters": 0}[expect]
+    rng = np.random.default_rng(B * 7 + k)
+    scores = rng.standard_normal((B, stride)).astype(np.float32)
+    lengths = rng.integers(stride * 4 // 5, stride + 1, B).astype(np.int32)
+    s, l = to_dev(scores), to_dev(lengths)
+    ws = torch.zeros(tk.workspace_bytes(k, B), dtype=torch.uint8, device="cuda:0")
+    cnt = counters_tensor()
+    got = tk.topk_select_ex(s, l, k, workspace=ws, counters=cnt)
+    want = tk.topk_select_ex(s, l, k, split_rows=-1)
+    torch.cuda.synchronize()
+    assert int(cnt[tk.Counter.SPLIT_ROWS]) == want_split
+    assert int(cnt[tk.Counter.CLUSTER_ROWS]) == (B if expect == "clusters" else 0)
+    assert torch.equal(got, want)
+    rows = np.array([0, B // 2, B - 1])
+    assert_parity(scores[rows], lengths[rows], k, got.cpu().numpy()[rows],
+                  run_oracle(scores[rows], lengths[rows], k), rows=rows)
