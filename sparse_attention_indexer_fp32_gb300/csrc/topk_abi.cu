@@ -138,9 +138,10 @@ int max_clusters(int kmax, bool paged, int G, int dev) {
 // sit in one GPC). Clusters of 2 are never chosen: on the dispatch sweep they
 // were never faster than one CTA per row, two split halves, or clusters of 4.
 int auto_cluster_size(int32_t B, int64_t stride, int kmax, bool paged, int dev, bool can_split_all) {
-  // 41 to 74 rows of 131072 to 196608 scores: every row split in two, when a
-  // workspace holds them, beat clusters of 4 (64 rows of 131072 at k =
-  // 1024: 21.9 against 24.8 us; at 32 rows clusters of 4 still win).
+  // 41 to 74 rows of 131072 to 196608 scores: every row split in two (when
+  // the split policy splits them all and a workspace holds them) beat
+  // clusters of 4 (64 rows of 131072 at k = 1024: 21.9 against 24.8 us; at
+  // 32 rows clusters of 4 still win).
   if (can_split_all && B > 40 && B <= kMaxWideKSplitBatch && stride >= kMinSplitWidth &&
       stride < 262144)
     return 1;
@@ -325,7 +326,8 @@ topk_status select_impl(const void* scores, bool bf16, int64_t stride, const int
                              : 0;
   if (G == 0)
     G = auto_cluster_size(B, stride, kmax, page_table != nullptr, dev,
-                          split_rows == 0 && ws_room >= B && B <= kMaxSplitRows);
+                          split_rows == 0 && ws_room >= B && B <= kMaxSplitRows &&
+                              auto_split_rows(B, stride, kmax, info->sm_count) == B);
   if (static_cast<int64_t>(B) * G > INT32_MAX) return TOPK_EINVAL;
 
   // Split rows: the last m rows each run as two independent CTAs.
@@ -481,7 +483,8 @@ topk_status topk_select_noalloc(const float* scores, int64_t stride, const int32
   const int G = stride <= kShortAutoWidth
                     ? 0
                     : auto_cluster_size(B, stride, kmax, page_table != nullptr, dev,
-                                        static_room >= B && B <= kMaxSplitRows);
+                                        static_room >= B && B <= kMaxSplitRows &&
+                                            auto_split_rows(B, stride, kmax, info->sm_count) == B);
   const int m = G == 1 ? auto_split_rows(B, stride, kmax, info->sm_count) : 0;
   if (ws_bytes_for(k, m) > kStaticWsBytes) return TOPK_ESCRATCH;
   void* ws = nullptr;
