@@ -19,6 +19,14 @@
 //     order) are written in index order.
 //  4. When b1 and above hold more entries than the stash (ties, narrow rows),
 //     the fine pass and a census run over the registers instead.
+//
+// A slot past the row's end holds key 0. Only a negative NaN has a key below
+// that of -inf (0x007f, bin 3), and NaN is excluded, so key 0 sits in bin 0,
+// below every score of the row: no pass needs a validity mask. The coarse
+// pass counts those slots in bin 0, which is never the cutoff's bin (the row
+// has more than k scores when the passes run), the filter and the census
+// compare against a bin or cut above it, and the fine passes take bin b1
+// only.
 #pragma once
 
 #include <cstdint>
@@ -118,7 +126,6 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? 6 : 4) topk_short_bf16_ker
   const int wbase = w * CH;
   auto index_of = [&](int j) -> uint32_t { return static_cast<uint32_t>(wbase + (j / V) * 32 * V + lane * V + j % V); };
   uint32_t kw[NKW];
-  uint32_t valid[NW];
   const bool aligned = (reinterpret_cast<uintptr_t>(rp) & 15u) == 0;
   if (aligned) {
 #pragma unroll
@@ -130,27 +137,25 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? 6 : 4) topk_short_bf16_ker
       kw[4 * q + 2] = bf16x2_keys(x.z);
       kw[4 * q + 3] = bf16x2_keys(x.w);
     }
-    if (wbase + CH <= n) {
+    if (wbase + CH > n) {  // warp-uniform: slots past the row's end get key 0
 #pragma unroll
-      for (int i = 0; i < NW; ++i) valid[i] = 0xffffffffu;
-    } else {
+      for (int q = 0; q < NQ; ++q) {
+        const int have = n - static_cast<int>(index_of(q * V));
 #pragma unroll
-      for (int i = 0; i < NW; ++i) valid[i] = 0;
-#pragma unroll
-      for (int j = 0; j < E; ++j) valid[j / 32] |= static_cast<uint32_t>(static_cast<int>(index_of(j)) < n) << (j % 32);
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t lo = 2 * i < have ? 0x0000ffffu : 0u, hi = 2 * i + 1 < have ? 0xffff0000u : 0u;
+          kw[4 * q + i] &= lo | hi;
+        }
+      }
     }
   } else {
-#pragma unroll
-    for (int i = 0; i < NW; ++i) valid[i] = 0;
 #pragma unroll
     for (int i = 0; i < NKW; ++i) {
       const int i0 = static_cast<int>(index_of(2 * i)), i1 = i0 + 1;
       const uint32_t lo = __ldg(rp + (i0 < n ? i0 : 0)), hi = __ldg(rp + (i1 < n ? i1 : 0));
-      kw[i] = bf16x2_keys(lo | (hi << 16));
-      valid[(2 * i) / 32] |= (static_cast<uint32_t>(i0 < n) | (static_cast<uint32_t>(i1 < n) << 1)) << ((2 * i) % 32);
+      kw[i] = bf16x2_keys(lo | (hi << 16)) & ((i0 < n ? 0x0000ffffu : 0u) | (i1 < n ? 0xffff0000u : 0u));
     }
   }
-  const bool full = aligned && wbase + CH <= n;
   for (int i = t; i < kBins / 4; i += kThreads) {
     reinterpret_cast<uint4*>(S.hist)[i] = make_uint4(0, 0, 0, 0);
     reinterpret_cast<uint4*>(S.hist2)[i] = make_uint4(0, 0, 0, 0);
@@ -170,22 +175,13 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? 6 : 4) topk_short_bf16_ker
   auto vec_bits = [&](const uint32_t (&m)[NW], int q) -> uint32_t {
     return (m[(q * V) / 32] >> ((q * V) % 32)) & ((1u << V) - 1u);
   };
-  auto vbit = [&](int j) -> bool { return (valid[j / 32] >> (j % 32)) & 1u; };
 
   // ---- 1. coarse bin (top 11 bits of the key) ----------------------------------
   uint32_t above, inbin;
-  if (full) {
 #pragma unroll
-    for (int i = 0; i < NKW; ++i) {
-      atomicAdd(&S.hist[(kw[i] >> 5) & 0x7ffu], 1u);
-      atomicAdd(&S.hist[kw[i] >> 21], 1u);
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < NKW; ++i) {
-      hist_add(S.hist, vbit(2 * i) ? ((kw[i] >> 5) & 0x7ffu) : 0xffffffffu);
-      hist_add(S.hist, vbit(2 * i + 1) ? (kw[i] >> 21) : 0xffffffffu);
-    }
+  for (int i = 0; i < NKW; ++i) {
+    atomicAdd(&S.hist[(kw[i] >> 5) & 0x7ffu], 1u);
+    atomicAdd(&S.hist[kw[i] >> 21], 1u);
   }
   const uint32_t b1 = find_bin_all<8>(S, S.hist, S.hist2, kk, &above, &inbin);
   uint32_t rem = kk - above;
@@ -203,8 +199,6 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? 6 : 4) topk_short_bf16_ker
       const uint32_t h2 = static_cast<uint32_t>((kw[i] << 16) >= LO) | (static_cast<uint32_t>(kw[i] >= LO) << 1);
       hit[(2 * i) / 32] |= h2 << ((2 * i) % 32);
     }
-#pragma unroll
-    for (int i = 0; i < NW; ++i) hit[i] &= valid[i];
     uint32_t cnt[NQ];
 #pragma unroll
     for (int q = 0; q < NQ; ++q) cnt[q] = __popc(vec_bits(hit, q));
@@ -297,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? 6 : 4) topk_short_bf16_ker
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const uint32_t key = half_key(kw[i], h);
-        hist_add(S.hist2, (vbit(2 * i + h) && (key >> 5) == b1) ? (key & 31u) : 0xffffffffu);
+        hist_add(S.hist2, (key >> 5) == b1 ? (key & 31u) : 0xffffffffu);
       }
     }
     __syncthreads();
@@ -315,11 +309,6 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? 6 : 4) topk_short_bf16_ker
     const uint32_t hi = half_key(kw[j / 2], j % 2) >> cut.shift;
     gtm[j / 32] |= static_cast<uint32_t>(hi > cut.P) << (j % 32);
     eqm[j / 32] |= static_cast<uint32_t>(hi == cut.P) << (j % 32);
-  }
-#pragma unroll
-  for (int i = 0; i < NW; ++i) {
-    gtm[i] &= valid[i];
-    eqm[i] &= valid[i];
   }
   uint32_t cg[NQ], ce[NQ];
 #pragma unroll
