@@ -211,6 +211,31 @@ def test_bf16_adversarial_rows(width, k):
     assert_parity(vals, lengths, k, out.cpu().numpy(), run_oracle(vals, lengths, k, pt, 7), page_table=pt)
 
 
+@pytest.mark.parametrize("width", [8192, 16384, 9001])
+@pytest.mark.parametrize("k", [1, 512, 2048])
+def test_bf16_rows_of_negative_infinity(width, k):
+    """Rows whose k-th largest score is -inf, the lowest key any score has
+    (slots past a row's end sit below it): ragged lengths that end inside a
+    warp's range, mixed with a few finite scores and with -max, the lowest
+    finite BF16 value."""
+    rng = np.random.default_rng(width + k)
+    lengths = np.array([width, width - 1, width - 77, 5000, 4097, 2049, k + 1, 3000], dtype=np.int32)
+    scores = np.full((lengths.size, width), np.nan, dtype=np.float32)
+    for i, n in enumerate(lengths):
+        scores[i, :n] = -np.inf
+    scores[1, rng.integers(0, lengths[1], 100)] = rng.standard_normal(100).astype(np.float32)
+    scores[2, :lengths[2]:5] = np.float32(-3.3895314e38)  # -max in BF16
+    scores[4, lengths[4] - 1] = 0.0
+    scores[5, 0] = -np.inf
+    scores[6, lengths[6] - 1] = np.float32(-3.3895314e38)
+    bits = to_bf16_bits(scores)
+    vals = bf16_bits_to_float(bits)
+    s, l = _bf16_dev(bits), to_dev(lengths)
+    out = tk.topk_select_bf16(s, l, k)
+    torch.cuda.synchronize()
+    assert_parity(vals, lengths, k, out.cpu().numpy(), run_oracle(vals, lengths, k))
+
+
 @pytest.mark.parametrize("width,k", [(8192, 512), (16384, 2048)])
 def test_bf16_and_fp32_kernels_agree(width, k):
     """The BF16 kernel's 16-bit keys are the high halves of the FP32 keys of
