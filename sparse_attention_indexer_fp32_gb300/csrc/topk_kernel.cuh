@@ -955,6 +955,11 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
         });
         handed = need;
       } else {
+        // Every thread reads stash entries that others wrote in the last
+        // group, after that group's barrier: wait for all of them (a half
+        // whose last group is a stage, with no scalar tail after it, has no
+        // barrier since).
+        __syncthreads();
         for (int e = t; e < static_cast<int>(n_st); e += kThreads) {
           p.ws_key[off + e] = S.skey[e];
           p.ws_idx[off + e] = S.sidx[e];

@@ -138,6 +138,36 @@ def test_split_rows_forced(k, sample_mode):
     assert not torch.any(ws[:4096]), "arrival counters must be left at zero"
 
 
+@pytest.mark.parametrize("k", [512, 1024, 2048])
+@pytest.mark.parametrize("paged", [False, True])
+def test_split_halves_that_hand_over_their_whole_stash(k, paged):
+    """Rows just longer than k, split: a half that holds no more than k
+    scores hands its whole stash over, right after its last stream group
+    (with no scalar tail after it when the row's start and length line up),
+    and the merge must see every entry of it. Rows at all four 4-byte
+    offsets, repeated calls, each against the oracle."""
+    rng = np.random.default_rng(k + paged)
+    B, stride = 64, 140003  # odd: the rows start at every 4-byte offset
+    lengths = (k + 1 + np.arange(B) % 4).astype(np.int32)
+    scores = np.full((B, stride), np.nan, dtype=np.float32)
+    for b in range(B):
+        x = rng.standard_normal(lengths[b]).astype(np.float32)
+        if b % 8 == 7:
+            x = np.round(x * 2) / 2  # ties at the cut
+        scores[b, :lengths[b]] = x
+    pt, ps = None, 0
+    if paged:
+        ps = 64
+        pages = -(-stride // ps)
+        pt = rng.permutation(B * pages).astype(np.int32).reshape(B, pages)
+    want = run_oracle(scores, lengths, k, pt, ps)
+    ws = _workspace(k, B)
+    for _ in range(10):
+        got = run_gpu(scores, lengths, k, pt, ps, split_rows=B, workspace=ws)
+        assert_parity(scores, lengths, k, got, want, page_table=pt)
+    assert not torch.any(ws[:4096])
+
+
 @pytest.mark.parametrize("k", [512, 2048])
 def test_split_rows_compaction_and_rescan(k):
     """Halves that compact their own candidate buffer (smallest capacity), and

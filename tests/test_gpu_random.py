@@ -1,0 +1,139 @@
+"""Seeded random cases through the automatic dispatch (needs an sm_103 GPU).
+
+The other GPU tests force each path or run the fixed workloads; here every
+case draws a batch size, a row width (1 to 300000), k, a length mode, value
+kinds with ties, infinities and signed zeros, a row start that may not sit on
+16 bytes, and paging, and lets the library choose its path (short-row kernel,
+sampled cutoff, clusters, split rows). Each result must equal the oracle's
+(identical -1 pattern, index set and value multiset), the split and unsplit
+calls must agree slot for slot, and a second call must repeat the first.
+Rows of at most 16384 scores also go through the BF16 entry point, compared
+with the oracle on the BF16-rounded values.
+"""
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from gpu_helpers import assert_parity, run_oracle, to_dev  # noqa: E402
+from synth import bf16_bits_to_float, to_bf16_bits  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - CPU-only machines
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import sparse_attention_indexer_fp32_gb300 as tk  # noqa: E402
+
+N_CASES = 64
+MAX_ELEMENTS = 12_000_000  # per case, so that the oracle's full sorts stay quick
+
+
+def _row_values(rng, kind, width):
+    if kind == 0:
+        return rng.standard_normal(width)
+    if kind == 1:  # an offset, as in the decode workload
+        return rng.standard_normal(width) + rng.uniform(-4, 4)
+    if kind == 2:  # few distinct values: ties at every cutoff
+        return rng.integers(-3, 4, width).astype(np.float64) * 0.25
+    if kind == 3:  # infinities and signed zeros over N(0,1)
+        x = rng.standard_normal(width)
+        pick = rng.integers(0, 8, width)
+        x[pick == 0] = np.inf
+        x[pick == 1] = -np.inf
+        x[pick == 2] = -0.0
+        x[pick == 3] = 0.0
+        return x
+    if kind == 4:
+        return np.arange(width, dtype=np.float64)
+    if kind == 5:
+        return -np.arange(width, dtype=np.float64)
+    if kind == 6:
+        return np.full(width, rng.standard_normal())
+    return np.where(rng.random(width) < 0.01, rng.uniform(3, 6, width), 0.0) + rng.standard_normal(width)
+
+
+def _lengths(rng, mode, B, width, k):
+    if mode == 0:
+        return np.full(B, width, dtype=np.int64)
+    if mode == 1:
+        lo = (8 * width + 9) // 10
+        return rng.integers(lo, width + 1, B)
+    if mode == 2:
+        return rng.integers(-2, width + 21, B)
+    return k + rng.integers(-1, 2, B)
+
+
+def _case(i):
+    rng = np.random.default_rng([0x5EED, 0xF022, i])
+    if rng.random() < 0.3:  # long rows: the sampled cutoff, clusters and split rows
+        width = int(rng.integers(65536, 300001))
+    else:
+        width = int(np.exp(rng.uniform(0.0, np.log(300000.0))))
+    B = int(np.exp(rng.uniform(0.0, np.log(1200.0))))
+    while B > 1 and B * width > MAX_ELEMENTS:
+        B //= 2
+    k = int(rng.choice([1, 2, 17, 100, 511, 512, 513, 1000, 1024, 2047, 2048, int(rng.integers(1, 2049))]))
+    lengths = _lengths(rng, int(rng.integers(0, 4)), B, width, k)
+    scores = np.full((B, width), np.nan, dtype=np.float32)
+    for b in range(B):
+        n = int(min(max(lengths[b], 0), width))
+        scores[b, :n] = _row_values(rng, int(rng.integers(0, 8)), n).astype(np.float32)
+    offset = int(rng.integers(0, 4))  # floats before row 0 in the device buffer
+    paged = bool(rng.integers(0, 2))
+    page_size = int(rng.choice([1, 7, 16, 64]))
+    pages = -(-width // page_size)
+    pt = rng.permutation(B * pages).astype(np.int32).reshape(B, pages) if paged else None
+    return scores, np.clip(lengths, -2**31, 2**31 - 1).astype(np.int32), k, offset, pt, page_size
+
+
+def _device_rows(scores, offset):
+    B, width = scores.shape
+    flat = np.full(B * width + 4, np.nan, dtype=np.float32)
+    flat[offset: offset + B * width] = scores.ravel()
+    return to_dev(flat)[offset: offset + B * width].view(B, width)
+
+
+@pytest.mark.parametrize("case", range(N_CASES))
+def test_random_case_through_the_automatic_path(case):
+    scores, lengths, k, offset, pt, page_size = _case(case)
+    s, l = _device_rows(scores, offset), to_dev(lengths)
+    if pt is None:
+        got = tk.topk_ragged(s, l, k)
+        again = tk.topk_ragged(s, l, k)
+        unsplit = tk.topk_ragged(s, l, k, split=False)
+        want = run_oracle(scores, lengths, k)
+    else:
+        dpt = to_dev(pt)
+        got = tk.topk_paged(s, l, k, dpt, page_size)
+        again = tk.topk_paged(s, l, k, dpt, page_size)
+        unsplit = tk.topk_paged(s, l, k, dpt, page_size, split=False)
+        want = run_oracle(scores, lengths, k, pt, page_size)
+    torch.cuda.synchronize()
+    assert torch.equal(got, again)
+    assert torch.equal(got, unsplit)
+    assert_parity(scores, lengths, k, got.cpu().numpy(), want, page_table=pt)
+
+
+@pytest.mark.parametrize("case", range(N_CASES))
+def test_random_case_in_bf16(case):
+    scores, lengths, k, offset, pt, page_size = _case(case)
+    if scores.shape[1] > 16384:
+        pytest.skip("BF16 rows hold at most 16384 scores")
+    bits = to_bf16_bits(scores)
+    vals = bf16_bits_to_float(bits)
+    B, width = bits.shape
+    flat = np.zeros(B * width + 8, dtype=np.uint16)
+    flat[offset: offset + B * width] = bits.ravel()
+    s = torch.from_numpy(flat.view(np.int16)).to("cuda:0")[offset: offset + B * width].view(B, width)
+    s = s.view(torch.bfloat16)
+    l = to_dev(lengths)
+    if pt is None:
+        got = tk.topk_select_bf16(s, l, k)
+        want = run_oracle(vals, lengths, k)
+    else:
+        got = tk.topk_select_bf16(s, l, k, to_dev(pt), page_size)
+        want = run_oracle(vals, lengths, k, pt, page_size)
+    torch.cuda.synchronize()
+    assert_parity(vals, lengths, k, got.cpu().numpy(), want, page_table=pt)
