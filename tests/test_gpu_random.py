@@ -7,8 +7,10 @@ kinds with ties, infinities and signed zeros, a row start that may not sit on
 sampled cutoff, clusters, split rows). Each result must equal the oracle's
 (identical -1 pattern, index set and value multiset), the split and unsplit
 calls must agree slot for slot, and a second call must repeat the first.
-Rows of at most 16384 scores also go through the BF16 entry point, compared
-with the oracle on the BF16-rounded values.
+Each case also runs once on a randomly forced path (clusters of 1 to 16,
+split rows, the short-row kernel, sampling on or off, the smallest candidate
+buffer). Rows of at most 16384 scores also go through the BF16 entry point,
+compared with the oracle on the BF16-rounded values.
 """
 
 import numpy as np
@@ -113,6 +115,42 @@ def test_random_case_through_the_automatic_path(case):
     torch.cuda.synchronize()
     assert torch.equal(got, again)
     assert torch.equal(got, unsplit)
+    assert_parity(scores, lengths, k, got.cpu().numpy(), want, page_table=pt)
+
+
+def _forced_options(case, B, stride, k):
+    """A random forced path for the case: the streaming kernel on clusters of
+    1 to 16, split rows, or the short-row kernel, with random sampling and
+    candidate-buffer capacity."""
+    rng = np.random.default_rng([0x5EED, 0xF023, case])
+    cap_max = 2560 if k <= 512 else 5120
+    caps = [c for c in (0, k + 2048, cap_max) if c == 0 or k + 2048 <= c <= cap_max]
+    opts = {"sample_mode": int(rng.integers(0, 3)), "stash_capacity": int(rng.choice(caps))}
+    kind = int(rng.integers(0, 3))
+    if kind == 2 and stride <= 16384:
+        return {"short_rows": 1, "sample_mode": opts["sample_mode"]}
+    opts["short_rows"] = -1
+    if kind == 1:
+        m = int(rng.integers(1, min(B, 1024) + 1))
+        opts["split_rows"] = m
+        opts["workspace"] = torch.zeros(tk.workspace_bytes(k, m), dtype=torch.uint8, device="cuda:0")
+    else:
+        opts["cluster_size"] = int(rng.choice([1, 2, 4, 8, 16]))
+    return opts
+
+
+@pytest.mark.parametrize("case", range(N_CASES))
+def test_random_case_on_a_forced_path(case):
+    scores, lengths, k, offset, pt, page_size = _case(case)
+    B, stride = scores.shape
+    opts = _forced_options(case, B, stride, k)
+    s, l = _device_rows(scores, offset), to_dev(lengths)
+    dpt = None if pt is None else to_dev(pt)
+    got = tk.topk_select_ex(s, l, k, dpt, page_size if pt is not None else 0, **opts)
+    torch.cuda.synchronize()
+    if "workspace" in opts:
+        assert not torch.any(opts["workspace"][:4096]), "arrival counters must be left at zero"
+    want = run_oracle(scores, lengths, k) if pt is None else run_oracle(scores, lengths, k, pt, page_size)
     assert_parity(scores, lengths, k, got.cpu().numpy(), want, page_table=pt)
 
 
