@@ -175,3 +175,46 @@ def test_random_case_in_bf16(case):
         want = run_oracle(vals, lengths, k, pt, page_size)
     torch.cuda.synchronize()
     assert_parity(vals, lengths, k, got.cpu().numpy(), want, page_table=pt)
+
+
+N_CHAIN_CASES = 16
+
+
+@pytest.mark.parametrize("case", range(N_CHAIN_CASES))
+def test_random_two_level_chain(case):
+    """Block keys (padded output rows), top-k over the keys, block table:
+    each step against the oracle's, bit for bit, on seeded random shapes."""
+    import oracle
+
+    rng = np.random.default_rng([0x5EED, 0xF024, case])
+    stride = int(np.exp(rng.uniform(np.log(8.0), np.log(70000.0))))
+    B = int(rng.integers(1, 201))
+    while B > 1 and B * stride > MAX_ELEMENTS // 2:
+        B //= 2
+    k_blocks = int(rng.choice([1, 17, 100, 512, 1000, 2048]))
+    lengths = _lengths(rng, int(rng.integers(0, 3)), B, stride, 8 * k_blocks)
+    lengths = np.clip(lengths, -2, stride + 20).astype(np.int32)
+    scores = np.full((B, stride), np.nan, dtype=np.float32)
+    for b in range(B):
+        n = int(min(max(lengths[b], 0), stride))
+        scores[b, :n] = _row_values(rng, int(rng.integers(0, 8)), n).astype(np.float32)
+    width = -(-stride // 8)
+    out_stride = width + int(rng.integers(0, 10))
+    init = np.full((B, out_stride), np.float32(-12345.5), dtype=np.float32)
+    page_size = int(rng.choice([8, 16, 64]))
+    bpp = page_size // 8
+    pt = rng.permutation(B * -(-width // bpp)).astype(np.int32).reshape(B, -1)
+    nb = -(-np.clip(lengths.astype(np.int64), 0, stride) // 8)
+    blen = nb.astype(np.int32)
+
+    keys = tk.amax8_varlen(to_dev(scores), to_dev(lengths), k_blocks, out=to_dev(init))
+    sel = tk.topk_ragged(keys, to_dev(blen), k_blocks)
+    pages = tk.sort_candidate_blocks(sel, to_dev(lengths), stride, to_dev(pt), page_size)
+    torch.cuda.synchronize()
+
+    want_keys = oracle.amax8_varlen(scores, lengths, k_blocks, init)
+    assert np.array_equal(keys.cpu().numpy().view(np.uint32), want_keys.view(np.uint32))
+    want_sel = oracle.topk_ragged(want_keys, blen, k_blocks)
+    want_ids, want_pages = oracle.sort_candidate_blocks(want_sel, lengths, stride, pt, page_size)
+    assert np.array_equal(sel.cpu().numpy(), want_ids)
+    assert np.array_equal(pages.cpu().numpy(), want_pages)
