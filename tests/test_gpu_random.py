@@ -1,7 +1,8 @@
 """Seeded random cases through the automatic dispatch (needs an sm_103 GPU).
 
 The other GPU tests force each path or run the fixed workloads; here every
-case draws a batch size, a row width (1 to 300000), k, a length mode, value
+case draws a batch size, a row width (1 to 300000), k, a length mode (full,
+80-100 %, anything, around k, up to 2k, up to k + 16384), value
 kinds with ties, infinities and signed zeros, a row start that may not sit on
 16 bytes, and paging, and lets the library choose its path (short-row kernel,
 sampled cutoff, clusters, split rows). Each result must equal the oracle's
@@ -28,7 +29,7 @@ if not torch.cuda.is_available():  # pragma: no cover - CPU-only machines
 
 import sparse_attention_indexer_fp32_gb300 as tk  # noqa: E402
 
-N_CASES = 64
+N_CASES = 96
 MAX_ELEMENTS = 12_000_000  # per case, so that the oracle's full sorts stay quick
 
 
@@ -64,7 +65,11 @@ def _lengths(rng, mode, B, width, k):
         return rng.integers(lo, width + 1, B)
     if mode == 2:
         return rng.integers(-2, width + 21, B)
-    return k + rng.integers(-1, 2, B)
+    if mode == 3:
+        return k + rng.integers(-1, 2, B)
+    if mode == 4:  # a little over k: split halves and cluster slices with few scores
+        return rng.integers(k + 1, 2 * k + 2, B)
+    return rng.integers(k + 1, k + 16385, B)  # around the sampled cutoff's gate
 
 
 def _case(i):
@@ -77,7 +82,7 @@ def _case(i):
     while B > 1 and B * width > MAX_ELEMENTS:
         B //= 2
     k = int(rng.choice([1, 2, 17, 100, 511, 512, 513, 1000, 1024, 2047, 2048, int(rng.integers(1, 2049))]))
-    lengths = _lengths(rng, int(rng.integers(0, 4)), B, width, k)
+    lengths = _lengths(rng, int(rng.integers(0, 6)), B, width, k)
     scores = np.full((B, width), np.nan, dtype=np.float32)
     for b in range(B):
         n = int(min(max(lengths[b], 0), width))
@@ -177,7 +182,7 @@ def test_random_case_in_bf16(case):
     assert_parity(vals, lengths, k, got.cpu().numpy(), want, page_table=pt)
 
 
-N_CHAIN_CASES = 16
+N_CHAIN_CASES = 24
 
 
 @pytest.mark.parametrize("case", range(N_CHAIN_CASES))
