@@ -158,3 +158,30 @@ def test_noalloc_without_scratch_paths(B, stride, k):
     rows = np.arange(0, B, max(1, B // 6))
     assert_parity(scores[rows], lengths[rows], k, got.cpu().numpy()[rows],
                   run_oracle(scores[rows], lengths[rows], k), rows=rows)
+
+
+@pytest.mark.parametrize("case", range(24))
+def test_noalloc_on_random_cases(case):
+    """The seeded random cases of the automatic-path tests (any batch, width,
+    k, length mode, row offset and paging) through the allocation-free entry
+    point: the regular call's output and the oracle's selection, or a refusal
+    that leaves the output untouched when the split rows need more scratch
+    than the array holds."""
+    import test_gpu_random as R
+
+    lib = tk.load_library()
+    scores, lengths, k, offset, pt, page_size = R._case(case)
+    s, l = R._device_rows(scores, offset), to_dev(lengths)
+    dpt = None if pt is None else to_dev(pt)
+    want = tk.topk_ragged(s, l, k) if pt is None else tk.topk_paged(s, l, k, dpt, page_size)
+    got = torch.full_like(want, -7)
+    status = _noalloc(lib, s, l, k, got, dpt, page_size if pt is not None else 0)
+    torch.cuda.synchronize()
+    if status == tk.Status.ESCRATCH:
+        assert torch.all(got == -7)
+        return
+    assert status == tk.Status.OK, lib.topk_status_string(status)
+    assert torch.equal(got, want)
+    assert_parity(scores, lengths, k, got.cpu().numpy(),
+                  run_oracle(scores, lengths, k) if pt is None else run_oracle(scores, lengths, k, pt, page_size),
+                  page_table=pt)
