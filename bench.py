@@ -966,7 +966,7 @@ def main(argv=None):
                          "topk_select_bf16 (profiling runs)")
     ap.add_argument("--sweep", action="store_true",
                     help="time every path over batch x width x k instead (dispatch sweep)")
-    ap.add_argument("--sweep-out", default="gpurun_out",
+    ap.add_argument("--sweep-out", default="sweep_out",
                     help="folder for the sweep's JSON and markdown summary")
     args = ap.parse_args(argv)
     if args.warmup < 3:
