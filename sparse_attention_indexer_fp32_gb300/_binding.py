@@ -119,13 +119,23 @@ def _check(status: int) -> None:
         raise TopkError(status, f"top-k call failed: {msg}")
 
 
-def _stream(device: torch.device, stream):
-    """The torch stream a call is enqueued on (default: the current one)."""
+def _stream(device, stream):
+    """The torch stream a call is enqueued on (default: the current one);
+    ``device`` a torch.device or a device index."""
     return torch.cuda.current_stream(device) if stream is None else stream
 
 
-def _stream_handle(device: torch.device, stream) -> int:
+def _stream_handle(device, stream) -> int:
     return int(_stream(device, stream).cuda_stream)
+
+
+def _on_device(index: int, fn):
+    """Runs ``fn`` with CUDA device ``index`` current (the library launches
+    on the current device), switching only when another one is current."""
+    if torch.cuda.current_device() == index:
+        return fn()
+    with torch.cuda.device(index):
+        return fn()
 
 
 def workspace_bytes(k: int = TOPK_MAX_K, max_split_rows: int = 0) -> int:
@@ -144,21 +154,26 @@ _workspaces = {}
 _ws_lock = threading.Lock()
 
 
-def _workspace(device: torch.device, stream) -> Optional[torch.Tensor]:
+def _workspace(device, stream) -> Optional[torch.Tensor]:
     """The cached workspace of this device and stream, created (and zeroed on
     that stream, so that the first call is ordered after the zeroing) on first
     use. None while the stream captures a CUDA graph and has no workspace yet:
     zeroing it inside the capture would run only at replay, so the call takes
-    the unsplit path instead (same results)."""
-    stream = _stream(device, stream)
-    key = (device.index, int(stream.cuda_stream))
+    the unsplit path instead (same results). ``device`` a torch.device or a
+    device index; ``stream`` a torch stream or None (the current one)."""
+    index = device if isinstance(device, int) else device.index
+    stream = _stream(index, stream)
+    key = (index, int(stream.cuda_stream))
+    ws = _workspaces.get(key)  # entries are only ever added
+    if ws is not None:
+        return ws
     with _ws_lock:
         ws = _workspaces.get(key)
         if ws is None:
             with torch.cuda.stream(stream):
                 if torch.cuda.is_current_stream_capturing():
                     return None
-                ws = torch.zeros(workspace_bytes(TOPK_MAX_K), dtype=torch.uint8, device=device)
+                ws = torch.zeros(workspace_bytes(TOPK_MAX_K), dtype=torch.uint8, device=index)
             _workspaces[key] = ws
     return ws
 
@@ -195,15 +210,18 @@ def topk_ragged(scores: torch.Tensor, lengths: torch.Tensor, k: int,
     outside a CUDA graph capture: a call captured before that runs unsplit."""
     lib = load_library()
     B, stride, out = _prepare(scores, lengths, k, out)
-    with torch.cuda.device(scores.device):
-        sh = _stream_handle(scores.device, stream)
-        ws = _workspace(scores.device, stream) if split else None
+    index = scores.get_device()
+    st = _stream(index, stream)
+    sh = int(st.cuda_stream)
+
+    def call():
+        ws = _workspace(index, st) if split else None
         if ws is not None:
-            _check(lib.topk_ragged_ws(scores.data_ptr(), stride, lengths.data_ptr(), B, k,
-                                      out.data_ptr(), ws.data_ptr(), ws.numel(), sh))
-        else:
-            _check(lib.topk_ragged(scores.data_ptr(), stride, lengths.data_ptr(), B, k,
-                                   out.data_ptr(), sh))
+            return lib.topk_ragged_ws(scores.data_ptr(), stride, lengths.data_ptr(), B, k,
+                                      out.data_ptr(), ws.data_ptr(), ws.numel(), sh)
+        return lib.topk_ragged(scores.data_ptr(), stride, lengths.data_ptr(), B, k, out.data_ptr(), sh)
+
+    _check(_on_device(index, call))
     return out
 
 
@@ -217,17 +235,20 @@ def topk_paged(scores: torch.Tensor, lengths: torch.Tensor, k: int, page_table: 
     if (page_table.dtype != torch.int32 or page_table.device != scores.device
             or page_table.dim() != 2 or page_table.shape[0] != B or not page_table.is_contiguous()):
         raise ValueError("page_table must be a contiguous int32 tensor [B, pages] on the scores' device")
-    with torch.cuda.device(scores.device):
-        sh = _stream_handle(scores.device, stream)
-        ws = _workspace(scores.device, stream) if split else None
+    index = scores.get_device()
+    st = _stream(index, stream)
+    sh = int(st.cuda_stream)
+
+    def call():
+        ws = _workspace(index, st) if split else None
         if ws is not None:
-            _check(lib.topk_paged_ws(scores.data_ptr(), stride, lengths.data_ptr(), B, k,
+            return lib.topk_paged_ws(scores.data_ptr(), stride, lengths.data_ptr(), B, k,
                                      page_table.data_ptr(), page_table.shape[1], page_size,
-                                     out.data_ptr(), ws.data_ptr(), ws.numel(), sh))
-        else:
-            _check(lib.topk_paged(scores.data_ptr(), stride, lengths.data_ptr(), B, k,
-                                  page_table.data_ptr(), page_table.shape[1], page_size,
-                                  out.data_ptr(), sh))
+                                     out.data_ptr(), ws.data_ptr(), ws.numel(), sh)
+        return lib.topk_paged(scores.data_ptr(), stride, lengths.data_ptr(), B, k,
+                              page_table.data_ptr(), page_table.shape[1], page_size, out.data_ptr(), sh)
+
+    _check(_on_device(index, call))
     return out
 
 
@@ -261,10 +282,11 @@ def topk_select_ex(scores: torch.Tensor, lengths: torch.Tensor, k: int,
     if counters is not None and (counters.numel() < NUM_COUNTERS or not counters.is_cuda
                                  or counters.element_size() != 4):
         raise ValueError("counters must be a 4-byte CUDA tensor of NUM_COUNTERS entries")
-    with torch.cuda.device(scores.device):
-        _check(lib.topk_select_ex(scores.data_ptr(), stride, lengths.data_ptr(), B, k, pt_ptr,
-                                  pt_stride, page_size, out.data_ptr(), ctypes.byref(opts),
-                                  _stream_handle(scores.device, stream)))
+    index = scores.get_device()
+    sh = _stream_handle(index, stream)
+    _check(_on_device(index, lambda: lib.topk_select_ex(scores.data_ptr(), stride, lengths.data_ptr(), B, k,
+                                                        pt_ptr, pt_stride, page_size, out.data_ptr(),
+                                                        ctypes.byref(opts), sh)))
     return out
 
 
@@ -292,10 +314,10 @@ def topk_select_bf16(scores: torch.Tensor, lengths: torch.Tensor, k: int,
                 or not page_table.is_contiguous()):
             raise ValueError("page_table must be a contiguous int32 tensor [B, pages]")
         pt_ptr, pt_stride = page_table.data_ptr(), page_table.shape[1]
-    with torch.cuda.device(scores.device):
-        _check(lib.topk_select_bf16(scores.data_ptr(), stride, lengths.data_ptr(), B, k, pt_ptr,
-                                    pt_stride, page_size, out.data_ptr(),
-                                    _stream_handle(scores.device, stream)))
+    index = scores.get_device()
+    sh = _stream_handle(index, stream)
+    _check(_on_device(index, lambda: lib.topk_select_bf16(scores.data_ptr(), stride, lengths.data_ptr(), B, k,
+                                                          pt_ptr, pt_stride, page_size, out.data_ptr(), sh)))
     return out
 
 
@@ -317,10 +339,10 @@ def amax8_varlen(scores: torch.Tensor, lengths: torch.Tensor, topk: int = 0,
     elif out.dtype != torch.float32 or out.device != scores.device or out.dim() != 2 \
             or out.shape[0] != B or out.stride(1) != 1:
         raise ValueError("out must be a float32 tensor [B, width] with unit inner stride")
-    with torch.cuda.device(scores.device):
-        _check(lib.topk_amax8_varlen(scores.data_ptr(), stride, lengths.data_ptr(), B, int(topk),
-                                     out.data_ptr(), out.stride(0),
-                                     _stream_handle(scores.device, stream)))
+    index = scores.get_device()
+    sh = _stream_handle(index, stream)
+    _check(_on_device(index, lambda: lib.topk_amax8_varlen(scores.data_ptr(), stride, lengths.data_ptr(), B,
+                                                           int(topk), out.data_ptr(), out.stride(0), sh)))
     return out
 
 
@@ -340,12 +362,11 @@ def sort_candidate_blocks(blocks: torch.Tensor, lengths: torch.Tensor, stride: i
         out_pages = torch.empty_like(blocks)
     if page_table.dtype != torch.int32 or not page_table.is_contiguous() or page_table.dim() != 2:
         raise ValueError("page_table must be a contiguous int32 tensor [B, pages]")
-    with torch.cuda.device(blocks.device):
-        _check(lib.topk_sort_candidate_blocks(blocks.data_ptr(), B, k, lengths.data_ptr(),
-                                              int(stride), page_table.data_ptr(),
-                                              page_table.shape[1], int(page_size),
-                                              out_pages.data_ptr(),
-                                              _stream_handle(blocks.device, stream)))
+    index = blocks.get_device()
+    sh = _stream_handle(index, stream)
+    _check(_on_device(index, lambda: lib.topk_sort_candidate_blocks(
+        blocks.data_ptr(), B, k, lengths.data_ptr(), int(stride), page_table.data_ptr(),
+        page_table.shape[1], int(page_size), out_pages.data_ptr(), sh)))
     return out_pages
 
 

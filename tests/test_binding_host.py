@@ -2,7 +2,8 @@
 calls pass to the library (one per device and stream, zeroed on the stream
 that uses it, never created inside a graph capture) and the entry point each
 call reaches. The CUDA runtime pieces the binding touches (current stream,
-stream context, capture status, device context) and the library are fakes
+stream context, capture status, current device and device context) and the
+library are fakes
 that record what they are asked; no kernel runs."""
 
 import contextlib
@@ -69,6 +70,7 @@ def fake_cuda(monkeypatch):
     monkeypatch.setattr(_binding.torch.cuda, "is_current_stream_capturing",
                         lambda: state["current"].capturing)
     monkeypatch.setattr(_binding.torch.cuda, "device", lambda d: contextlib.nullcontext())
+    monkeypatch.setattr(_binding.torch.cuda, "current_device", lambda: 0)
     monkeypatch.setattr(_binding.torch, "zeros", zeros)
     monkeypatch.setattr(_binding, "load_library", lambda path=None: lib)
     monkeypatch.setattr(_binding, "workspace_bytes", lambda k=2048, max_split_rows=0: 4096)
@@ -98,7 +100,7 @@ def test_default_call_gets_one_workspace_per_stream(fake_cuda):
     assert ws_ptrs[0] == ws_ptrs[1] != ws_ptrs[2]
     assert [c[1][-1] for c in lib.calls] == [100, 100, 200]
     assert [c[1][-2] for c in lib.calls] == [4096] * 3
-    assert set(_binding._workspaces) == {(None, 100), (None, 200)}
+    assert set(_binding._workspaces) == {(-1, 100), (-1, 200)}
 
 
 def test_workspace_is_zeroed_on_the_stream_that_uses_it(fake_cuda):
@@ -122,7 +124,7 @@ def test_capture_without_workspace_takes_the_unsplit_entry_point(fake_cuda):
         _binding.topk_paged(s, l, 8, pt, 64)
     assert [c[0] for c in lib.calls] == ["topk_ragged", "topk_paged"]
     assert state["zeroed_on"] == []
-    assert (None, 400) not in _binding._workspaces
+    assert (-1, 400) not in _binding._workspaces
     # once the capture has ended, the same stream gets its workspace
     capturing.capturing = False
     _binding.topk_ragged(s, l, 8, stream=capturing)
