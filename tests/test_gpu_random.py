@@ -223,3 +223,42 @@ def test_random_two_level_chain(case):
     want_ids, want_pages = oracle.sort_candidate_blocks(want_sel, lengths, stride, pt, page_size)
     assert np.array_equal(sel.cpu().numpy(), want_ids)
     assert np.array_equal(pages.cpu().numpy(), want_pages)
+
+
+@pytest.mark.parametrize("case", range(0, N_CASES, 6))
+def test_random_case_replayed_from_a_graph_with_new_lengths(case):
+    """The automatic call captured in a CUDA graph (its path fixed at capture
+    from B, the width and k), replayed after the lengths were rewritten in
+    place with another draw: the oracle's result for the new lengths."""
+    scores, lengths, k, offset, pt, page_size = _case(case)
+    B, width = scores.shape
+    rng = np.random.default_rng([0x5EED, 0xF025, case])
+    new_lengths = _lengths(rng, int(rng.integers(0, 6)), B, width, k)
+    new_lengths = np.clip(new_lengths, -2, width + 20).astype(np.int32)
+    full = np.asarray(scores, dtype=np.float32).copy()
+    for b in range(B):  # valid scores wherever either draw reads
+        n = int(min(max(max(lengths[b], new_lengths[b]), 0), width))
+        holes = np.isnan(full[b, :n])
+        full[b, :n][holes] = rng.standard_normal(int(holes.sum())).astype(np.float32)
+    s, l = _device_rows(full, offset), to_dev(lengths)
+    dpt = None if pt is None else to_dev(pt)
+    out = torch.empty((B, k), dtype=torch.int32, device="cuda:0")
+    stream = torch.cuda.Stream()
+
+    def call():
+        if dpt is None:
+            tk.topk_ragged(s, l, k, out=out)
+        else:
+            tk.topk_paged(s, l, k, dpt, page_size, out=out)
+
+    with torch.cuda.stream(stream):
+        call()  # creates the stream's workspace outside the capture
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            call()
+        l.copy_(torch.from_numpy(new_lengths))
+        graph.replay()
+        stream.synchronize()
+    want = run_oracle(full, new_lengths, k) if pt is None else run_oracle(full, new_lengths, k, pt, page_size)
+    assert_parity(full, new_lengths, k, out.cpu().numpy(), want, page_table=pt)
