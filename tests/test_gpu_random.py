@@ -29,70 +29,7 @@ if not torch.cuda.is_available():  # pragma: no cover - CPU-only machines
 
 import sparse_attention_indexer_fp32_gb300 as tk  # noqa: E402
 
-N_CASES = 96
-MAX_ELEMENTS = 12_000_000  # per case, so that the oracle's full sorts stay quick
-
-
-def _row_values(rng, kind, width):
-    if kind == 0:
-        return rng.standard_normal(width)
-    if kind == 1:  # an offset, as in the decode workload
-        return rng.standard_normal(width) + rng.uniform(-4, 4)
-    if kind == 2:  # few distinct values: ties at every cutoff
-        return rng.integers(-3, 4, width).astype(np.float64) * 0.25
-    if kind == 3:  # infinities and signed zeros over N(0,1)
-        x = rng.standard_normal(width)
-        pick = rng.integers(0, 8, width)
-        x[pick == 0] = np.inf
-        x[pick == 1] = -np.inf
-        x[pick == 2] = -0.0
-        x[pick == 3] = 0.0
-        return x
-    if kind == 4:
-        return np.arange(width, dtype=np.float64)
-    if kind == 5:
-        return -np.arange(width, dtype=np.float64)
-    if kind == 6:
-        return np.full(width, rng.standard_normal())
-    return np.where(rng.random(width) < 0.01, rng.uniform(3, 6, width), 0.0) + rng.standard_normal(width)
-
-
-def _lengths(rng, mode, B, width, k):
-    if mode == 0:
-        return np.full(B, width, dtype=np.int64)
-    if mode == 1:
-        lo = (8 * width + 9) // 10
-        return rng.integers(lo, width + 1, B)
-    if mode == 2:
-        return rng.integers(-2, width + 21, B)
-    if mode == 3:
-        return k + rng.integers(-1, 2, B)
-    if mode == 4:  # a little over k: split halves and cluster slices with few scores
-        return rng.integers(k + 1, 2 * k + 2, B)
-    return rng.integers(k + 1, k + 16385, B)  # around the sampled cutoff's gate
-
-
-def _case(i):
-    rng = np.random.default_rng([0x5EED, 0xF022, i])
-    if rng.random() < 0.3:  # long rows: the sampled cutoff, clusters and split rows
-        width = int(rng.integers(65536, 300001))
-    else:
-        width = int(np.exp(rng.uniform(0.0, np.log(300000.0))))
-    B = int(np.exp(rng.uniform(0.0, np.log(1200.0))))
-    while B > 1 and B * width > MAX_ELEMENTS:
-        B //= 2
-    k = int(rng.choice([1, 2, 17, 100, 511, 512, 513, 1000, 1024, 2047, 2048, int(rng.integers(1, 2049))]))
-    lengths = _lengths(rng, int(rng.integers(0, 6)), B, width, k)
-    scores = np.full((B, width), np.nan, dtype=np.float32)
-    for b in range(B):
-        n = int(min(max(lengths[b], 0), width))
-        scores[b, :n] = _row_values(rng, int(rng.integers(0, 8)), n).astype(np.float32)
-    offset = int(rng.integers(0, 4))  # floats before row 0 in the device buffer
-    paged = bool(rng.integers(0, 2))
-    page_size = int(rng.choice([1, 7, 16, 64]))
-    pages = -(-width // page_size)
-    pt = rng.permutation(B * pages).astype(np.int32).reshape(B, pages) if paged else None
-    return scores, np.clip(lengths, -2**31, 2**31 - 1).astype(np.int32), k, offset, pt, page_size
+from random_cases import MAX_ELEMENTS, N_CASES, draw_case, draw_lengths, row_values  # noqa: E402
 
 
 def _device_rows(scores, offset):
@@ -104,7 +41,7 @@ def _device_rows(scores, offset):
 
 @pytest.mark.parametrize("case", range(N_CASES))
 def test_random_case_through_the_automatic_path(case):
-    scores, lengths, k, offset, pt, page_size = _case(case)
+    scores, lengths, k, offset, pt, page_size = draw_case(case)
     s, l = _device_rows(scores, offset), to_dev(lengths)
     if pt is None:
         got = tk.topk_ragged(s, l, k)
@@ -146,7 +83,7 @@ def _forced_options(case, B, stride, k):
 
 @pytest.mark.parametrize("case", range(N_CASES))
 def test_random_case_on_a_forced_path(case):
-    scores, lengths, k, offset, pt, page_size = _case(case)
+    scores, lengths, k, offset, pt, page_size = draw_case(case)
     B, stride = scores.shape
     opts = _forced_options(case, B, stride, k)
     s, l = _device_rows(scores, offset), to_dev(lengths)
@@ -161,7 +98,7 @@ def test_random_case_on_a_forced_path(case):
 
 @pytest.mark.parametrize("case", range(N_CASES))
 def test_random_case_in_bf16(case):
-    scores, lengths, k, offset, pt, page_size = _case(case)
+    scores, lengths, k, offset, pt, page_size = draw_case(case)
     if scores.shape[1] > 16384:
         pytest.skip("BF16 rows hold at most 16384 scores")
     bits = to_bf16_bits(scores)
@@ -197,12 +134,12 @@ def test_random_two_level_chain(case):
     while B > 1 and B * stride > MAX_ELEMENTS // 2:
         B //= 2
     k_blocks = int(rng.choice([1, 17, 100, 512, 1000, 2048]))
-    lengths = _lengths(rng, int(rng.integers(0, 3)), B, stride, 8 * k_blocks)
+    lengths = draw_lengths(rng, int(rng.integers(0, 3)), B, stride, 8 * k_blocks)
     lengths = np.clip(lengths, -2, stride + 20).astype(np.int32)
     scores = np.full((B, stride), np.nan, dtype=np.float32)
     for b in range(B):
         n = int(min(max(lengths[b], 0), stride))
-        scores[b, :n] = _row_values(rng, int(rng.integers(0, 8)), n).astype(np.float32)
+        scores[b, :n] = row_values(rng, int(rng.integers(0, 8)), n).astype(np.float32)
     width = -(-stride // 8)
     out_stride = width + int(rng.integers(0, 10))
     init = np.full((B, out_stride), np.float32(-12345.5), dtype=np.float32)
@@ -230,10 +167,10 @@ def test_random_case_replayed_from_a_graph_with_new_lengths(case):
     """The automatic call captured in a CUDA graph (its path fixed at capture
     from B, the width and k), replayed after the lengths were rewritten in
     place with another draw: the oracle's result for the new lengths."""
-    scores, lengths, k, offset, pt, page_size = _case(case)
+    scores, lengths, k, offset, pt, page_size = draw_case(case)
     B, width = scores.shape
     rng = np.random.default_rng([0x5EED, 0xF025, case])
-    new_lengths = _lengths(rng, int(rng.integers(0, 6)), B, width, k)
+    new_lengths = draw_lengths(rng, int(rng.integers(0, 6)), B, width, k)
     new_lengths = np.clip(new_lengths, -2, width + 20).astype(np.int32)
     full = np.asarray(scores, dtype=np.float32).copy()
     for b in range(B):  # valid scores wherever either draw reads

@@ -168,9 +168,10 @@ def test_noalloc_on_random_cases(case):
     that leaves the output untouched when the split rows need more scratch
     than the array holds."""
     import test_gpu_random as R
+    from random_cases import draw_case
 
     lib = tk.load_library()
-    scores, lengths, k, offset, pt, page_size = R._case(case)
+    scores, lengths, k, offset, pt, page_size = draw_case(case)
     s, l = R._device_rows(scores, offset), to_dev(lengths)
     dpt = None if pt is None else to_dev(pt)
     want = tk.topk_ragged(s, l, k) if pt is None else tk.topk_paged(s, l, k, dpt, page_size)
