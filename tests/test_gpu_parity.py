@@ -287,6 +287,24 @@ def test_unaligned_rows(offset):
         assert_parity(host, lengths, k, out.cpu().numpy(), run_oracle(host, lengths, k))
 
 
+@pytest.mark.parametrize("width,B", [(2000003, 3), (1 << 24, 1)])
+@pytest.mark.parametrize("k", [512, 2048])
+def test_very_wide_rows(width, B, k):
+    """Rows far wider than the workloads' (2,000,003 scores, odd; 2^24
+    scores): the index arithmetic of every stage, sample and page-table
+    lookup, on the automatic path (clusters of 16 for so few rows), ragged
+    and paged."""
+    rng = np.random.default_rng(width + k)
+    scores = rng.standard_normal((B, width)).astype(np.float32)
+    scores[:, width // 3] = np.inf  # one clear maximum far into the row
+    lengths = np.array([width, width - 5, width // 2][:B], dtype=np.int32)
+    check_against_oracle(scores, lengths, k)
+    ps = 64
+    pages = -(-width // ps)
+    pt = rng.permutation(B * pages).astype(np.int32).reshape(B, pages)
+    check_against_oracle(scores, lengths, k, pt, ps)
+
+
 @pytest.mark.parametrize("k", [1, 2, 3, 100, 511, 513, 2047])
 def test_other_k_values(k):
     w = make_rows(5, list(range(0, 128, 5)))
