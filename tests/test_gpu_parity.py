@@ -305,6 +305,17 @@ def test_very_wide_rows(width, B, k):
     check_against_oracle(scores, lengths, k, pt, ps)
 
 
+@pytest.mark.parametrize("B,width,k", [(300000, 5, 3), (70000, 40, 17), (5000, 20000, 512)])
+def test_large_batches(B, width, k):
+    """Many rows: a grid of hundreds of thousands of CTAs on the short-row
+    kernel, and thousands of rows just past its width on the streaming
+    kernel (several waves, the split tail), ragged."""
+    rng = np.random.default_rng(B + width)
+    scores = rng.standard_normal((B, width)).astype(np.float32)
+    lengths = rng.integers(-1, width + 2, B).astype(np.int32)
+    check_against_oracle(scores, lengths, k)
+
+
 @pytest.mark.parametrize("k", [1, 2, 3, 100, 511, 513, 2047])
 def test_other_k_values(k):
     w = make_rows(5, list(range(0, 128, 5)))
