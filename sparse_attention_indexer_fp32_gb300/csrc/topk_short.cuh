@@ -331,10 +331,9 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? (KMAX <= 1024 ? 5 : 4) : 3
     }
   }
   const bool full = aligned && wbase + CH <= n;  // warp-uniform
-  for (int i = t; i < kBins / 4; i += kThreads) {
-    reinterpret_cast<uint4*>(S.hist)[i] = make_uint4(0, 0, 0, 0);
-    reinterpret_cast<uint4*>(S.hist2)[i] = make_uint4(0, 0, 0, 0);
-  }
+  // (S.hist2 needs no clearing here: the coarse search clears it while it
+  // reads S.hist, before anything adds into it.)
+  for (int i = t; i < kBins / 4; i += kThreads) reinterpret_cast<uint4*>(S.hist)[i] = make_uint4(0, 0, 0, 0);
   if (t < 64) S.sum64[t] = 0;
   __syncthreads();
 
@@ -390,10 +389,6 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? (KMAX <= 1024 ? 5 : 4) : 3
     for (int q = 0; q < NQ; ++q) wt += SlabScan<NQ, V>::field(sc.tot, q);
     uint32_t before, total;
     warp_prefix(wt, before, total);  // total == above + inbin
-    // Every warp is past its coarse search, which left S.hist as it was:
-    // clear it for a third pass.
-    reinterpret_cast<uint4*>(&S.hist[8 * t])[0] = make_uint4(0, 0, 0, 0);
-    reinterpret_cast<uint4*>(&S.hist[8 * t])[1] = make_uint4(0, 0, 0, 0);
     uint32_t vbase = before;  // the warp's hits in the vectors before q
 #pragma unroll
     for (int q = 0; q < NQ; ++q) {
@@ -433,6 +428,11 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? (KMAX <= 1024 ? 5 : 4) : 3
     if (rem == inbin) {
       cut = Cut{10, p2, rem, true};
     } else {
+      // S.hist still holds the coarse counts: clear it for this third pass
+      // (every warp is past the search that read it).
+      reinterpret_cast<uint4*>(&S.hist[8 * t])[0] = make_uint4(0, 0, 0, 0);
+      reinterpret_cast<uint4*>(&S.hist[8 * t])[1] = make_uint4(0, 0, 0, 0);
+      __syncthreads();
       short_stash_hist(S, S.hist, static_cast<int>(total), 10, p2, 0, 0x3ff);
       const uint32_t b3 = find_bin_all<4>(S, S.hist, S.hist2, rem, &above, &inbin);
       rem -= above;

@@ -156,10 +156,8 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? 6 : 4) topk_short_bf16_ker
       kw[i] = bf16x2_keys(lo | (hi << 16)) & ((i0 < n ? 0x0000ffffu : 0u) | (i1 < n ? 0xffff0000u : 0u));
     }
   }
-  for (int i = t; i < kBins / 4; i += kThreads) {
-    reinterpret_cast<uint4*>(S.hist)[i] = make_uint4(0, 0, 0, 0);
-    reinterpret_cast<uint4*>(S.hist2)[i] = make_uint4(0, 0, 0, 0);
-  }
+  // (S.hist2 is cleared by the coarse search, which reads S.hist.)
+  for (int i = t; i < kBins / 4; i += kThreads) reinterpret_cast<uint4*>(S.hist)[i] = make_uint4(0, 0, 0, 0);
   __syncthreads();
 
   int grp = 0;
