@@ -238,14 +238,21 @@ __device__ __forceinline__ void hist_inc(uint32_t* hist, HistDst<G> d, uint32_t 
 // Locates the bin holding the target-th largest element (1 <= target <= total).
 // Thread t owns BPT consecutive bins, given in DESCENDING bin order in c[].
 // Returns the bin; *above = elements in higher bins; *inbin = elements in it.
+// With `zero_own`, each thread also clears the BPT/4 vectors of its own bins
+// there, after the scan (stores ahead of the scan's shuffles delayed it) and
+// before the last barrier (the next histogram adds into them after it).
 template <int BPT, class SM>
 __device__ uint32_t find_bin(const uint32_t (&c)[BPT], uint32_t target, SM& S,
-                             uint32_t* above, uint32_t* inbin) {
+                             uint32_t* above, uint32_t* inbin, uint4* zero_own = nullptr) {
   constexpr int nbins = BPT * kThreads;
   uint32_t s = 0;
 #pragma unroll
   for (int i = 0; i < BPT; ++i) s += c[i];
   const uint32_t incl = block_incl_scan(s, S);
+  if (zero_own != nullptr) {
+#pragma unroll
+    for (int q = 0; q < BPT / 4; ++q) zero_own[q] = make_uint4(0, 0, 0, 0);
+  }
   uint32_t acc = incl - s;
   if (acc < target && target <= incl) {
 #pragma unroll
@@ -280,13 +287,12 @@ __device__ uint32_t merged_find(SM& S, uint32_t target, uint32_t* above, uint32_
 #pragma unroll
     for (int q = 0; q < BPT; q += 4) {
       const uint4 v = h4[q / 4];
-      h4[q / 4] = make_uint4(0, 0, 0, 0);
       c[BPT - 1 - q] = v.x;
       c[BPT - 2 - q] = v.y;
       c[BPT - 3 - q] = v.z;
       c[BPT - 4 - q] = v.w;
     }
-    return find_bin<BPT>(c, target, S, above, inbin);
+    return find_bin<BPT>(c, target, S, above, inbin, h4);  // zeroes these bins
   };
   if constexpr (G == 1) {
     __syncthreads();

@@ -77,11 +77,13 @@ struct ShortSmem {
 // sums the BPT consecutive bins it owns, and after the second barrier every
 // warp locates, from the warp totals and the per-thread sums, the thread and
 // then the bin that holds the target, by itself. The bins are left as they
-// are: each thread instead zeroes its own bins of `other`, the buffer of the
-// previous search, which every warp finished reading before the first
-// barrier and which the next histogram fills after the second. Returns the
-// bin; *above = elements in higher bins; *inbin = elements in it.
-template <int BPT, class SM>
+// are. With ClearOther each thread also zeroes its own bins of `other`, the
+// buffer of the previous search, which every warp finished reading before
+// the first barrier and which the next histogram fills after the second;
+// without it the caller clears `other` itself, off this search's path (the
+// coarse search: its stores there delayed the scan, ~3 % of the kernel).
+// Returns the bin; *above = elements in higher bins; *inbin = elements in it.
+template <int BPT, bool ClearOther = true, class SM>
 __device__ uint32_t find_bin_all(SM& S, const uint32_t* hist, uint32_t* other, uint32_t target,
                                  uint32_t* above, uint32_t* inbin) {
   constexpr int nbins = BPT * kThreads;
@@ -95,8 +97,10 @@ __device__ uint32_t find_bin_all(SM& S, const uint32_t* hist, uint32_t* other, u
     sum += v.x + v.y + v.z + v.w;
   }
   // (all 2048 bins of the other buffer, whatever this search's bin count)
-  reinterpret_cast<uint4*>(&other[kBins - 8 * (t + 1)])[0] = make_uint4(0, 0, 0, 0);
-  reinterpret_cast<uint4*>(&other[kBins - 8 * (t + 1)])[1] = make_uint4(0, 0, 0, 0);
+  if constexpr (ClearOther) {
+    reinterpret_cast<uint4*>(&other[kBins - 8 * (t + 1)])[0] = make_uint4(0, 0, 0, 0);
+    reinterpret_cast<uint4*>(&other[kBins - 8 * (t + 1)])[1] = make_uint4(0, 0, 0, 0);
+  }
   const uint32_t incl = warp_incl_scan(sum);
   S.tincl[t] = incl;
   if (lane == 31) S.scan[w] = incl;
@@ -331,8 +335,7 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? (KMAX <= 1024 ? 5 : 4) : 3
     }
   }
   const bool full = aligned && wbase + CH <= n;  // warp-uniform
-  // (S.hist2 needs no clearing here: the coarse search clears it while it
-  // reads S.hist, before anything adds into it.)
+  // (S.hist2 is cleared later, by each path before it adds into it.)
   for (int i = t; i < kBins / 4; i += kThreads) reinterpret_cast<uint4*>(S.hist)[i] = make_uint4(0, 0, 0, 0);
   if (t < 64) S.sum64[t] = 0;
   __syncthreads();
@@ -363,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? (KMAX <= 1024 ? 5 : 4) : 3
     for (int j = 0; j < E; ++j) hist_add(S.hist, ((valid[j / 32] >> (j % 32)) & 1u) ? (key[j] >> 21) : 0xffffffffu);
   }
   // Searches alternate between the two buffers: S.hist, S.hist2, S.hist.
-  const uint32_t b1 = find_bin_all<8>(S, S.hist, S.hist2, kk, &above, &inbin);
+  const uint32_t b1 = find_bin_all<8, false>(S, S.hist, S.hist2, kk, &above, &inbin);
   uint32_t rem = kk - above;
   Cut cut;
   if (rem == inbin) {
@@ -408,8 +411,10 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? (KMAX <= 1024 ? 5 : 4) : 3
       const int p1 = (n + p.page_size - 1) / p.page_size;
       for (int q = 32 * t; q < p1; q += 32 * kThreads) prefetch_l2(pt_row + q);
     }
+    reinterpret_cast<uint4*>(&S.hist2[8 * t])[0] = make_uint4(0, 0, 0, 0);  // for the second pass
+    reinterpret_cast<uint4*>(&S.hist2[8 * t])[1] = make_uint4(0, 0, 0, 0);
     // ---- 3. the exact cutoff inside bin b1 (its entries only), emission -------
-    __syncthreads();  // the stash is complete
+    __syncthreads();  // the stash is complete, the second histogram clear
     for (int base0 = 0; base0 < static_cast<int>(total); base0 += kRoundEntries) {
       const int base = base0 + kRoundPerThread * t;
       uint32_t kv[kRoundPerThread];
@@ -445,6 +450,9 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? (KMAX <= 1024 ? 5 : 4) : 3
     return;
   } else {
     // ---- 4. exact register path: the finer passes over the registers --------
+    reinterpret_cast<uint4*>(&S.hist2[8 * t])[0] = make_uint4(0, 0, 0, 0);
+    reinterpret_cast<uint4*>(&S.hist2[8 * t])[1] = make_uint4(0, 0, 0, 0);
+    __syncthreads();
 #pragma unroll
     for (int j = 0; j < E; ++j) {
       const bool ok = ((valid[j / 32] >> (j % 32)) & 1u) && (key[j] >> 21) == b1;

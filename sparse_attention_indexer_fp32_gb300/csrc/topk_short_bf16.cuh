@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? 6 : 4) topk_short_bf16_ker
       kw[i] = bf16x2_keys(lo | (hi << 16)) & ((i0 < n ? 0x0000ffffu : 0u) | (i1 < n ? 0xffff0000u : 0u));
     }
   }
-  // (S.hist2 is cleared by the coarse search, which reads S.hist.)
+  // (S.hist2 is cleared later, by each path before it adds into it.)
   for (int i = t; i < kBins / 4; i += kThreads) reinterpret_cast<uint4*>(S.hist)[i] = make_uint4(0, 0, 0, 0);
   __syncthreads();
 
@@ -181,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? 6 : 4) topk_short_bf16_ker
     atomicAdd(&S.hist[(kw[i] >> 5) & 0x7ffu], 1u);
     atomicAdd(&S.hist[kw[i] >> 21], 1u);
   }
-  const uint32_t b1 = find_bin_all<8>(S, S.hist, S.hist2, kk, &above, &inbin);
+  const uint32_t b1 = find_bin_all<8, false>(S, S.hist, S.hist2, kk, &above, &inbin);
   uint32_t rem = kk - above;
   Cut cut;
   if (rem == inbin) {
@@ -226,6 +226,7 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? 6 : 4) topk_short_bf16_ker
       const int p1 = (n + p.page_size - 1) / p.page_size;
       for (int q = 32 * t; q < p1; q += 32 * kThreads) prefetch_l2(pt_row + q);
     }
+    if (t < 8) reinterpret_cast<uint4*>(&S.hist2[4 * t])[0] = make_uint4(0, 0, 0, 0);
     // ---- 3. fine pass: low 5 bits of the b1 entries, then emission ------------
     __syncthreads();
     const int nt = static_cast<int>(total);
@@ -284,6 +285,8 @@ __global__ void __launch_bounds__(kThreads, E <= 32 ? 6 : 4) topk_short_bf16_ker
     return;
   } else {
     // ---- 4. register path: the fine pass over the registers ---------------------
+    if (t < 8) reinterpret_cast<uint4*>(&S.hist2[4 * t])[0] = make_uint4(0, 0, 0, 0);
+    __syncthreads();
 #pragma unroll
     for (int i = 0; i < NKW; ++i) {
 #pragma unroll
